@@ -1,0 +1,506 @@
+// capi.cu -- the C ABI (include/moe_gb300.h): argument checks, workspace
+// layout, the order of kernels behind each entry point, launch counting and
+// per-kernel event profiling.
+#include "common.cuh"
+
+#include <atomic>
+#include <mutex>
+#include <string>
+#include <vector>
+#include <map>
+#include <cstdio>
+#include <cstring>
+
+namespace moe {
+
+// ---------------------------------------------------------------- launch bookkeeping
+namespace {
+std::atomic<uint64_t> g_launches{0};
+std::atomic<bool> g_profile{false};
+
+struct ProfRecord {
+    const char *name;
+    cudaEvent_t start, stop;
+};
+std::mutex g_prof_mu;
+std::vector<ProfRecord> g_records;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t take_event() {
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+}  // namespace
+
+int launch_begin(const char *name, cudaStream_t stream) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (!g_profile.load(std::memory_order_relaxed)) return -1;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    ProfRecord r{name, take_event(), take_event()};
+    cudaEventRecord(r.start, stream);
+    g_records.push_back(r);
+    return (int)g_records.size() - 1;
+}
+
+void launch_end(int token, cudaStream_t stream) {
+    if (token < 0) return;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (token < (int)g_records.size()) cudaEventRecord(g_records[token].stop, stream);
+}
+
+int num_sms() {
+    static int cached[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (cached[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = n > 0 ? n : 1;
+    }
+    return cached[dev];
+}
+
+// ---------------------------------------------------------------- shapes and layouts
+int64_t route_chunks(const moe_shape &s) {
+    if (s.num_tokens == 0) return 0;
+    const int64_t M = s.num_tokens / s.num_partitions;
+    return s.num_partitions * ((M + kRouteChunkTokens - 1) / kRouteChunkTokens);
+}
+
+moe_status check_shape(const moe_shape *s, bool need_ffn) {
+    if (!s) return MOE_ERR_NULLPTR;
+    if (s->num_tokens < 0 || s->num_partitions < 1 || s->num_tokens % s->num_partitions != 0)
+        return MOE_ERR_SHAPE;
+    if (s->hidden < 8 || s->hidden % 8 != 0) return MOE_ERR_SHAPE;
+    if (s->num_experts < 1 || s->num_experts > kMaxExperts) return MOE_ERR_SHAPE;
+    if (s->topk < 1 || s->topk > kMaxTopK) return MOE_ERR_SHAPE;
+    if (s->mask_kind < 0 || s->mask_kind > 2) return MOE_ERR_PARAM_INVALID;
+    if (s->has_shared != 0 && s->has_shared != 1) return MOE_ERR_PARAM_INVALID;
+    const int64_t cap = s->num_tokens * s->topk;
+    if (cap > INT32_MAX) return MOE_ERR_SHAPE;
+    if (need_ffn) {
+        if (s->ffn <= 0 || s->ffn % 256 != 0 || s->ffn > 8192) return MOE_ERR_SHAPE;
+        if (s->hidden % 16 != 0 || s->hidden > 8192) return MOE_ERR_SHAPE;
+    } else if (s->ffn < 0) {
+        return MOE_ERR_SHAPE;
+    }
+    return MOE_OK;
+}
+
+Layout layout_for(const moe_shape &s, Op op) {
+    Layout L;
+    const int64_t T = s.num_tokens, K = s.topk, E = s.num_experts, H = s.hidden, P = s.num_partitions;
+    const int64_t cap = T * K, Nh = s.ffn / 2;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = off;
+        off = align_up(off + (bytes ? bytes : 1), kAlign);
+        return at;
+    };
+    L.status = take(4);
+    if (op == Op::Dispatch || op == Op::Layer) {
+        const int64_t C = route_chunks(s);
+        L.hist = take((size_t)(C * E + C) * sizeof(int32_t));
+    }
+    if (op == Op::Ffn || op == Op::Layer) L.sched = take((size_t)(E + 1) * sizeof(int32_t));
+    if (op == Op::Layer) {
+        L.route_row = take((size_t)cap * sizeof(int32_t));
+        L.assist = take((size_t)cap * 3 * sizeof(int32_t));
+        L.offsets = take((size_t)(E + 1) * sizeof(int32_t));
+        L.counts = take((size_t)E * sizeof(int64_t));
+        L.recv_cum = take((size_t)(E * P) * sizeof(int32_t));
+    }
+    if (op == Op::Ffn || op == Op::Layer) {
+        L.q1 = take((size_t)cap * H * 2);
+        L.s1 = take((size_t)cap * sizeof(float));
+        L.g = take((size_t)cap * Nh * sizeof(float));
+        L.q2 = take((size_t)cap * Nh * 2);
+        L.s2 = take((size_t)cap * sizeof(float));
+    }
+    if (op == Op::Layer) L.y = take((size_t)cap * H * 2);
+    L.total = off;
+    return L;
+}
+
+static bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+template <typename T>
+static T *at(void *ws, size_t off) {
+    return reinterpret_cast<T *>(reinterpret_cast<uint8_t *>(ws) + off);
+}
+
+static RouteDev route_dev(const moe_shape &s, const int32_t *ids, const uint8_t *mask, void *ws,
+                          const Layout &L) {
+    RouteDev r;
+    r.ids = ids;
+    r.mask = mask;
+    r.mask_kind = s.mask_kind;
+    r.T = s.num_tokens;
+    r.P = s.num_partitions;
+    r.M = s.num_tokens / s.num_partitions;
+    r.K = s.topk;
+    r.E = s.num_experts;
+    r.chunks_per_partition = (r.M + kRouteChunkTokens - 1) / kRouteChunkTokens;
+    if (r.chunks_per_partition == 0) r.chunks_per_partition = 1;
+    const int64_t C = route_chunks(s);
+    r.hist = at<int32_t>(ws, L.hist);
+    r.bad = r.hist + C * s.num_experts;
+    r.status = at<int32_t>(ws, L.status);
+    return r;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+// ====================================================================== C ABI
+extern "C" {
+
+const char *moe_status_string(moe_status st) {
+    switch (st) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_NULLPTR: return "required pointer is NULL";
+        case MOE_ERR_PARAM_INVALID: return "argument value out of range";
+        case MOE_ERR_SHAPE: return "shape not supported";
+        case MOE_ERR_WORKSPACE: return "workspace too small";
+        case MOE_ERR_ALIGNMENT: return "pointer misaligned";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_UNSUPPORTED: return "unsupported device";
+    }
+    return "unknown status";
+}
+
+uint64_t moe_launch_count(void) { return g_launches.load(); }
+
+moe_status moe_profile_enable(int on) {
+    g_profile.store(on != 0);
+    return MOE_OK;
+}
+
+moe_status moe_profile_report(char *buf, size_t bytes) {
+    if (!buf || bytes == 0) return MOE_ERR_NULLPTR;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    std::map<std::string, std::pair<int, double>> agg;
+    std::vector<std::string> order;
+    for (auto &r : g_records) {
+        float ms = 0.0f;
+        if (cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess) ms = -1.0f;
+        auto it = agg.find(r.name);
+        if (it == agg.end()) {
+            order.push_back(r.name);
+            agg[r.name] = {1, (double)ms};
+        } else {
+            it->second.first += 1;
+            it->second.second += ms;
+        }
+        g_event_pool.push_back(r.start);
+        g_event_pool.push_back(r.stop);
+    }
+    g_records.clear();
+    cudaGetLastError();
+    std::string out;
+    char line[256];
+    for (auto &n : order) {
+        snprintf(line, sizeof line, "%s %d %.6f\n", n.c_str(), agg[n].first, agg[n].second);
+        out += line;
+    }
+    if (out.size() + 1 > bytes) return MOE_ERR_PARAM_INVALID;
+    memcpy(buf, out.c_str(), out.size() + 1);
+    return MOE_OK;
+}
+
+moe_status moe_read_device_status(void *workspace, cudaStream_t stream, int32_t *status_host) {
+    if (!workspace || !status_host) return MOE_ERR_NULLPTR;
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(workspace, 0, sizeof v, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+    *status_host = v;
+    return MOE_OK;
+}
+
+// ---------------------------------------------------------------- dispatch
+moe_status moe_dispatch_workspace_size(const moe_shape *shape, size_t *bytes) {
+    MOE_TRY(check_shape(shape, false));
+    if (!bytes) return MOE_ERR_NULLPTR;
+    *bytes = layout_for(*shape, Op::Dispatch).total;
+    return MOE_OK;
+}
+
+moe_status moe_dispatch(const moe_shape *shape, const void *x, const int32_t *expert_ids,
+                        const uint8_t *x_active_mask, void *expand_x, int32_t *assist,
+                        int64_t *expert_token_nums, int32_t *expert_offsets,
+                        int32_t *ep_recv_counts, int32_t *route_row, void *workspace,
+                        size_t workspace_bytes, cudaStream_t stream) {
+    MOE_TRY(check_shape(shape, false));
+    const moe_shape &s = *shape;
+    if (!expert_ids || !assist || !expert_token_nums || !expert_offsets || !ep_recv_counts ||
+        !route_row || !workspace)
+        return MOE_ERR_NULLPTR;
+    if (expand_x && !x) return MOE_ERR_NULLPTR;
+    if (s.mask_kind != 0 && !x_active_mask) return MOE_ERR_NULLPTR;
+    if (s.mask_kind == 0 && x_active_mask) return MOE_ERR_PARAM_INVALID;
+    if ((expand_x && (!aligned(x, 16) || !aligned(expand_x, 16))) || !aligned(workspace, kAlign))
+        return MOE_ERR_ALIGNMENT;
+    if (!aligned(expert_ids, 4) || !aligned(assist, 4) || !aligned(expert_token_nums, 8) ||
+        !aligned(expert_offsets, 4) || !aligned(ep_recv_counts, 4) || !aligned(route_row, 4))
+        return MOE_ERR_ALIGNMENT;
+    const Layout L = layout_for(s, Op::Dispatch);
+    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+    RouteDev r = route_dev(s, expert_ids, x_active_mask, workspace, L);
+    MOE_TRY(launch_route(r, route_chunks(s), expert_token_nums, expert_offsets, ep_recv_counts,
+                         nullptr, route_row, assist, stream));
+    if (expand_x)
+        MOE_TRY(launch_dispatch_rows(x, route_row, expand_x, s.num_tokens, s.topk, s.hidden, stream));
+    return MOE_OK;
+}
+
+// ---------------------------------------------------------------- combine
+moe_status moe_combine(const moe_shape *shape, const void *expand_x, const int32_t *route_row,
+                       const float *expert_scales, const uint8_t *x_active_mask,
+                       const void *shared_expert_x, void *x_out, cudaStream_t stream) {
+    MOE_TRY(check_shape(shape, false));
+    const moe_shape &s = *shape;
+    if (!expand_x || !route_row || !expert_scales || !x_out) return MOE_ERR_NULLPTR;
+    if (s.has_shared && !shared_expert_x) return MOE_ERR_NULLPTR;
+    if (!s.has_shared && shared_expert_x) return MOE_ERR_PARAM_INVALID;
+    if (s.mask_kind != 0 && !x_active_mask) return MOE_ERR_NULLPTR;
+    if (s.mask_kind == 0 && x_active_mask) return MOE_ERR_PARAM_INVALID;
+    if (!aligned(expand_x, 16) || !aligned(x_out, 16) ||
+        (shared_expert_x && !aligned(shared_expert_x, 16)) || !aligned(route_row, 4) ||
+        !aligned(expert_scales, 4))
+        return MOE_ERR_ALIGNMENT;
+    return launch_combine(expand_x, route_row, expert_scales, x_active_mask, s.mask_kind,
+                          shared_expert_x, x_out, s.num_tokens, s.topk, s.hidden,
+                          s.num_tokens * s.topk, stream);
+}
+
+// ---------------------------------------------------------------- weights
+moe_status moe_packed_weight_bytes(const moe_shape *shape, size_t *w1_bytes, size_t *w2_bytes) {
+    MOE_TRY(check_shape(shape, true));
+    if (!w1_bytes || !w2_bytes) return MOE_ERR_NULLPTR;
+    const moe_shape &s = *shape;
+    *w1_bytes = (size_t)s.num_experts * s.ffn * s.hidden * 2;
+    *w2_bytes = (size_t)s.num_experts * s.hidden * (s.ffn / 2) * 2;
+    return MOE_OK;
+}
+
+moe_status moe_pack_weights(const moe_shape *shape, const int8_t *w1, const int8_t *w2,
+                            void *w1_packed, void *w2_packed, cudaStream_t stream) {
+    MOE_TRY(check_shape(shape, true));
+    const moe_shape &s = *shape;
+    if (!w1 || !w2 || !w1_packed || !w2_packed) return MOE_ERR_NULLPTR;
+    if (!aligned(w1, 16) || !aligned(w2, 16) || !aligned(w1_packed, kAlign) ||
+        !aligned(w2_packed, kAlign))
+        return MOE_ERR_ALIGNMENT;
+    MOE_TRY(launch_pack_w1(w1, w1_packed, s.num_experts, s.ffn, s.hidden, stream));
+    MOE_TRY(launch_i8_to_f16(w2, w2_packed, s.num_experts * s.hidden * (s.ffn / 2), stream));
+    return MOE_OK;
+}
+
+// ---------------------------------------------------------------- grouped FFN
+static moe_status run_ffn_core(const moe_shape &s, const Layout &L, void *ws,
+                               const int32_t *offsets, const void *w1p, const float *scale1,
+                               const void *w2p, const float *scale2, void *y,
+                               cudaStream_t stream) {
+    const int64_t cap = s.num_tokens * s.topk, Nh = s.ffn / 2;
+    int32_t *status = at<int32_t>(ws, L.status);
+    GemmArgs g1{};
+    g1.a_img = at<void>(ws, L.q1);
+    g1.cap_rows = cap;
+    g1.b_img = w1p;
+    g1.E = s.num_experts;
+    g1.Nout = s.ffn;
+    g1.Kd = s.hidden;
+    g1.offsets = offsets;
+    g1.sched = at<int32_t>(ws, L.sched);
+    g1.g = at<float>(ws, L.g);
+    g1.scale1 = scale1;
+    g1.s1 = at<float>(ws, L.s1);
+    g1.status = status;
+    MOE_TRY(launch_grouped_gemm(Epi::SwiGLU, g1, stream));
+    MOE_TRY(launch_quant2(at<float>(ws, L.g), offsets, s.num_experts, at<void>(ws, L.q2),
+                          at<float>(ws, L.s2), cap, Nh, stream));
+    GemmArgs g2{};
+    g2.a_img = at<void>(ws, L.q2);
+    g2.cap_rows = cap;
+    g2.b_img = w2p;
+    g2.E = s.num_experts;
+    g2.Nout = s.hidden;
+    g2.Kd = Nh;
+    g2.offsets = offsets;
+    g2.sched = at<int32_t>(ws, L.sched);
+    g2.y = y;
+    g2.scale2 = scale2;
+    g2.s2 = at<float>(ws, L.s2);
+    g2.status = status;
+    return launch_grouped_gemm(Epi::DequantBF16, g2, stream);
+}
+
+moe_status moe_grouped_ffn_workspace_size(const moe_shape *shape, size_t *bytes) {
+    MOE_TRY(check_shape(shape, true));
+    if (!bytes) return MOE_ERR_NULLPTR;
+    *bytes = layout_for(*shape, Op::Ffn).total;
+    return MOE_OK;
+}
+
+moe_status moe_grouped_ffn(const moe_shape *shape, const void *expand_x,
+                           const int32_t *expert_offsets, const void *w1_packed,
+                           const float *scale1, const void *w2_packed, const float *scale2,
+                           void *y, void *workspace, size_t workspace_bytes,
+                           cudaStream_t stream) {
+    MOE_TRY(check_shape(shape, true));
+    const moe_shape &s = *shape;
+    if (!expand_x || !expert_offsets || !w1_packed || !scale1 || !w2_packed || !scale2 || !y ||
+        !workspace)
+        return MOE_ERR_NULLPTR;
+    if (!aligned(expand_x, 16) || !aligned(y, 16) || !aligned(scale1, 16) || !aligned(scale2, 16) ||
+        !aligned(w1_packed, kAlign) || !aligned(w2_packed, kAlign) || !aligned(workspace, kAlign))
+        return MOE_ERR_ALIGNMENT;
+    const Layout L = layout_for(s, Op::Ffn);
+    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+    if (s.num_tokens == 0) return MOE_OK;
+    const int64_t cap = s.num_tokens * s.topk;
+    MOE_TRY(launch_sched(expert_offsets, s.num_experts, at<int32_t>(workspace, L.sched),
+                         at<int32_t>(workspace, L.status), stream));
+    MOE_TRY(launch_quant_rows(expand_x, expert_offsets, s.num_experts, at<void>(workspace, L.q1),
+                              at<float>(workspace, L.s1), cap, s.hidden, stream));
+    return run_ffn_core(s, L, workspace, expert_offsets, w1_packed, scale1, w2_packed, scale2, y,
+                        stream);
+}
+
+// ---------------------------------------------------------------- whole layer
+moe_status moe_layer_workspace_size(const moe_shape *shape, size_t *bytes) {
+    MOE_TRY(check_shape(shape, true));
+    if (!bytes) return MOE_ERR_NULLPTR;
+    *bytes = layout_for(*shape, Op::Layer).total;
+    return MOE_OK;
+}
+
+moe_status moe_layer(const moe_shape *shape, const void *x, const int32_t *expert_ids,
+                     const float *expert_scales, const uint8_t *x_active_mask,
+                     const void *shared_expert_x, const void *w1_packed, const float *scale1,
+                     const void *w2_packed, const float *scale2, void *x_out, void *workspace,
+                     size_t workspace_bytes, cudaStream_t stream) {
+    MOE_TRY(check_shape(shape, true));
+    const moe_shape &s = *shape;
+    if (!x || !expert_ids || !expert_scales || !w1_packed || !scale1 || !w2_packed || !scale2 ||
+        !x_out || !workspace)
+        return MOE_ERR_NULLPTR;
+    if (s.has_shared && !shared_expert_x) return MOE_ERR_NULLPTR;
+    if (!s.has_shared && shared_expert_x) return MOE_ERR_PARAM_INVALID;
+    if (s.mask_kind != 0 && !x_active_mask) return MOE_ERR_NULLPTR;
+    if (s.mask_kind == 0 && x_active_mask) return MOE_ERR_PARAM_INVALID;
+    if (!aligned(x, 16) || !aligned(x_out, 16) || !aligned(scale1, 16) || !aligned(scale2, 16) ||
+        (shared_expert_x && !aligned(shared_expert_x, 16)) || !aligned(w1_packed, kAlign) ||
+        !aligned(w2_packed, kAlign) || !aligned(workspace, kAlign) || !aligned(expert_ids, 4) ||
+        !aligned(expert_scales, 4))
+        return MOE_ERR_ALIGNMENT;
+    const Layout L = layout_for(s, Op::Layer);
+    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+    const int64_t cap = s.num_tokens * s.topk;
+    RouteDev r = route_dev(s, expert_ids, x_active_mask, workspace, L);
+    int32_t *route_row = at<int32_t>(workspace, L.route_row);
+    int32_t *offsets = at<int32_t>(workspace, L.offsets);
+    MOE_TRY(launch_route(r, route_chunks(s), at<int64_t>(workspace, L.counts), offsets,
+                         at<int32_t>(workspace, L.recv_cum), at<int32_t>(workspace, L.sched),
+                         route_row, at<int32_t>(workspace, L.assist), stream));
+    if (s.num_tokens == 0) return MOE_OK;
+    MOE_TRY(launch_quant_scatter(x, route_row, at<void>(workspace, L.q1), at<float>(workspace, L.s1),
+                                 s.num_tokens, s.topk, s.hidden, stream));
+    void *y = at<void>(workspace, L.y);
+    MOE_TRY(run_ffn_core(s, L, workspace, offsets, w1_packed, scale1, w2_packed, scale2, y, stream));
+    return launch_combine(y, route_row, expert_scales, x_active_mask, s.mask_kind, shared_expert_x,
+                          x_out, s.num_tokens, s.topk, s.hidden, cap, stream);
+}
+
+moe_status moe_stage_views_get(const moe_shape *shape, int for_layer, void *workspace,
+                               size_t workspace_bytes, moe_stage_views *v) {
+    MOE_TRY(check_shape(shape, true));
+    if (!workspace || !v) return MOE_ERR_NULLPTR;
+    const Layout L = layout_for(*shape, for_layer ? Op::Layer : Op::Ffn);
+    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+    memset(v, 0, sizeof *v);
+    if (for_layer) {
+        v->route_row = at<int32_t>(workspace, L.route_row);
+        v->assist = at<int32_t>(workspace, L.assist);
+        v->expert_offsets = at<int32_t>(workspace, L.offsets);
+        v->expert_token_nums = at<int64_t>(workspace, L.counts);
+        v->ep_recv_counts = at<int32_t>(workspace, L.recv_cum);
+        v->y = at<void>(workspace, L.y);
+    }
+    v->q1 = at<void>(workspace, L.q1);
+    v->s1 = at<float>(workspace, L.s1);
+    v->g = at<float>(workspace, L.g);
+    v->q2 = at<void>(workspace, L.q2);
+    v->s2 = at<float>(workspace, L.s2);
+    return MOE_OK;
+}
+
+// ---------------------------------------------------------------- plain grouped GEMM
+static Layout gemm_layout(int64_t rows, int64_t E, int64_t N, int64_t Kd) {
+    Layout L;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t a = off;
+        off = align_up(off + (bytes ? bytes : 1), kAlign);
+        return a;
+    };
+    L.status = take(4);
+    L.sched = take((size_t)(E + 1) * sizeof(int32_t));
+    L.a_img = take((size_t)rows * Kd * 2);
+    L.w_img = take((size_t)E * N * Kd * 2);
+    L.total = off;
+    return L;
+}
+
+moe_status moe_grouped_gemm_s32_workspace_size(int64_t rows, int64_t E, int64_t N, int64_t Kd,
+                                               size_t *bytes) {
+    if (!bytes) return MOE_ERR_NULLPTR;
+    if (rows < 0 || rows > INT32_MAX || E < 1 || E > kMaxExperts || N < 8 || N % 8 != 0 || Kd < 8 ||
+        Kd % 8 != 0 || N > (1 << 20) || Kd > 131072)
+        return MOE_ERR_SHAPE;
+    *bytes = gemm_layout(rows, E, N, Kd).total;
+    return MOE_OK;
+}
+
+moe_status moe_grouped_gemm_s32(int64_t rows, int64_t E, int64_t N, int64_t Kd,
+                                const int32_t *expert_offsets, const int8_t *A, const int8_t *W,
+                                int32_t *C, void *workspace, size_t workspace_bytes,
+                                cudaStream_t stream) {
+    size_t need = 0;
+    MOE_TRY(moe_grouped_gemm_s32_workspace_size(rows, E, N, Kd, &need));
+    if (!expert_offsets || !A || !W || !C || !workspace) return MOE_ERR_NULLPTR;
+    if (!aligned(A, 16) || !aligned(W, 16) || !aligned(C, 16) || !aligned(workspace, kAlign))
+        return MOE_ERR_ALIGNMENT;
+    if (workspace_bytes < need) return MOE_ERR_WORKSPACE;
+    if (rows == 0) return MOE_OK;
+    const Layout L = gemm_layout(rows, E, N, Kd);
+    MOE_TRY(launch_sched(expert_offsets, E, at<int32_t>(workspace, L.sched),
+                         at<int32_t>(workspace, L.status), stream));
+    MOE_TRY(launch_i8_to_f16(A, at<void>(workspace, L.a_img), rows * Kd, stream));
+    MOE_TRY(launch_i8_to_f16(W, at<void>(workspace, L.w_img), E * N * Kd, stream));
+    GemmArgs g{};
+    g.a_img = at<void>(workspace, L.a_img);
+    g.cap_rows = rows;
+    g.b_img = at<void>(workspace, L.w_img);
+    g.E = E;
+    g.Nout = N;
+    g.Kd = Kd;
+    g.offsets = expert_offsets;
+    g.sched = at<int32_t>(workspace, L.sched);
+    g.c_s32 = C;
+    g.status = at<int32_t>(workspace, L.status);
+    return launch_grouped_gemm(Epi::S32, g, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,154 @@
+// common.cuh -- shared host/device definitions of the GB300 MoE library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "moe_gb300.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------- limits
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 16;
+constexpr int kRouteThreads = 256;
+constexpr int kRouteWarps = kRouteThreads / 32;
+constexpr int kRouteChunkTokens = 256;   // tokens per routing chunk (within one partition)
+constexpr int kGemmBM = 128;             // GEMM tile rows (routed rows)
+constexpr int kGemmBN = 256;             // GEMM tile columns (output channels)
+constexpr size_t kAlign = 1024;
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// ---------------------------------------------------------------- launch bookkeeping
+// Every kernel launch goes through launch_begin/launch_end: they count launches
+// and, when profiling is on, bracket the launch with a CUDA event pair recorded
+// on the launching stream.
+int launch_begin(const char *name, cudaStream_t stream);
+void launch_end(int token, cudaStream_t stream);
+int num_sms();
+
+#define MOE_LAUNCH(name, kernel, grid, block, smem, stream, ...)              \
+    do {                                                                      \
+        int _tok = ::moe::launch_begin(name, stream);                         \
+        kernel<<<(grid), (block), (smem), (stream)>>>(__VA_ARGS__);           \
+        cudaError_t _err = cudaGetLastError();                                \
+        ::moe::launch_end(_tok, stream);                                      \
+        if (_err != cudaSuccess) return MOE_ERR_CUDA;                         \
+    } while (0)
+
+#define MOE_TRY(expr)                                                         \
+    do {                                                                      \
+        moe_status _s = (expr);                                               \
+        if (_s != MOE_OK) return _s;                                          \
+    } while (0)
+
+// ---------------------------------------------------------------- workspace
+// Regions of a workspace, byte offsets from its start (0 = region absent,
+// except `status`, which is always at offset 0).  Each region is 1024-aligned.
+struct Layout {
+    size_t status = 0;        // int32 status word (+ padding to 1024)
+    size_t hist = 0;          // int32 [chunks][E] routing histograms / bases
+    size_t sched = 0;         // int32 [E+1] GEMM m-block starts per expert
+    size_t route_row = 0;     // int32 [T*K]
+    size_t assist = 0;        // int32 [T*K*3]
+    size_t offsets = 0;       // int32 [E+1]
+    size_t counts = 0;        // int64 [E]
+    size_t recv_cum = 0;      // int32 [E*P]
+    size_t q1 = 0;            // fp16 [T*K, H]  int8 values
+    size_t s1 = 0;            // fp32 [T*K]
+    size_t g = 0;             // fp32 [T*K, N/2]
+    size_t q2 = 0;            // fp16 [T*K, N/2] int8 values
+    size_t s2 = 0;            // fp32 [T*K]
+    size_t y = 0;             // bf16 [T*K, H]
+    size_t a_img = 0;         // fp16 images for the plain grouped GEMM
+    size_t w_img = 0;
+    size_t total = 0;
+};
+
+enum class Op { Dispatch, Combine, Ffn, Layer };
+
+int64_t route_chunks(const moe_shape &s);
+moe_status check_shape(const moe_shape *s, bool need_ffn);
+Layout layout_for(const moe_shape &s, Op op);
+
+// ---------------------------------------------------------------- device helpers
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+    return __uint_as_float(((uint32_t)b) << 16);
+}
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+}  // namespace moe
+
+// ---------------------------------------------------------------- kernel-level entry points
+// (host functions implemented in the .cu files, used by capi.cu)
+namespace moe {
+
+struct RouteDev {
+    const int32_t *ids;
+    const uint8_t *mask;
+    int mask_kind;
+    int64_t T, P, M, K, E;
+    int64_t chunks_per_partition;
+    int32_t *hist;     // [chunks][E]
+    int32_t *bad;      // [chunks] 1 if the chunk saw an invalid expert id
+    int32_t *status;
+};
+
+moe_status launch_route(const RouteDev &r, int64_t chunks, int64_t *counts, int32_t *offsets,
+                        int32_t *recv_cum, int32_t *sched, int32_t *route_row, int32_t *assist,
+                        cudaStream_t stream);
+
+moe_status launch_dispatch_rows(const void *x, const int32_t *route_row, void *expand_x,
+                                int64_t T, int64_t K, int64_t H, cudaStream_t stream);
+
+moe_status launch_combine(const void *y, const int32_t *route_row, const float *probs,
+                          const uint8_t *mask, int mask_kind, const void *shared, void *out,
+                          int64_t T, int64_t K, int64_t H, int64_t cap_rows, cudaStream_t stream);
+
+moe_status launch_quant_scatter(const void *x, const int32_t *route_row, void *q1, float *s1,
+                                int64_t T, int64_t K, int64_t H, cudaStream_t stream);
+
+moe_status launch_quant_rows(const void *x_rows, const int32_t *offsets, int64_t E, void *q1,
+                             float *s1, int64_t cap_rows, int64_t H, cudaStream_t stream);
+
+
+moe_status launch_quant2(const float *g, const int32_t *offsets, int64_t E, void *q2, float *s2,
+                         int64_t cap_rows, int64_t Nh, cudaStream_t stream);
+
+moe_status launch_sched(const int32_t *offsets, int64_t E, int32_t *sched, int32_t *status,
+                        cudaStream_t stream);
+
+moe_status launch_pack_w1(const int8_t *w1, void *w1p, int64_t E, int64_t N, int64_t H,
+                          cudaStream_t stream);
+moe_status launch_i8_to_f16(const int8_t *src, void *dst, int64_t n, cudaStream_t stream);
+
+// Grouped GEMM on fp16 images of int8 operands (tcgen05, TMEM accumulators).
+enum class Epi { S32 = 0, SwiGLU = 1, DequantBF16 = 2 };
+struct GemmArgs {
+    const void *a_img;        // fp16 [cap_rows, Kd]
+    int64_t cap_rows;
+    const void *b_img;        // fp16 [E, Nout, Kd]
+    int64_t E, Nout, Kd;
+    const int32_t *offsets;   // [E+1]; rows >= cap_rows are never stored
+    const int32_t *sched;     // [E+1]
+    // epilogue operands
+    int32_t *c_s32;           // [cap_rows, Nout]
+    float *g;                 // [cap_rows, Nout/2]
+    const float *scale1;      // [E, Nout]
+    const float *s1;          // [cap_rows]
+    void *y;                  // bf16 [cap_rows, Nout]
+    const float *scale2;      // [E, Nout]
+    const float *s2;          // [cap_rows]
+    int32_t *status;
+};
+moe_status launch_grouped_gemm(Epi epi, const GemmArgs &a, cudaStream_t stream);
+
+}  // namespace moe

@@ -1,0 +1,536 @@
+// gemm_tc.cu -- grouped int8 GEMMs on the 5th-generation tensor cores.
+//
+// "PTO MegaMoE Dispatch + Combine Fusion Example", GMM1 and GMM2: per local
+// expert, int8 rows x int8 weights -> int32 accumulator -> per-channel fp32
+// scale (fixpipe) -> epilogue.  Here every expert is local.
+//
+// Exact int8 products on tcgen05.  sm_103a has no tcgen05 int8 kind, so the
+// int8 operands are stored as fp16 images (every integer in [-127, 127] is an
+// fp16 number) and multiplied with tcgen05.mma kind::f16 into fp32 TMEM
+// accumulators.  Each product is at most 127*127 = 16129 in magnitude and is
+// exact in fp32, and a sum of at most 1024 of them stays below 2^24 =
+// 16777216, where every integer is an fp32 number.  The K loop is therefore cut
+// into chunks of 1024 (16 k-blocks of 64): each chunk's accumulator holds an
+// exact integer, which the epilogue warps convert to int32 and add up in
+// registers.  The int32 total is the exact int8 dot product.
+//
+// Kernel shape (one persistent CTA per SM, 320 threads):
+//   warp 0      TMA producer: A tile 128 x 64 and B tile 256 x 64 (fp16,
+//               128-byte swizzle) per k-block into a 4-stage shared-memory ring
+//   warp 1      TMEM owner (allocates all 512 columns) and MMA issuer
+//               (one thread): 4 x tcgen05.mma M=128 N=256 K=16 per k-block,
+//               alternating between two 256-column TMEM accumulators, one
+//               accumulator per 1024-deep K chunk
+//   warps 2..9  epilogue: each (TMEM lane quadrant, column half) pair drains
+//               its 32 rows x 128 columns per chunk with tcgen05.ld, keeps the
+//               int32 sums in registers and, after the last chunk, applies the
+//               epilogue and stores
+// Tiles are (expert, 128-row block, 256-column block), enumerated from the
+// per-expert m-block schedule computed on the device, column block fastest so
+// that the CTAs in flight share the same rows of A and the same expert's
+// weights in L2.  Rows past an expert's end are computed and never stored.
+// Every wait is bounded: after about two seconds a wait gives up, sets
+// MOE_DEV_TIMEOUT in the status word and the CTA drains and exits.
+#include "common.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+namespace moe {
+namespace {
+
+constexpr int BM = kGemmBM;          // 128
+constexpr int BN = kGemmBN;          // 256
+constexpr int BK = 64;               // fp16 elements per k-block = one 128-byte swizzle row
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int CHUNK_KB = 16;         // 16 x 64 = 1024-deep exact chunk
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr unsigned long long kTimeoutNs = 2000000000ull;
+constexpr size_t kBarrierBytes = 256;
+constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + 1024 + kBarrierBytes +
+                              2 * (kMaxExperts + 1) * sizeof(int32_t);
+
+struct GemmDev {
+    const int32_t *offsets;
+    const int32_t *sched;
+    int E;
+    int n_blocks;
+    int num_kb;
+    int Nout;
+    int64_t cap_rows;
+    int32_t *c_s32;
+    float *g;
+    const float *scale1;
+    const float *s1;
+    __nv_bfloat16 *y;
+    const float *scale2;
+    const float *s2;
+    int32_t *status;
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(slot)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);        // start address
+    d |= (uint64_t)1 << 16;                          // leading byte offset (unused here)
+    d |= (uint64_t)(1024 >> 4) << 32;                // stride byte offset: 8 rows x 128 B
+    d |= (uint64_t)1 << 46;                          // descriptor version
+    d |= (uint64_t)2 << 61;                          // swizzle: 128 B
+    return d;
+}
+
+// Instruction descriptor: fp16 A and B (K-major), fp32 accumulator, M x N.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+    return (1u << 4)                        // D format: f32
+           | (0u << 7) | (0u << 10)         // A, B format: f16
+           | ((uint32_t)(N >> 3) << 17)     // N
+           | ((uint32_t)(M >> 4) << 24);    // M
+}
+
+// Waits for phase `parity` of `bar`.  Gives up when the CTA's abort flag is set
+// or after kTimeoutNs, setting the abort flag and the status bit.
+__device__ __noinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          int32_t *status, bool honour_abort = true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 255u) == 0) {
+            if (honour_abort && *abort_flag) return false;
+            if (globaltimer() - t0 > kTimeoutNs) {
+                *abort_flag = 1;
+                atomicOr(status, MOE_DEV_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+struct Tile {
+    int e, row0, rows, nb;
+};
+
+__device__ __forceinline__ Tile decode_tile(int64_t tile, int n_blocks, int E, const int32_t *s_sched,
+                                            const int32_t *s_off) {
+    Tile t;
+    int mblk = (int)(tile / n_blocks);
+    t.nb = (int)(tile % n_blocks);
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {   // last expert whose first m-block is <= mblk
+        int mid = (lo + hi + 1) >> 1;
+        if (s_sched[mid] <= mblk) lo = mid; else hi = mid - 1;
+    }
+    t.e = lo;
+    t.row0 = s_off[lo] + (mblk - s_sched[lo]) * BM;
+    t.rows = min(BM, s_off[lo + 1] - t.row0);
+    return t;
+}
+
+__device__ __forceinline__ float silu_f32(float v) {
+    return __fdiv_rn(v, __fadd_rn(1.0f, expf(-v)));
+}
+
+// ---------------------------------------------------------------- epilogues
+// acc[i] is the exact int32 sum for row `row` and tile column hf*128 + i.
+template <int EPI>
+__device__ __forceinline__ void epilogue_store(const GemmDev &p, const Tile &t, int row, int hf,
+                                               const int32_t (&acc)[128]) {
+    if (EPI == (int)Epi::S32) {
+        const int c0 = t.nb * BN + hf * 128;
+        int4 *dst = reinterpret_cast<int4 *>(p.c_s32 + (int64_t)row * p.Nout + c0);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (c0 + 4 * i < p.Nout)
+                dst[i] = make_int4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+    } else if (EPI == (int)Epi::SwiGLU) {
+        // packed columns hf*128 + [0, 64) are SiLU-half channels j0 + cc and
+        // hf*128 + [64, 128) their multiplier channels Nh + j0 + cc.
+        const int Nh = p.Nout / 2;
+        const int j0 = t.nb * 128 + hf * 64;
+        const float s1 = p.s1[row];
+        const float *sc_a = p.scale1 + (int64_t)t.e * p.Nout + j0;
+        const float *sc_b = sc_a + Nh;
+        float4 *dst = reinterpret_cast<float4 *>(p.g + (int64_t)row * Nh + j0);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float4 sa = __ldg(reinterpret_cast<const float4 *>(sc_a) + i);
+            const float4 sb = __ldg(reinterpret_cast<const float4 *>(sc_b) + i);
+            const float sav[4] = {sa.x, sa.y, sa.z, sa.w};
+            const float sbv[4] = {sb.x, sb.y, sb.z, sb.w};
+            float o[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int cc = 4 * i + u;
+                float ha = __fmul_rn(__fmul_rn(__int2float_rn(acc[cc]), sav[u]), s1);
+                float hb = __fmul_rn(__fmul_rn(__int2float_rn(acc[64 + cc]), sbv[u]), s1);
+                o[u] = __fmul_rn(silu_f32(ha), hb);
+            }
+            dst[i] = make_float4(o[0], o[1], o[2], o[3]);
+        }
+    } else {
+        const int c0 = t.nb * BN + hf * 128;
+        const float s2 = p.s2[row];
+        const float *sc = p.scale2 + (int64_t)t.e * p.Nout + c0;
+        uint4 *dst = reinterpret_cast<uint4 *>(p.y + (int64_t)row * p.Nout + c0);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if (c0 + 8 * i < p.Nout) {
+                const float4 sa = __ldg(reinterpret_cast<const float4 *>(sc) + 2 * i);
+                const float4 sb = __ldg(reinterpret_cast<const float4 *>(sc) + 2 * i + 1);
+                const float sv[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+                uint32_t w[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    float lo = __fmul_rn(__fmul_rn(__int2float_rn(acc[8 * i + 2 * u]), sv[2 * u]), s2);
+                    float hi = __fmul_rn(__fmul_rn(__int2float_rn(acc[8 * i + 2 * u + 1]), sv[2 * u + 1]), s2);
+                    w[u] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+                           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+                }
+                dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- the kernel
+template <int EPI>
+__global__ void __launch_bounds__(THREADS, 1)
+k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               GemmDev p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)STAGES * STAGE_BYTES);
+    uint64_t *empty = full + STAGES;
+    uint64_t *acc_full = empty + STAGES;
+    uint64_t *acc_empty = acc_full + 2;
+    uint64_t *drain = acc_empty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int32_t *s_sched = reinterpret_cast<int32_t *>(smem + (size_t)STAGES * STAGE_BYTES + kBarrierBytes);
+    int32_t *s_off = s_sched + (kMaxExperts + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], EPI_WARPS);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
+        s_sched[i] = p.sched[i];
+        s_off[i] = p.offsets[i];
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int64_t total_tiles = (int64_t)s_sched[p.E] * p.n_blocks;
+    const int num_chunks = (p.num_kb + CHUNK_KB - 1) / CHUNK_KB;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued_phase[STAGES];
+#pragma unroll
+            for (int s = 0; s < STAGES; ++s) issued_phase[s] = -1;
+            for (int64_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+                const Tile t = decode_tile(tile, p.n_blocks, p.E, s_sched, s_off);
+                bool ok = true;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                    uint8_t *sa = smem + (size_t)stage * STAGE_BYTES;
+                    mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+                    tma_load_2d(sa, &tmA, &full[stage], kb * BK, t.row0);
+                    tma_load_3d(sa + A_BYTES, &tmB, &full[stage], kb * BK, t.nb * BN, t.e);
+                    issued_phase[stage] = (int)phase;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+            }
+            // every issued load must have landed before the CTA may exit
+            for (int s = 0; s < STAGES; ++s)
+                if (issued_phase[s] >= 0)
+                    wait_bounded(&full[s], (uint32_t)issued_phase[s], abort_flag, p.status, false);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            constexpr uint32_t idesc = idesc_f16(BM, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int accb = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int64_t tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+                for (int kb0 = 0; ok && kb0 < p.num_kb; kb0 += CHUNK_KB) {
+                    if (!wait_bounded(&acc_empty[accb], acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + (uint32_t)(accb * BN);
+                    const int kb1 = min(kb0 + CHUNK_KB, p.num_kb);
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!wait_bounded(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t a_addr = smem_u32(smem + (size_t)stage * STAGE_BYTES);
+                        const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+                        for (int k = 0; k < BK / 16; ++k) {
+                            mma_f16(d_tmem, desc_sw128(a_addr + 32 * k), desc_sw128(b_addr + 32 * k),
+                                    idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                        }
+                        mma_commit(&empty[stage]);
+                        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                    }
+                    if (!ok) break;
+                    mma_commit(&acc_full[accb]);
+                    if (++accb == 2) { accb = 0; acc_phase ^= 1u; }
+                }
+            }
+            // no MMA may still be running when TMEM is released
+            mma_commit(drain);
+            wait_bounded(drain, 0, abort_flag, p.status, false);
+        }
+    } else {
+        // ---------------------------------------------------- epilogue warps
+        const int q = warp & 3;              // TMEM lane quadrant this warp may read
+        const int hf = (warp - 2) >> 2;      // column half of the tile
+        const int rloc = q * 32 + lane;
+        int accb = 0;
+        uint32_t acc_phase = 0;
+        for (int64_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+            const Tile t = decode_tile(tile, p.n_blocks, p.E, s_sched, s_off);
+            int32_t acc[128];
+            bool ok = true;
+            for (int c = 0; c < num_chunks; ++c) {
+                bool w = wait_bounded(&acc_full[accb], acc_phase, abort_flag, p.status);
+                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) +
+                                       (uint32_t)(accb * BN + hf * 128);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t r[32];
+                    tmem_ld32(taddr + 32 * j, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int v = __float2int_rn(__uint_as_float(r[i]));
+                        acc[32 * j + i] = (c == 0) ? v : acc[32 * j + i] + v;
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[accb]);
+                if (++accb == 2) { accb = 0; acc_phase ^= 1u; }
+            }
+            if (!ok) break;
+            if (rloc < t.rows && (int64_t)t.row0 + rloc < p.cap_rows)
+                epilogue_store<EPI>(p, t, t.row0 + rloc, hf, acc);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+bool make_map(CUtensorMap *m, const void *base, int rank, const uint64_t *dims,
+              const uint64_t *strides_bytes, const uint32_t *box) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t d[3], s[2];
+    cuuint32_t b[3], es[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) { d[i] = dims[i]; b[i] = box[i]; }
+    for (int i = 0; i < rank - 1; ++i) s[i] = strides_bytes[i];
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (cuuint32_t)rank, const_cast<void *>(base), d, s,
+                    b, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int EPI>
+moe_status launch_epi(const CUtensorMap &ma, const CUtensorMap &mb, const GemmDev &d,
+                      cudaStream_t stream) {
+    static bool configured = false;
+    if (!configured) {
+        if (cudaFuncSetAttribute(k_grouped_gemm<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)SMEM_BYTES) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        configured = true;
+    }
+    const char *names[3] = {"gemm_s32", "gemm1_swiglu", "gemm2_dequant"};
+    MOE_LAUNCH(names[EPI], k_grouped_gemm<EPI>, num_sms(), THREADS, SMEM_BYTES, stream, ma, mb, d);
+    return MOE_OK;
+}
+
+}  // namespace
+
+moe_status launch_grouped_gemm(Epi epi, const GemmArgs &a, cudaStream_t stream) {
+    if (a.cap_rows <= 0 || a.E <= 0) return MOE_OK;
+    CUtensorMap ma, mb;
+    const uint64_t adims[2] = {(uint64_t)a.Kd, (uint64_t)a.cap_rows};
+    const uint64_t astr[1] = {(uint64_t)a.Kd * 2};
+    const uint32_t abox[2] = {BK, BM};
+    const uint64_t bdims[3] = {(uint64_t)a.Kd, (uint64_t)a.Nout, (uint64_t)a.E};
+    const uint64_t bstr[2] = {(uint64_t)a.Kd * 2, (uint64_t)a.Kd * a.Nout * 2};
+    const uint32_t bbox[3] = {BK, BN, 1};
+    if (!make_map(&ma, a.a_img, 2, adims, astr, abox)) return MOE_ERR_CUDA;
+    if (!make_map(&mb, a.b_img, 3, bdims, bstr, bbox)) return MOE_ERR_CUDA;
+    GemmDev d;
+    d.offsets = a.offsets;
+    d.sched = a.sched;
+    d.E = (int)a.E;
+    d.n_blocks = (int)((a.Nout + BN - 1) / BN);
+    d.num_kb = (int)((a.Kd + BK - 1) / BK);
+    d.Nout = (int)a.Nout;
+    d.cap_rows = a.cap_rows;
+    d.c_s32 = a.c_s32;
+    d.g = a.g;
+    d.scale1 = a.scale1;
+    d.s1 = a.s1;
+    d.y = reinterpret_cast<__nv_bfloat16 *>(a.y);
+    d.scale2 = a.scale2;
+    d.s2 = a.s2;
+    d.status = a.status;
+    switch (epi) {
+        case Epi::S32: return launch_epi<(int)Epi::S32>(ma, mb, d, stream);
+        case Epi::SwiGLU: return launch_epi<(int)Epi::SwiGLU>(ma, mb, d, stream);
+        case Epi::DequantBF16: return launch_epi<(int)Epi::DequantBF16>(ma, mb, d, stream);
+    }
+    return MOE_ERR_PARAM_INVALID;
+}
+
+}  // namespace moe

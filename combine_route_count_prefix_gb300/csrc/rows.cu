@@ -1,0 +1,407 @@
+// rows.cu -- the HBM-bound row kernels: dispatch copy, combine, the two
+// dynamic quantisations and weight packing.
+//
+// All of them move whole rows as 16-byte vectors: a CTA takes one row (or one
+// token) at a time, every thread loads its slice of the row into registers
+// (up to 8 x 16 B), and then writes it once per destination.  H is a multiple
+// of 8, so a 16-byte vector never straddles a row.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kRowThreads = 128;
+constexpr int kVec = 8;                 // 16-byte vectors held per thread per pass
+constexpr uint32_t kFull = 0xffffffffu;
+
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4 &v, float (&f)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat16 a = __float2bfloat16_rn(lo), b = __float2bfloat16_rn(hi);
+    return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+    __half a = __float2half_rn(lo), b = __float2half_rn(hi);
+    return (uint32_t)__half_as_ushort(a) | ((uint32_t)__half_as_ushort(b) << 16);
+}
+
+__device__ __forceinline__ float block_max(float v, float *scratch /*[32]*/) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) scratch[warp] = v;
+    __syncthreads();
+    float r = scratch[0];
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) r = fmaxf(r, scratch[w]);
+    __syncthreads();
+    return r;
+}
+
+// Dynamic int8 quantisation code of v with scale s (s = amax / 127): rint(v/s)
+// clamped to [-127, 127], 0 when s == 0.  IEEE division and round-half-even.
+__device__ __forceinline__ float quant_code(float v, float s) {
+    if (s == 0.0f) return 0.0f;
+    float r = rintf(__fdiv_rn(v, s));
+    return fminf(fmaxf(r, -127.0f), 127.0f);
+}
+
+// ---------------------------------------------------------------- dispatch copy
+// expand_x[route_row[t*K+k]] = x[t] for every active route of token t.
+__global__ void __launch_bounds__(kRowThreads)
+k_dispatch_rows(const uint4 *__restrict__ x, const int32_t *__restrict__ route_row,
+                uint4 *__restrict__ expand_x, int64_t T, int K, int64_t H8) {
+    __shared__ int32_t rows[kMaxTopK];
+    for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+        __syncthreads();
+        if (threadIdx.x < K) rows[threadIdx.x] = route_row[t * K + threadIdx.x];
+        __syncthreads();
+        for (int64_t j0 = threadIdx.x; j0 < H8; j0 += (int64_t)kRowThreads * kVec) {
+            uint4 v[kVec];
+#pragma unroll
+            for (int u = 0; u < kVec; ++u) {
+                int64_t j = j0 + (int64_t)u * kRowThreads;
+                if (j < H8) v[u] = ld_stream(x + t * H8 + j);
+            }
+            for (int k = 0; k < K; ++k) {
+                int32_t r = rows[k];
+                if (r < 0) continue;
+                uint4 *dst = expand_x + (int64_t)r * H8;
+#pragma unroll
+                for (int u = 0; u < kVec; ++u) {
+                    int64_t j = j0 + (int64_t)u * kRowThreads;
+                    if (j < H8) dst[j] = v[u];
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- combine
+// out[t] = bf16( sum_{k active, ascending} p[t,k] * float(y[row]) + float(shared[t]) )
+// with separately rounded fp32 multiply and add (no FMA) so the result is the
+// same as the slot-ordered fp32 loop of the pages' combine.
+__global__ void __launch_bounds__(kRowThreads)
+k_combine(const uint4 *__restrict__ y, const int32_t *__restrict__ route_row,
+          const float *__restrict__ probs, const uint8_t *__restrict__ mask, int mask_kind,
+          const uint4 *__restrict__ shared, uint4 *__restrict__ out, int64_t T, int K, int64_t H8,
+          int64_t cap_rows) {
+    __shared__ int32_t rows[kMaxTopK];
+    __shared__ float ps[kMaxTopK];
+    for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+        __syncthreads();
+        if (threadIdx.x < K) {
+            int k = threadIdx.x;
+            int32_t r = route_row[t * K + k];
+            bool on = r >= 0 && r < cap_rows;
+            if (mask_kind == 1) on = on && mask[t] != 0;
+            if (mask_kind == 2) on = on && mask[t * K + k] != 0;
+            rows[k] = on ? r : -1;
+            ps[k] = probs[t * K + k];
+        }
+        __syncthreads();
+        for (int64_t j0 = threadIdx.x; j0 < H8; j0 += (int64_t)kRowThreads * kVec) {
+            float acc[kVec][8];
+#pragma unroll
+            for (int u = 0; u < kVec; ++u)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
+            for (int k = 0; k < K; ++k) {
+                int32_t r = rows[k];
+                if (r < 0) continue;
+                const float p = ps[k];
+                const uint4 *src = y + (int64_t)r * H8;
+                uint4 v[kVec];
+#pragma unroll
+                for (int u = 0; u < kVec; ++u) {
+                    int64_t j = j0 + (int64_t)u * kRowThreads;
+                    if (j < H8) v[u] = ld_stream(src + j);
+                }
+#pragma unroll
+                for (int u = 0; u < kVec; ++u) {
+                    float f[8];
+                    unpack_bf16x8(v[u], f);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[u][i] = __fadd_rn(acc[u][i], __fmul_rn(p, f[i]));
+                }
+            }
+            if (shared) {
+#pragma unroll
+                for (int u = 0; u < kVec; ++u) {
+                    int64_t j = j0 + (int64_t)u * kRowThreads;
+                    if (j < H8) {
+                        float f[8];
+                        unpack_bf16x8(ld_stream(shared + t * H8 + j), f);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) acc[u][i] = __fadd_rn(acc[u][i], f[i]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kVec; ++u) {
+                int64_t j = j0 + (int64_t)u * kRowThreads;
+                if (j < H8) {
+                    uint4 o;
+                    o.x = pack_bf16x2(acc[u][0], acc[u][1]);
+                    o.y = pack_bf16x2(acc[u][2], acc[u][3]);
+                    o.z = pack_bf16x2(acc[u][4], acc[u][5]);
+                    o.w = pack_bf16x2(acc[u][6], acc[u][7]);
+                    out[t * H8 + j] = o;
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- quantisation of bf16 rows
+// One source row (bf16, H8 vectors) -> int8 codes stored as fp16 images plus
+// the fp32 scale, written to every destination row in rows[0..ndst).
+// The whole row stays in registers: H8 <= kRowThreads * kVec (H <= 8192).
+template <bool kFromRouteTable>
+__global__ void __launch_bounds__(kRowThreads)
+k_quant_bf16_rows(const uint4 *__restrict__ src, const int32_t *__restrict__ route_row,
+                  const int32_t *__restrict__ offsets, int64_t E, int64_t T, int K,
+                  uint4 *__restrict__ q, float *__restrict__ s_out, int64_t H8) {
+    __shared__ int32_t rows[kMaxTopK];
+    __shared__ int32_t nrows;
+    __shared__ float scratch[32];
+    // kFromRouteTable: one iteration per token t, destinations = its active routes.
+    // otherwise:       one iteration per dispatched row r < offsets[E], destination = r.
+    const int64_t n_items = kFromRouteTable ? T : min((int64_t)offsets[E], T);
+    for (int64_t it = blockIdx.x; it < n_items; it += gridDim.x) {
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int n = 0;
+            if (kFromRouteTable) {
+                for (int k = 0; k < K; ++k) {
+                    int32_t r = route_row[it * K + k];
+                    if (r >= 0) rows[n++] = r;
+                }
+            } else {
+                rows[n++] = (int32_t)it;
+            }
+            nrows = n;
+        }
+        __syncthreads();
+        const int n = nrows;
+        if (n == 0) continue;
+        uint4 v[kVec];
+        float amax = 0.0f;
+#pragma unroll
+        for (int u = 0; u < kVec; ++u) {
+            int64_t j = threadIdx.x + (int64_t)u * kRowThreads;
+            v[u] = make_uint4(0, 0, 0, 0);
+            if (j < H8) {
+                v[u] = ld_stream(src + it * H8 + j);
+                float f[8];
+                unpack_bf16x8(v[u], f);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+            }
+        }
+        amax = block_max(amax, scratch);
+        const float s = __fdiv_rn(amax, 127.0f);
+        // 8 bf16 in -> 8 fp16 codes out: one 16-byte vector in, one out
+        uint4 qv[kVec];
+#pragma unroll
+        for (int u = 0; u < kVec; ++u) {
+            float f[8];
+            unpack_bf16x8(v[u], f);
+            qv[u].x = pack_half2(quant_code(f[0], s), quant_code(f[1], s));
+            qv[u].y = pack_half2(quant_code(f[2], s), quant_code(f[3], s));
+            qv[u].z = pack_half2(quant_code(f[4], s), quant_code(f[5], s));
+            qv[u].w = pack_half2(quant_code(f[6], s), quant_code(f[7], s));
+        }
+        for (int d = 0; d < n; ++d) {
+            const int64_t r = rows[d];
+            uint4 *dst = q + r * H8;
+#pragma unroll
+            for (int u = 0; u < kVec; ++u) {
+                int64_t j = threadIdx.x + (int64_t)u * kRowThreads;
+                if (j < H8) dst[j] = qv[u];
+            }
+            if (threadIdx.x == 0) s_out[r] = s;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- second quantisation
+// g fp32 [rows, Nh] -> q2 fp16 images + s2, for rows r < offsets[E].
+// Each thread holds up to kQ2Vec float4 of the row (Nh <= 256 * 4 * kQ2Vec).
+constexpr int kQ2Threads = 256;
+constexpr int kQ2Vec = 4;
+__global__ void __launch_bounds__(kQ2Threads)
+k_quant2(const float4 *__restrict__ g, const int32_t *__restrict__ offsets, int64_t E,
+         uint2 *__restrict__ q2, float *__restrict__ s2, int64_t Nh4, int64_t cap_rows) {
+    __shared__ float scratch[32];
+    const int64_t R = min((int64_t)offsets[E], cap_rows);
+    for (int64_t r = blockIdx.x; r < R; r += gridDim.x) {
+        float4 v[kQ2Vec];
+        float amax = 0.0f;
+#pragma unroll
+        for (int u = 0; u < kQ2Vec; ++u) {
+            int64_t j = threadIdx.x + (int64_t)u * kQ2Threads;
+            if (j < Nh4) {
+                v[u] = __ldcs(g + r * Nh4 + j);
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)),
+                                         fmaxf(fabsf(v[u].z), fabsf(v[u].w))));
+            }
+        }
+        amax = block_max(amax, scratch);
+        const float s = __fdiv_rn(amax, 127.0f);
+#pragma unroll
+        for (int u = 0; u < kQ2Vec; ++u) {
+            int64_t j = threadIdx.x + (int64_t)u * kQ2Threads;
+            if (j < Nh4) {
+                uint2 o;
+                o.x = pack_half2(quant_code(v[u].x, s), quant_code(v[u].y, s));
+                o.y = pack_half2(quant_code(v[u].z, s), quant_code(v[u].w, s));
+                q2[r * Nh4 + j] = o;
+            }
+        }
+        if (threadIdx.x == 0) s2[r] = s;
+    }
+}
+
+// ---------------------------------------------------------------- weight packing
+// int8 -> fp16 image of the same integer (exact), 16 values per thread.
+__device__ __forceinline__ void i8x16_to_f16(const int4 &in, uint4 &lo, uint4 &hi) {
+    const int8_t *b = reinterpret_cast<const int8_t *>(&in);
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = pack_half2((float)b[2 * i], (float)b[2 * i + 1]);
+    lo = make_uint4(w[0], w[1], w[2], w[3]);
+    hi = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+__global__ void k_i8_to_f16(const int4 *__restrict__ src, uint4 *__restrict__ dst, int64_t n16) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        uint4 lo, hi;
+        i8x16_to_f16(src[i], lo, hi);
+        dst[2 * i] = lo;
+        dst[2 * i + 1] = hi;
+    }
+}
+
+__global__ void k_i8_to_f16_tail(const int8_t *__restrict__ src, __half *__restrict__ dst,
+                                 int64_t start, int64_t n) {
+    int64_t i = start + blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if (i < n) dst[i] = __float2half_rn((float)src[i]);
+}
+
+// W1 [E, N, H] -> packed fp16 [E, N, H] with rows reordered so that packed
+// block b (rows 256b .. 256b+255) holds, for half h in {0, 1}:
+//   rows 256b + 128h +  0..63 : SiLU-half channels 128b + 64h + (0..63)
+//   rows 256b + 128h + 64..127: multiplier channels N/2 + 128b + 64h + (0..63)
+// so one 256-column GEMM tile carries 128 complete SwiGLU pairs.
+__global__ void k_pack_w1(const int8_t *__restrict__ w1, uint4 *__restrict__ out, int64_t E,
+                          int64_t N, int64_t H) {
+    const int64_t H16 = H / 16;
+    const int64_t total = E * N * H16;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        int64_t col16 = i % H16;
+        int64_t prow = (i / H16) % N;
+        int64_t e = i / (H16 * N);
+        int64_t b = prow / 256, within = prow % 256, h = within / 128, ii = within % 128;
+        int64_t src_row = (ii < 64) ? (128 * b + 64 * h + ii) : (N / 2 + 128 * b + 64 * h + (ii - 64));
+        int4 in = *reinterpret_cast<const int4 *>(w1 + (e * N + src_row) * H + col16 * 16);
+        uint4 lo, hi;
+        i8x16_to_f16(in, lo, hi);
+        out[2 * i] = lo;
+        out[2 * i + 1] = hi;
+    }
+}
+
+int grid_for(int64_t items, int per_sm) {
+    int64_t g = (int64_t)num_sms() * per_sm;
+    if (items < g) g = items;
+    return (int)(g > 0 ? g : 1);
+}
+
+}  // namespace
+
+moe_status launch_dispatch_rows(const void *x, const int32_t *route_row, void *expand_x,
+                                int64_t T, int64_t K, int64_t H, cudaStream_t stream) {
+    if (T == 0) return MOE_OK;
+    MOE_LAUNCH("dispatch_rows", k_dispatch_rows, grid_for(T, 16), kRowThreads, 0, stream,
+               (const uint4 *)x, route_row, (uint4 *)expand_x, T, (int)K, H / 8);
+    return MOE_OK;
+}
+
+moe_status launch_combine(const void *y, const int32_t *route_row, const float *probs,
+                          const uint8_t *mask, int mask_kind, const void *shared, void *out,
+                          int64_t T, int64_t K, int64_t H, int64_t cap_rows, cudaStream_t stream) {
+    if (T == 0) return MOE_OK;
+    MOE_LAUNCH("combine", k_combine, grid_for(T, 16), kRowThreads, 0, stream, (const uint4 *)y,
+               route_row, probs, mask, mask_kind, (const uint4 *)shared, (uint4 *)out, T, (int)K,
+               H / 8, cap_rows);
+    return MOE_OK;
+}
+
+moe_status launch_quant_scatter(const void *x, const int32_t *route_row, void *q1, float *s1,
+                                int64_t T, int64_t K, int64_t H, cudaStream_t stream) {
+    if (T == 0) return MOE_OK;
+    MOE_LAUNCH("quant_scatter", k_quant_bf16_rows<true>, grid_for(T, 16), kRowThreads, 0, stream,
+               (const uint4 *)x, route_row, (const int32_t *)nullptr, (int64_t)0, T, (int)K,
+               (uint4 *)q1, s1, H / 8);
+    return MOE_OK;
+}
+
+moe_status launch_quant_rows(const void *x_rows, const int32_t *offsets, int64_t E, void *q1,
+                             float *s1, int64_t cap_rows, int64_t H, cudaStream_t stream) {
+    if (cap_rows == 0) return MOE_OK;
+    // T carries the row capacity here: rows >= cap_rows are never touched
+    MOE_LAUNCH("quant_rows", k_quant_bf16_rows<false>, grid_for(cap_rows, 16), kRowThreads, 0,
+               stream, (const uint4 *)x_rows, (const int32_t *)nullptr, offsets, E, cap_rows, 1,
+               (uint4 *)q1, s1, H / 8);
+    return MOE_OK;
+}
+
+moe_status launch_quant2(const float *g, const int32_t *offsets, int64_t E, void *q2, float *s2,
+                         int64_t cap_rows, int64_t Nh, cudaStream_t stream) {
+    if (cap_rows == 0) return MOE_OK;
+    MOE_LAUNCH("quant2", k_quant2, grid_for(cap_rows, 8), kQ2Threads, 0, stream,
+               (const float4 *)g, offsets, E, (uint2 *)q2, s2, Nh / 4, cap_rows);
+    return MOE_OK;
+}
+
+moe_status launch_pack_w1(const int8_t *w1, void *w1p, int64_t E, int64_t N, int64_t H,
+                          cudaStream_t stream) {
+    int64_t total = E * N * (H / 16);
+    if (total == 0) return MOE_OK;
+    MOE_LAUNCH("pack_w1", k_pack_w1, grid_for((total + 255) / 256, 8), 256, 0, stream, w1,
+               (uint4 *)w1p, E, N, H);
+    return MOE_OK;
+}
+
+moe_status launch_i8_to_f16(const int8_t *src, void *dst, int64_t n, cudaStream_t stream) {
+    int64_t n16 = n / 16;
+    if (n16 > 0) {
+        MOE_LAUNCH("i8_to_f16", k_i8_to_f16, grid_for((n16 + 255) / 256, 8), 256, 0, stream,
+                   (const int4 *)src, (uint4 *)dst, n16);
+    }
+    int64_t rem = n - n16 * 16;
+    if (rem > 0) {
+        MOE_LAUNCH("i8_to_f16_tail", k_i8_to_f16_tail, 1, 32, 0, stream, src, (__half *)dst,
+                   n16 * 16, n);
+    }
+    return MOE_OK;
+}
+
+}  // namespace moe

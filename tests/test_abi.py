@@ -1,0 +1,74 @@
+"""The C ABI library loads, exports every entry point its header declares, and
+rejects bad arguments on the host before any launch (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_gb300.h")
+
+
+@pytest.fixture(scope="module")
+def B():
+    from combine_route_count_prefix_gb300 import build as b
+    b.build()
+    from combine_route_count_prefix_gb300 import binding
+    binding.lib()
+    return binding
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_list(B):
+    assert declared_functions() == sorted(B.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(B):
+    lib = ctypes.CDLL(B.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_workspace_sizes_and_shape_checks(B):
+    s = B.make_shape(2048, 16, 7168, 256, 8)
+    assert B.dispatch_workspace_size(s) > 0
+    with pytest.raises(B.MoeError) as e:
+        B.grouped_ffn_workspace_size(s)          # N = 0: no FFN
+    assert e.value.code == 561002
+    s = B.make_shape(16384, 8, 7168, 128, 8, 4096)
+    n = B.layer_workspace_size(s)
+    cap = 16384 * 8
+    assert n >= cap * 7168 * 2 * 2 + cap * 2048 * 6      # q1 + y + g + q2
+    a, b = B.packed_weight_bytes(s)
+    assert a == 128 * 4096 * 7168 * 2 and b == 128 * 7168 * 2048 * 2
+    for bad in [B.make_shape(10, 3, 128, 8, 2),      # T % P
+                B.make_shape(16, 2, 100, 8, 2),      # H % 8
+                B.make_shape(16, 2, 128, 2000, 2),   # E too large
+                B.make_shape(16, 2, 128, 8, 17),     # K > 16
+                B.make_shape(16, 2, 128, 8, 2, 300)]:  # N % 256
+        with pytest.raises(B.MoeError):
+            B.layer_workspace_size(bad) if bad.ffn else B.dispatch_workspace_size(bad)
+
+
+def test_null_pointers_rejected_before_launch(B):
+    L = B.lib()
+    s = B.make_shape(16, 2, 128, 8, 2)
+    rc = L.moe_dispatch(ctypes.byref(s), None, None, None, None, None, None, None, None, None,
+                        None, 0, None)
+    assert rc == 161001
+    rc = L.moe_combine(ctypes.byref(s), None, None, None, None, None, None, None)
+    assert rc == 161001
+    rc = L.moe_read_device_status(None, None, None)
+    assert rc == 161001
+
+
+def test_status_strings(B):
+    L = B.lib()
+    assert L.moe_status_string(0) == b"ok"
+    assert L.moe_status_string(561003) == b"workspace too small"
