@@ -243,11 +243,13 @@ moe_status moe_dispatch(const moe_shape *shape, const void *x, const int32_t *ex
                         size_t workspace_bytes, cudaStream_t stream) {
     MOE_TRY(check_shape(shape, false));
     const moe_shape &s = *shape;
-    if (!expert_ids || !assist || !expert_token_nums || !expert_offsets || !ep_recv_counts ||
-        !route_row || !workspace)
+    // with T == 0 the per-token and per-route arrays are empty and may be NULL
+    const bool empty = s.num_tokens == 0;
+    if (!expert_token_nums || !expert_offsets || !ep_recv_counts || !workspace)
         return MOE_ERR_NULLPTR;
-    if (expand_x && !x) return MOE_ERR_NULLPTR;
-    if (s.mask_kind != 0 && !x_active_mask) return MOE_ERR_NULLPTR;
+    if (!empty && (!expert_ids || !assist || !route_row)) return MOE_ERR_NULLPTR;
+    if (!empty && expand_x && !x) return MOE_ERR_NULLPTR;
+    if (!empty && s.mask_kind != 0 && !x_active_mask) return MOE_ERR_NULLPTR;
     if (s.mask_kind == 0 && x_active_mask) return MOE_ERR_PARAM_INVALID;
     if ((expand_x && (!aligned(x, 16) || !aligned(expand_x, 16))) || !aligned(workspace, kAlign))
         return MOE_ERR_ALIGNMENT;
@@ -270,6 +272,7 @@ moe_status moe_combine(const moe_shape *shape, const void *expand_x, const int32
                        const void *shared_expert_x, void *x_out, cudaStream_t stream) {
     MOE_TRY(check_shape(shape, false));
     const moe_shape &s = *shape;
+    if (s.num_tokens == 0) return MOE_OK;
     if (!expand_x || !route_row || !expert_scales || !x_out) return MOE_ERR_NULLPTR;
     if (s.has_shared && !shared_expert_x) return MOE_ERR_NULLPTR;
     if (!s.has_shared && shared_expert_x) return MOE_ERR_PARAM_INVALID;
