@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_PKG, "_build", "libmoe_gb300.so")
 STATUS = {
     0: "MOE_OK", 161001: "MOE_ERR_NULLPTR", 161002: "MOE_ERR_PARAM_INVALID",
     561002: "MOE_ERR_SHAPE", 561003: "MOE_ERR_WORKSPACE", 561004: "MOE_ERR_ALIGNMENT",
-    561005: "MOE_ERR_CUDA", 561006: "MOE_ERR_UNSUPPORTED",
+    561005: "MOE_ERR_CUDA", 561006: "MOE_ERR_UNSUPPORTED", 561007: "MOE_ERR_TOO_LARGE",
 }
 DEV_BAD_EXPERT_ID = 0x1
 DEV_TIMEOUT = 0x2
@@ -34,6 +34,7 @@ EXPORTED = [
     "moe_grouped_gemm_s32_workspace_size", "moe_grouped_gemm_s32",
     "moe_read_device_status", "moe_launch_count", "moe_profile_enable",
     "moe_profile_report", "moe_status_string",
+    "moe_dispatch_noalloc", "moe_dispatch_noalloc_scratch_bytes",
 ]
 
 
@@ -86,6 +87,7 @@ def lib():
         "moe_read_device_status": [P, P, ctypes.POINTER(ctypes.c_int32)],
         "moe_profile_enable": [ctypes.c_int],
         "moe_profile_report": [ctypes.c_char_p, SZ],
+        "moe_dispatch_noalloc": [SP, P, P, P, P, P, P, P, P, P, P],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -93,6 +95,8 @@ def lib():
         f.restype = ctypes.c_int
     L.moe_launch_count.argtypes = []
     L.moe_launch_count.restype = ctypes.c_uint64
+    L.moe_dispatch_noalloc_scratch_bytes.argtypes = []
+    L.moe_dispatch_noalloc_scratch_bytes.restype = ctypes.c_size_t
     L.moe_status_string.argtypes = [ctypes.c_int]
     L.moe_status_string.restype = ctypes.c_char_p
     _lib = L
@@ -211,6 +215,33 @@ def dispatch(x, expert_ids, num_experts, num_partitions, mask=None, ws=None, out
           _ptr(out["expert_offsets"]), _ptr(out["ep_recv_counts"]), _ptr(out["route_row"]),
           _ptr(ws), ctypes.c_size_t(ws.numel()), _stream(stream))
     out["workspace"] = ws
+    return out
+
+
+def dispatch_noalloc(x, expert_ids, num_experts, num_partitions, mask=None, out=None,
+                     stream=None):
+    """moe_dispatch_noalloc: moe_dispatch for callers that cannot allocate
+    device memory; the routing scratch is the library's own fixed array.
+    Returns the same dict as :func:`dispatch` (without a workspace)."""
+    T, K = expert_ids.shape
+    H = x.shape[1]
+    E, P = int(num_experts), int(num_partitions)
+    dev = expert_ids.device
+    shape = make_shape(T, P, H, E, K, 0, mask_kind_of(mask, T, K))
+    _check(expert_ids, torch.int32, (T, K), "expert_ids")
+    _check(x, torch.bfloat16, (T, H), "x")
+    if out is None:
+        out = dict(
+            expand_x=torch.empty((T * K, H), dtype=torch.bfloat16, device=dev),
+            assist=torch.empty((T * K, 3), dtype=torch.int32, device=dev),
+            expert_token_nums=torch.empty(E, dtype=torch.int64, device=dev),
+            expert_offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+            ep_recv_counts=torch.empty(E * P, dtype=torch.int32, device=dev),
+            route_row=torch.empty(T * K, dtype=torch.int32, device=dev))
+    _call("moe_dispatch_noalloc", ctypes.byref(shape), _ptr(x), _ptr(expert_ids), _ptr(mask),
+          _ptr(out["expand_x"]), _ptr(out["assist"]), _ptr(out["expert_token_nums"]),
+          _ptr(out["expert_offsets"]), _ptr(out["ep_recv_counts"]), _ptr(out["route_row"]),
+          _stream(stream))
     return out
 
 

@@ -173,6 +173,7 @@ const char *moe_status_string(moe_status st) {
         case MOE_ERR_ALIGNMENT: return "pointer misaligned";
         case MOE_ERR_CUDA: return "CUDA error";
         case MOE_ERR_UNSUPPORTED: return "unsupported device";
+        case MOE_ERR_TOO_LARGE: return "problem exceeds the fixed scratch of the allocation-free entry point";
     }
     return "unknown status";
 }

@@ -54,7 +54,8 @@ typedef enum moe_status {
     MOE_ERR_WORKSPACE = 561003,      /* workspace too small */
     MOE_ERR_ALIGNMENT = 561004,      /* a pointer is not aligned as required */
     MOE_ERR_CUDA = 561005,           /* a CUDA launch or runtime call failed */
-    MOE_ERR_UNSUPPORTED = 561006     /* the device is not sm_103 / feature missing */
+    MOE_ERR_UNSUPPORTED = 561006,    /* the device is not sm_103 / feature missing */
+    MOE_ERR_TOO_LARGE = 561007       /* problem exceeds the fixed scratch of moe_dispatch_noalloc */
 } moe_status;
 
 /* Device status word bits (moe_read_device_status). */
@@ -233,6 +234,32 @@ moe_status moe_grouped_gemm_s32(int64_t rows, int64_t E, int64_t N, int64_t Kd,
                                 const int32_t *expert_offsets, const int8_t *A,
                                 const int8_t *W, int32_t *C,
                                 void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Dispatch without any device allocation by the caller.
+ * The pages have no counterpart: this entry point exists for callers that
+ * cannot allocate device memory -- a runtime whose device memory is planned
+ * once at load time, a plugin inside a framework that exposes no allocator,
+ * or a latency-critical path on which an allocation is not allowed -- and so
+ * cannot provide moe_dispatch's workspace.
+ * Same arguments and results as moe_dispatch, minus the workspace: the
+ * routing scratch lives in a fixed array in the library's own device memory
+ * (moe_dispatch_noalloc_scratch_bytes() bytes, held on every GPU that loads
+ * the library until the process exits).  Limit: chunks*E + chunks <= 262144,
+ * where chunks = P * ceil(M / 256); larger problems return MOE_ERR_TOO_LARGE
+ * before any launch.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture on the device.  All calls share the array:
+ * calls whose kernels overlap on the GPU race.  Invalid ids are treated as
+ * inactive, as in moe_dispatch; the status word is kept in the scratch and is
+ * not reported.  No cudaMalloc, cudaFree or other allocating call is made.
+ * ------------------------------------------------------------------------ */
+size_t moe_dispatch_noalloc_scratch_bytes(void);
+moe_status moe_dispatch_noalloc(const moe_shape *shape, const void *x, const int32_t *expert_ids,
+                                const uint8_t *x_active_mask, void *expand_x, int32_t *assist,
+                                int64_t *expert_token_nums, int32_t *expert_offsets,
+                                int32_t *ep_recv_counts, int32_t *route_row,
+                                cudaStream_t stream);
 
 /* Reads the device status word of `workspace` (synchronising `stream`),
  * stores it in *status_host (0 = no device-side error, else MOE_DEV_* bits)
