@@ -181,6 +181,22 @@ def identity_bytes(w, inp, R):
                 total=dispatch_rows + routing + combine)
 
 
+def max_over_ranks(v, dist, device=None):
+    """Largest value of v over all ranks (v itself without a process group)."""
+    if dist is None:
+        return float(v)
+    import torch
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tokens_per_s(tokens_per_rank, world, ms_per_step):
+    """Weak scaling: every rank processes its own tokens_per_rank per step;
+    the job's rate is all ranks' tokens over the slowest rank's step time."""
+    return world * tokens_per_rank / (ms_per_step * 1e-3)
+
+
 # ------------------------------------------------------------------ reference arm (CPU oracle)
 def run_reference(args, rank, world):
     if rank != 0:
@@ -335,12 +351,8 @@ def run_ours(args, rank, world, dist):
     launches = B.launch_count() - n0
     ms = [a.elapsed_time(b) for a, b in ev]
     clk = clocks.stop()
-    ms_step = float(np.mean(ms))
-    if dist is not None:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
-    value = world * T / (ms_step * 1e-3)
+    ms_step = max_over_ranks(float(np.mean(ms)), dist, dev)
+    value = whole_job_tokens_per_s(T, world, ms_step)
 
     # ---------------- per-kernel durations (same K steps, profiled)
     B.profile_enable(True)
@@ -402,11 +414,7 @@ def run_ours(args, rank, world, dist):
         e2e_step()
         ev2[i][1].record(stream)
     barrier()
-    e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in ev2]))
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in ev2])), dist, dev)
 
     secondary = None
     if args.layer:
@@ -422,7 +430,7 @@ def run_ours(args, rank, world, dist):
         "data": "synthetic", "config": workload_config(w),
         "hbm_gbs": step_gbs, "hbm_frac_of_peak": step_gbs / pk["hbm_gbs"],
         "roofline": roofline, "cpu_baseline": cpu,
-        "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": whole_job_tokens_per_s(T, world, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches, "clocks": clk, "routed_rows": R,
     }
