@@ -28,6 +28,7 @@ bounded sample of the same workload; under torchrun only rank 0 runs it.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -59,6 +60,12 @@ def parse():
     ap.add_argument("--layer", action="store_true",
                     help="also time the full layer workload (full_layer) as a secondary line item")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--tokens-per-partition", type=int, default=0,
+                    help="override M (tokens per partition) of the workload")
+    ap.add_argument("--experts", type=int, default=0, help="override E of the workload")
+    ap.add_argument("--soak", type=float, default=2.0,
+                    help="seconds of untimed steps before the timed region (clock samples)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
 
@@ -198,42 +205,50 @@ def whole_job_tokens_per_s(tokens_per_rank, world, ms_per_step):
 
 
 # ------------------------------------------------------------------ reference arm (CPU oracle)
-def run_reference(args, rank, world):
-    if rank != 0:
-        return
+def oracle_sample(w, inp, seed):
+    """A bounded sample of the workload for the CPU oracle: returns
+    (step callable returning tokens processed, description)."""
     import oracle
     oracle.build()
-    w = wl.WORKLOADS[args.workload]
-    inp = wl.make_inputs(w, seed=args.seed)
     M = w.tokens_per_partition
-    # bounded sample: whole partitions, sized so that one step is ~0.3-1 s
-    parts = 2 if w.identity else 1
-    S = parts * M
-    samp = dict(x=inp["x"][:S], ids=inp["ids"][:S], probs=inp["probs"][:S],
-                mask=None if inp["mask"] is None else inp["mask"][:S],
-                shared=None if inp["shared"] is None else inp["shared"][:S])
-    if not w.identity:
-        W1, S1, W2, S2 = None, None, None, None
-        n_tok = 2
-        need = sorted(set(samp["ids"][:n_tok].ravel().tolist()))
-        ws = {e: wl.expert_weights(w, e, args.seed) for e in need}
+    if w.identity:
+        parts = min(2, w.num_partitions)
+        S = parts * M
+        samp = {k: (None if v is None else v[:S]) for k, v in inp.items()}
 
-    def step():
-        if w.identity:
+        def step():
             oracle.dispatch_combine_identity(samp["x"], samp["ids"], samp["probs"], w.num_experts,
                                              parts, mask=samp["mask"], shared=samp["shared"])
             return S
-        for t in range(n_tok):
-            experts = sorted(set(samp["ids"][t].tolist()))
-            remap = {e: j for j, e in enumerate(experts)}
-            W1 = np.stack([ws[e][0] for e in experts]); S1 = np.stack([ws[e][1] for e in experts])
-            W2 = np.stack([ws[e][2] for e in experts]); S2 = np.stack([ws[e][3] for e in experts])
-            ids_l = np.vectorize(remap.get)(samp["ids"][t: t + 1]).astype(np.int32)
-            oracle.layer_tokens(samp["x"][t: t + 1], ids_l, samp["probs"][t: t + 1], W1, S1, W2, S2,
-                                np.array([0]),
-                                shared=None if samp["shared"] is None else samp["shared"][t: t + 1])
-        return n_tok
+        return step, (f"dispatch+combine of {parts} of {w.num_partitions} partitions "
+                      f"({S} tokens) per step")
+    n_tok = 1
+    need = sorted(set(inp["ids"][:n_tok].ravel().tolist()))
+    weights = {e: wl.expert_weights(w, e, seed) for e in need}
 
+    def step():
+        for t in range(n_tok):
+            experts = sorted(set(inp["ids"][t].tolist()))
+            remap = {e: j for j, e in enumerate(experts)}
+            W1 = np.stack([weights[e][0] for e in experts])
+            S1 = np.stack([weights[e][1] for e in experts])
+            W2 = np.stack([weights[e][2] for e in experts])
+            S2 = np.stack([weights[e][3] for e in experts])
+            ids_l = np.array([[remap[e] for e in inp["ids"][t]]], np.int32)
+            mask = None if inp["mask"] is None else inp["mask"][t: t + 1]
+            shared = None if inp["shared"] is None else inp["shared"][t: t + 1]
+            oracle.layer_tokens(inp["x"][t: t + 1], ids_l, inp["probs"][t: t + 1], W1, S1, W2, S2,
+                                np.array([0]), mask=mask, shared=shared)
+        return n_tok
+    return step, f"{n_tok} token per step through the whole layer (its {w.topk} experts' FFNs)"
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = select_workload(args)
+    inp = wl.make_inputs(w, seed=args.seed)
+    step, sample = oracle_sample(w, inp, args.seed)
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
@@ -242,8 +257,6 @@ def run_reference(args, rank, world):
         units += step()
     dt = time.perf_counter() - t0
     value = units / dt
-    sample = (f"{parts} of {w.num_partitions} partitions ({S} tokens) per step" if w.identity
-              else f"{n_tok} tokens per step, full FFN per token")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -267,27 +280,152 @@ def workload_config(w):
 
 
 # ------------------------------------------------------------------ our arm
-def cpu_baseline_sample(w, inp, seed):
-    """The oracle as it stands, single-threaded, on a bounded sample."""
-    import oracle
-    oracle.build()
-    M = w.tokens_per_partition
-    parts = min(4, w.num_partitions)
-    S = parts * M
+def cpu_baseline_sample(w, inp, seed, budget_s=10.0):
+    """The oracle as it stands, single-threaded, on a bounded sample of the
+    same workload, repeated for about budget_s seconds."""
+    step, sample = oracle_sample(w, inp, seed)
     t0 = time.perf_counter()
-    reps = 0
+    units = reps = 0
     while True:
-        oracle.dispatch_combine_identity(inp["x"][:S], inp["ids"][:S], inp["probs"][:S],
-                                         w.num_experts, parts,
-                                         mask=None if inp["mask"] is None else inp["mask"][:S],
-                                         shared=None if inp["shared"] is None else inp["shared"][:S])
+        units += step()
         reps += 1
         dt = time.perf_counter() - t0
-        if dt > 10.0 or reps >= 200:
+        if dt > budget_s or reps >= 500:
             break
-    return {"value": reps * S / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"dispatch+combine of {parts} of {w.num_partitions} partitions "
-                      f"({S} tokens), repeated {reps}x over {dt:.1f} s"}
+    return {"value": units / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{sample}, repeated {reps}x over {dt:.1f} s"}
+
+
+def select_workload(args):
+    w = wl.WORKLOADS[args.workload]
+    over = {}
+    if args.tokens_per_partition:
+        over["tokens_per_partition"] = args.tokens_per_partition
+    if args.experts:
+        over["num_experts"] = args.experts
+    if over:
+        suffix = "".join(f"_{k[:1]}{v}" for k, v in over.items())
+        w = dataclasses.replace(w, name=w.name + suffix, **over)
+    return w
+
+
+def device_weights(w, dev, seed):
+    """Seeded synthetic expert weights drawn on the device (same distributions as
+    the recipe; a torch generator, so that the large workloads start quickly)."""
+    import torch
+    E, N, H = w.num_experts, w.ffn, w.hidden
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    w1 = torch.randint(-127, 128, (E, N, H), dtype=torch.int8, device=dev, generator=gen)
+    w2 = torch.randint(-127, 128, (E, H, N // 2), dtype=torch.int8, device=dev, generator=gen)
+    s1 = torch.empty((E, N), device=dev).uniform_(1e-3, 1e-2, generator=gen)
+    s2 = torch.empty((E, H), device=dev).uniform_(1e-3, 1e-2, generator=gen)
+    return w1, s1, w2, s2
+
+
+class IdentityPath:
+    """moe_dispatch + moe_combine with an identity expert (y = dispatched rows)."""
+
+    def __init__(self, B, w, inp, dev):
+        import torch
+        self.B, self.w, self.inp = B, w, inp
+        T, P, H, E = w.num_tokens, w.num_partitions, w.hidden, w.num_experts
+        self.x = bf16_dev(inp["x"], dev)
+        self.ids = torch.from_numpy(inp["ids"]).to(dev)
+        self.probs = torch.from_numpy(inp["probs"]).to(dev)
+        self.mask = None if inp["mask"] is None else torch.from_numpy(inp["mask"]).to(dev)
+        self.shared = bf16_dev(inp["shared"], dev)
+        self.d = B.dispatch(self.x, self.ids, E, P, mask=self.mask)
+        self.ws = self.d["workspace"]
+        self.out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+
+    def step(self, x=None, ids=None, probs=None, mask=None, shared=None):
+        w, B, d = self.w, self.B, self.d
+        x = self.x if x is None else x
+        ids = self.ids if ids is None else ids
+        probs = self.probs if probs is None else probs
+        mask = self.mask if mask is None else mask
+        shared = self.shared if shared is None else shared
+        B.dispatch(x, ids, w.num_experts, w.num_partitions, mask=mask, ws=self.ws, out=d)
+        B.combine(d["expand_x"], d["route_row"], probs, w.num_experts, w.num_partitions,
+                  mask=mask, shared=shared, out=self.out)
+
+    def rows(self):
+        return int(self.d["expert_offsets"][-1].item())
+
+    def roofline(self, prof, pk):
+        by = identity_bytes(self.w, self.inp, self.rows())
+        dom = max(("dispatch_rows", "combine"), key=lambda k: prof.get(k, (1, 0.0))[1])
+        n, ms = prof[dom]
+        us = ms / n * 1e3
+        achieved = by[dom] / (us * 1e-6) / 1e9
+        extra = {"hbm_gbs": None, "hbm_frac_of_peak": None}
+        return dict(bound="hbm", kernel=dom, achieved=achieved, peak=pk["hbm_gbs"], unit="GB/s",
+                    frac=achieved / pk["hbm_gbs"], traffic=recorded_traffic(dom, self.w.name),
+                    algorithmic_bytes=by[dom],
+                    algorithmic_unit="bytes per launch (each byte the step must move once)",
+                    peak_source=pk["source"] + " hbm_gbs (burst copy)"), by["total"], extra
+
+    def dtype(self):
+        return "bf16"
+
+
+class LayerPath:
+    """moe_layer: routing, per-token int8 quantisation, grouped GEMM1 + SwiGLU,
+    second quantisation, grouped GEMM2 + dequant, combine."""
+
+    def __init__(self, B, w, inp, dev, seed):
+        import torch
+        self.B, self.w, self.inp = B, w, inp
+        T, P, H, E, K, N = (w.num_tokens, w.num_partitions, w.hidden, w.num_experts, w.topk,
+                            w.ffn)
+        self.x = bf16_dev(inp["x"], dev)
+        self.ids = torch.from_numpy(inp["ids"]).to(dev)
+        self.probs = torch.from_numpy(inp["probs"]).to(dev)
+        self.mask = None if inp["mask"] is None else torch.from_numpy(inp["mask"]).to(dev)
+        self.shared = bf16_dev(inp["shared"], dev)
+        self.shape = B.make_shape(T, P, H, E, K, N, w.mask_kind, w.has_shared)
+        w1, self.s1, w2, self.s2 = device_weights(w, dev, seed)
+        (self.o1, self.w1p), (self.o2, self.w2p) = B.pack_weights(self.shape, w1, w2)
+        del w1, w2
+        torch.cuda.synchronize()
+        self.out, self.ws = B.layer(self.shape, self.x, self.ids, self.probs, self.w1p, self.s1,
+                                    self.w2p, self.s2, mask=self.mask, shared=self.shared)
+
+    def step(self, x=None, ids=None, probs=None, mask=None, shared=None):
+        self.B.layer(self.shape, self.x if x is None else x, self.ids if ids is None else ids,
+                     self.probs if probs is None else probs, self.w1p, self.s1, self.w2p, self.s2,
+                     mask=self.mask if mask is None else mask,
+                     shared=self.shared if shared is None else shared, ws=self.ws, out=self.out)
+
+    def rows(self):
+        return int(self.B.stage_views(self.shape, self.ws)["expert_offsets"][-1].item())
+
+    def roofline(self, prof, pk):
+        w = self.w
+        R = self.rows()
+        fl = {"gemm1_swiglu": 2.0 * R * w.hidden * w.ffn,
+              "gemm2_dequant": 2.0 * R * (w.ffn // 2) * w.hidden}
+        dom = max(fl, key=lambda k: prof.get(k, (1, 0.0))[1])
+        n, ms = prof[dom]
+        us = ms / n * 1e3
+        achieved = fl[dom] / (us * 1e-6) / 1e12
+        other = [k for k in fl if k != dom][0]
+        n2, ms2 = prof[other]
+        extra = {"gemm_tflops": {k: fl[k] / (prof[k][1] / prof[k][0] * 1e-3) / 1e12 for k in fl},
+                 "status": self.B.read_device_status(self.ws)}
+        step_bytes = None
+        return dict(bound="tensor", kernel=dom, achieved=achieved,
+                    peak=pk["bf16_tflops_sustained"], unit="TFLOP/s",
+                    frac=achieved / pk["bf16_tflops_sustained"],
+                    traffic=recorded_traffic(dom, w.name), algorithmic_flops=fl[dom],
+                    algorithmic_unit="2*R*H*N (GEMM1) or 2*R*(N/2)*H (GEMM2) flops per launch",
+                    peak_source=pk["source"] + " bf16_tflops_sustained (cuBLAS bf16; the int8 "
+                    "products run as exact fp16-image tcgen05 kind::f16 MMAs, whose dense rate "
+                    "equals bf16's)"), step_bytes, extra
+
+    def dtype(self):
+        return "int8 GEMMs (exact, on fp16 images), fp32 epilogues, bf16 rows"
 
 
 def run_ours(args, rank, world, dist):
@@ -299,24 +437,11 @@ def run_ours(args, rank, world, dist):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
-    w = wl.WORKLOADS[args.workload]
-    if not w.identity:
-        raise SystemExit("layer workloads run with --layer")
-    T, P, H, E, K = w.num_tokens, w.num_partitions, w.hidden, w.num_experts, w.topk
+    w = select_workload(args)
+    T, H = w.num_tokens, w.hidden
     inp = wl.make_inputs(w, seed=args.seed + rank)
-    x = bf16_dev(inp["x"], dev)
-    ids = torch.from_numpy(inp["ids"]).to(dev)
-    probs = torch.from_numpy(inp["probs"]).to(dev)
-    mask = None if inp["mask"] is None else torch.from_numpy(inp["mask"]).to(dev)
-    shared = bf16_dev(inp["shared"], dev)
-    d = B.dispatch(x, ids, E, P, mask=mask)
-    ws = d["workspace"]
-    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    path = IdentityPath(B, w, inp, dev) if w.identity else LayerPath(B, w, inp, dev, args.seed + rank)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-
-    def step(xx=x, ii=ids, pp=probs, mm=mask, ss=shared, oo=out):
-        B.dispatch(xx, ii, E, P, mask=mm, ws=ws, out=d)
-        B.combine(d["expand_x"], d["route_row"], pp, E, P, mask=mm, shared=ss, out=oo)
 
     def barrier():
         torch.cuda.synchronize()
@@ -325,16 +450,16 @@ def run_ours(args, rank, world, dist):
         torch.cuda.synchronize()
 
     for _ in range(max(args.warmup, 3)):
-        step()
+        path.step()
     torch.cuda.synchronize()
-    R = int(d["expert_offsets"][-1].item())
+    R = path.rows()
     clocks = ClockSampler(local)
     clocks.start()
-    t_end = time.time() + 2.0                       # untimed soak for the clock samples
+    t_end = time.time() + args.soak                 # untimed soak for the clock samples
     while time.time() < t_end:
-        for _ in range(50):
+        for _ in range(10):
             flush.fill_(1)
-            step()
+            path.step()
         torch.cuda.synchronize()
 
     # ---------------- timed region
@@ -345,7 +470,7 @@ def run_ours(args, rank, world, dist):
     for i in range(args.steps):
         flush.fill_(1)
         ev[i][0].record(stream)
-        step()
+        path.step()
         ev[i][1].record(stream)
     barrier()
     launches = B.launch_count() - n0
@@ -358,23 +483,13 @@ def run_ours(args, rank, world, dist):
     B.profile_enable(True)
     for i in range(args.steps):
         flush.fill_(1)
-        step()
+        path.step()
     torch.cuda.synchronize()
     B.profile_enable(False)
     prof = B.profile_report()
-    per_kernel = {k: dict(launches=n, avg_us=ms_ / n * 1e3) for k, (n, ms_) in prof.items()}
-    by = identity_bytes(w, inp, R)
     pk = peaks()
-    dom = max(("dispatch_rows", "combine"), key=lambda k: prof.get(k, (1, 0.0))[1])
-    dom_bytes = by[dom]
-    dom_us = per_kernel[dom]["avg_us"]
-    achieved = dom_bytes / (dom_us * 1e-6) / 1e9
-    traffic = recorded_traffic(dom, w.name)
-    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": pk["hbm_gbs"],
-                "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
-                "algorithmic_bytes": dom_bytes, "peak_source": pk["source"] + " hbm_gbs (burst copy)",
-                "per_kernel_us": {k: round(v["avg_us"], 3) for k, v in per_kernel.items()}}
-    step_gbs = by["total"] / (ms_step * 1e-3) / 1e9
+    roofline, step_bytes, extra = path.roofline(prof, pk)
+    roofline["per_kernel_us"] = {k: round(ms_ / n * 1e3, 3) for k, (n, ms_) in prof.items()}
 
     # ---------------- end to end through the C ABI with pinned host buffers
     def pin(a):
@@ -385,9 +500,9 @@ def run_ours(args, rank, world, dist):
     hshared = pin(None if inp["shared"] is None else inp["shared"].view(np.int16))
     hout = torch.empty((T, H), dtype=torch.int16).pin_memory()
     dx = torch.empty((T, H), dtype=torch.int16, device=dev)
-    dids, dprobs = torch.empty_like(ids), torch.empty_like(probs)
-    dmask = None if mask is None else torch.empty_like(mask)
-    dshared = None if shared is None else torch.empty((T, H), dtype=torch.int16, device=dev)
+    dids, dprobs = torch.empty_like(path.ids), torch.empty_like(path.probs)
+    dmask = None if path.mask is None else torch.empty_like(path.mask)
+    dshared = None if path.shared is None else torch.empty((T, H), dtype=torch.int16, device=dev)
     h2d = sum(t.numel() * t.element_size() for t in (hx, hids, hprobs, hmask, hshared) if t is not None)
     d2h = hout.numel() * hout.element_size()
 
@@ -399,9 +514,9 @@ def run_ours(args, rank, world, dist):
             dmask.copy_(hmask, non_blocking=True)
         if dshared is not None:
             dshared.copy_(hshared, non_blocking=True)
-        step(dx.view(torch.bfloat16), dids, dprobs, dmask,
-             None if dshared is None else dshared.view(torch.bfloat16))
-        hout.copy_(out.view(torch.int16), non_blocking=True)
+        path.step(dx.view(torch.bfloat16), dids, dprobs, dmask,
+                  None if dshared is None else dshared.view(torch.bfloat16))
+        hout.copy_(path.out.view(torch.int16), non_blocking=True)
 
     for _ in range(3):
         e2e_step()
@@ -417,84 +532,32 @@ def run_ours(args, rank, world, dist):
     e2e_ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in ev2])), dist, dev)
 
     secondary = None
-    if args.layer:
+    if args.layer and w.identity:
         secondary = run_layer_secondary(args, B, dev, stream, flush, pk)
 
     if rank != 0:
         return
-    cpu = cpu_baseline_sample(w, inp, args.seed) if world == 1 else None
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_sample(w, inp, args.seed)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": path.dtype(),
         "data": "synthetic", "config": workload_config(w),
-        "hbm_gbs": step_gbs, "hbm_frac_of_peak": step_gbs / pk["hbm_gbs"],
         "roofline": roofline, "cpu_baseline": cpu,
         "e2e": {"value": whole_job_tokens_per_s(T, world, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches, "clocks": clk, "routed_rows": R,
     }
+    if step_bytes:
+        gbs = step_bytes / (ms_step * 1e-3) / 1e9
+        line["step_hbm_gbs"] = gbs
+        line["step_hbm_frac_of_peak"] = gbs / pk["hbm_gbs"]
+    line.update({k: v for k, v in extra.items() if v is not None})
     if secondary is not None:
         line["full_layer"] = secondary
     print(json.dumps(line), flush=True)
-
-
-def run_layer_secondary(args, B, dev, stream, flush, pk):
-    """Full layer workload (16384 tokens, 128 experts, FFN 4096): tokens/s and
-    the grouped GEMMs' tensor throughput.  Weights are drawn on the device with
-    a seeded torch generator (same distributions as the recipe)."""
-    import torch
-    w = wl.WORKLOADS["full_layer"]
-    T, P, H, E, K, N = w.num_tokens, w.num_partitions, w.hidden, w.num_experts, w.topk, w.ffn
-    inp = wl.make_inputs(w, seed=args.seed)
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(args.seed)
-    w1 = torch.randint(-127, 128, (E, N, H), dtype=torch.int8, device=dev, generator=gen)
-    w2 = torch.randint(-127, 128, (E, H, N // 2), dtype=torch.int8, device=dev, generator=gen)
-    s1 = torch.empty((E, N), device=dev).uniform_(1e-3, 1e-2, generator=gen)
-    s2 = torch.empty((E, H), device=dev).uniform_(1e-3, 1e-2, generator=gen)
-    shape = B.make_shape(T, P, H, E, K, N)
-    (o1, w1p), (o2, w2p) = B.pack_weights(shape, w1, w2)
-    del w1, w2
-    x = bf16_dev(inp["x"], dev)
-    ids = torch.from_numpy(inp["ids"]).to(dev)
-    probs = torch.from_numpy(inp["probs"]).to(dev)
-    out, ws = B.layer(shape, x, ids, probs, w1p, s1, w2p, s2)
-    for _ in range(3):
-        B.layer(shape, x, ids, probs, w1p, s1, w2p, s2, ws=ws, out=out)
-    torch.cuda.synchronize()
-    steps = max(3, min(args.steps, 10))
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(steps)]
-    for i in range(steps):
-        flush.fill_(1)
-        ev[i][0].record(stream)
-        B.layer(shape, x, ids, probs, w1p, s1, w2p, s2, ws=ws, out=out)
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
-    B.profile_enable(True)
-    for i in range(steps):
-        B.layer(shape, x, ids, probs, w1p, s1, w2p, s2, ws=ws, out=out)
-    torch.cuda.synchronize()
-    B.profile_enable(False)
-    prof = B.profile_report()
-    R = T * K
-    flops1, flops2 = 2.0 * R * H * N, 2.0 * R * (N // 2) * H
-    g1 = prof.get("gemm1_swiglu", (1, float("nan")))
-    g2 = prof.get("gemm2_dequant", (1, float("nan")))
-    t1 = g1[1] / g1[0] * 1e-3
-    t2 = g2[1] / g2[0] * 1e-3
-    status = B.read_device_status(ws)
-    return {"workload": w.name, "tokens_per_s": T / (ms * 1e-3), "ms_per_step": ms,
-            "gemm1_tflops": flops1 / t1 / 1e12, "gemm2_tflops": flops2 / t2 / 1e12,
-            "gemm_peak_tflops": pk["bf16_tflops_sustained"],
-            "gemm_peak_note": "measured cuBLAS bf16 (sustained); the int8 products run as exact "
-                              "fp16-image tcgen05 f16 MMAs, whose dense rate equals bf16's",
-            "gemm1_frac": flops1 / t1 / 1e12 / pk["bf16_tflops_sustained"],
-            "gemm2_frac": flops2 / t2 / 1e12 / pk["bf16_tflops_sustained"],
-            "per_kernel_us": {k: round(v[1] / v[0] * 1e3, 2) for k, v in prof.items()},
-            "device_status": status}
 
 
 def main():

@@ -261,10 +261,9 @@ moe_status moe_dispatch(const moe_shape *shape, const void *x, const int32_t *ex
     if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
     RouteDev r = route_dev(s, expert_ids, x_active_mask, workspace, L);
     MOE_TRY(launch_route(r, route_chunks(s), expert_token_nums, expert_offsets, ep_recv_counts,
-                         nullptr, route_row, assist, stream));
-    if (expand_x)
-        MOE_TRY(launch_dispatch_rows(x, route_row, expand_x, s.num_tokens, s.topk, s.hidden, stream));
-    return MOE_OK;
+                         nullptr, route_row, stream));
+    if (expand_x) return launch_dispatch_rows(r, x, route_row, assist, expand_x, s.hidden, stream);
+    return launch_route_resolve(r, route_row, assist, stream);
 }
 
 // ---------------------------------------------------------------- combine
@@ -285,7 +284,7 @@ moe_status moe_combine(const moe_shape *shape, const void *expand_x, const int32
         return MOE_ERR_ALIGNMENT;
     return launch_combine(expand_x, route_row, expert_scales, x_active_mask, s.mask_kind,
                           shared_expert_x, x_out, s.num_tokens, s.topk, s.hidden,
-                          s.num_tokens * s.topk, stream);
+                          s.num_tokens * s.topk, nullptr, stream);
 }
 
 // ---------------------------------------------------------------- weights
@@ -417,14 +416,16 @@ moe_status moe_layer(const moe_shape *shape, const void *x, const int32_t *exper
     int32_t *offsets = at<int32_t>(workspace, L.offsets);
     MOE_TRY(launch_route(r, route_chunks(s), at<int64_t>(workspace, L.counts), offsets,
                          at<int32_t>(workspace, L.recv_cum), at<int32_t>(workspace, L.sched),
-                         route_row, at<int32_t>(workspace, L.assist), stream));
+                         route_row, stream));
     if (s.num_tokens == 0) return MOE_OK;
-    MOE_TRY(launch_quant_scatter(x, route_row, at<void>(workspace, L.q1), at<float>(workspace, L.s1),
-                                 s.num_tokens, s.topk, s.hidden, stream));
+    MOE_TRY(launch_quant_scatter(r, x, route_row, at<int32_t>(workspace, L.assist),
+                                 at<void>(workspace, L.q1), at<float>(workspace, L.s1), s.hidden,
+                                 stream));
     void *y = at<void>(workspace, L.y);
     MOE_TRY(run_ffn_core(s, L, workspace, offsets, w1_packed, scale1, w2_packed, scale2, y, stream));
     return launch_combine(y, route_row, expert_scales, x_active_mask, s.mask_kind, shared_expert_x,
-                          x_out, s.num_tokens, s.topk, s.hidden, cap, stream);
+                          x_out, s.num_tokens, s.topk, s.hidden, cap,
+                          at<int32_t>(workspace, L.status), stream);
 }
 
 moe_status moe_stage_views_get(const moe_shape *shape, int for_layer, void *workspace,

@@ -31,14 +31,40 @@ int launch_begin(const char *name, cudaStream_t stream);
 void launch_end(int token, cudaStream_t stream);
 int num_sms();
 
-#define MOE_LAUNCH(name, kernel, grid, block, smem, stream, ...)              \
-    do {                                                                      \
-        int _tok = ::moe::launch_begin(name, stream);                         \
-        kernel<<<(grid), (block), (smem), (stream)>>>(__VA_ARGS__);           \
-        cudaError_t _err = cudaGetLastError();                                \
-        ::moe::launch_end(_tok, stream);                                      \
-        if (_err != cudaSuccess) return MOE_ERR_CUDA;                         \
+// Kernels are launched with programmatic stream serialization: a kernel may
+// be scheduled while its predecessor on the stream drains, and waits in
+// pdl_wait() (griddepcontrol.wait) before it reads anything the predecessor
+// wrote.  Every kernel of this library calls pdl_wait() before its first
+// dependent read.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+#define MOE_LAUNCH(name, kernel, grid, block, smem, stream, ...)                          \
+    do {                                                                                  \
+        int _tok = ::moe::launch_begin(name, stream);                                     \
+        cudaError_t _err = ::moe::launch_pdl(kernel, dim3(grid), dim3(block), (smem),     \
+                                             (stream), __VA_ARGS__);                      \
+        if (_err == cudaSuccess) _err = cudaGetLastError();                               \
+        ::moe::launch_end(_tok, stream);                                                  \
+        if (_err != cudaSuccess) return MOE_ERR_CUDA;                                     \
     } while (0)
+
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 
 #define MOE_TRY(expr)                                                         \
     do {                                                                      \
@@ -102,19 +128,53 @@ struct RouteDev {
     int32_t *status;
 };
 
+// Final row of route (t, k): route_row holds the route's rank inside its
+// routing chunk (or -1) after launch_route; the chunk base of its expert is
+// in r.hist after the scan.  Replaces route_row[t*K+k] by the row, writes
+// the row's triplet (partition, token in partition, slot) and returns the
+// row (-1 if inactive).  Called exactly once per route per call.
+__device__ __forceinline__ int32_t resolve_route_row(const RouteDev &a, int64_t t, int k,
+                                                     int32_t *route_row, int32_t *assist) {
+    const int64_t i = t * a.K + k;
+    const int32_t lr = route_row[i];
+    if (lr < 0) return -1;
+    const int e = a.ids[i];
+    const int64_t p = t / a.M;
+    const int64_t c = p * a.chunks_per_partition + (t - p * a.M) / kRouteChunkTokens;
+    const int32_t row = a.hist[c * a.E + e] + lr;
+    route_row[i] = row;
+    if (assist) {
+        assist[3 * (int64_t)row + 0] = (int32_t)p;
+        assist[3 * (int64_t)row + 1] = (int32_t)(t - p * a.M);
+        assist[3 * (int64_t)row + 2] = k;
+    }
+    return row;
+}
+
+// Routing counts and scan: afterwards route_row holds ranks inside chunks
+// (see resolve_route_row), r.hist the chunk bases.
 moe_status launch_route(const RouteDev &r, int64_t chunks, int64_t *counts, int32_t *offsets,
-                        int32_t *recv_cum, int32_t *sched, int32_t *route_row, int32_t *assist,
+                        int32_t *recv_cum, int32_t *sched, int32_t *route_row,
                         cudaStream_t stream);
+// Resolution alone, when no kernel copies or quantises the rows.
+moe_status launch_route_resolve(const RouteDev &r, int32_t *route_row, int32_t *assist,
+                                cudaStream_t stream);
 
-moe_status launch_dispatch_rows(const void *x, const int32_t *route_row, void *expand_x,
-                                int64_t T, int64_t K, int64_t H, cudaStream_t stream);
+// Resolves every route's row and copies x[t] to each of its rows.
+moe_status launch_dispatch_rows(const RouteDev &r, const void *x, int32_t *route_row,
+                                int32_t *assist, void *expand_x, int64_t H, cudaStream_t stream);
 
+// status may be NULL (bounded waits that give up then only abort the kernel).
 moe_status launch_combine(const void *y, const int32_t *route_row, const float *probs,
                           const uint8_t *mask, int mask_kind, const void *shared, void *out,
-                          int64_t T, int64_t K, int64_t H, int64_t cap_rows, cudaStream_t stream);
+                          int64_t T, int64_t K, int64_t H, int64_t cap_rows, int32_t *status,
+                          cudaStream_t stream);
 
-moe_status launch_quant_scatter(const void *x, const int32_t *route_row, void *q1, float *s1,
-                                int64_t T, int64_t K, int64_t H, cudaStream_t stream);
+// Resolves every route's row and writes the int8 codes (fp16 images) and
+// scale of the quantised token x[t] to each of its rows.
+moe_status launch_quant_scatter(const RouteDev &r, const void *x, int32_t *route_row,
+                                int32_t *assist, void *q1, float *s1, int64_t H,
+                                cudaStream_t stream);
 
 moe_status launch_quant_rows(const void *x_rows, const int32_t *offsets, int64_t E, void *q1,
                              float *s1, int64_t cap_rows, int64_t H, cudaStream_t stream);

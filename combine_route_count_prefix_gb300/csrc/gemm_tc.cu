@@ -32,6 +32,7 @@
 // Every wait is bounded: after about two seconds a wait gives up, sets
 // MOE_DEV_TIMEOUT in the status word and the CTA drains and exits.
 #include "common.cuh"
+#include "ptx.cuh"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -50,7 +51,6 @@ constexpr int CHUNK_KB = 16;         // 16 x 64 = 1024-deep exact chunk
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr unsigned long long kTimeoutNs = 2000000000ull;
 constexpr size_t kBarrierBytes = 256;
 constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + 1024 + kBarrierBytes +
                               2 * (kMaxExperts + 1) * sizeof(int32_t);
@@ -74,36 +74,6 @@ struct GemmDev {
 };
 
 // ---------------------------------------------------------------- PTX wrappers
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ uint64_t globaltimer() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
                                             int x, int y) {
     asm volatile(
@@ -189,25 +159,6 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
            | (0u << 7) | (0u << 10)         // A, B format: f16
            | ((uint32_t)(N >> 3) << 17)     // N
            | ((uint32_t)(M >> 4) << 24);    // M
-}
-
-// Waits for phase `parity` of `bar`.  Gives up when the CTA's abort flag is set
-// or after kTimeoutNs, setting the abort flag and the status bit.
-__device__ __noinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          int32_t *status, bool honour_abort = true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    for (uint32_t n = 1;; ++n) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((n & 255u) == 0) {
-            if (honour_abort && *abort_flag) return false;
-            if (globaltimer() - t0 > kTimeoutNs) {
-                *abort_flag = 1;
-                atomicOr(status, MOE_DEV_TIMEOUT);
-                return false;
-            }
-        }
-    }
 }
 
 struct Tile {
@@ -329,6 +280,11 @@ k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if (warp == 0 && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB) : "memory");
+    }
+    pdl_wait();   // everything below may read what earlier kernels wrote
     for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
         s_sched[i] = p.sched[i];
         s_off[i] = p.offsets[i];

@@ -15,19 +15,26 @@
 // number of earlier active routes with the same expert: the "token_repeat_num"
 // of the send loop, computed here as a stable counting sort.
 //
-// GB300 design (not the pages' O((BS*K)^2) per-route count): three small
-// kernels.  Routes are cut into chunks of at most 256 tokens that never cross a
-// partition boundary.
-//   k_route_count  one CTA per chunk; each warp counts a contiguous slice of
-//                  the chunk with __match_any_sync (one shared-memory add per
-//                  distinct expert per 32 routes) -> hist[chunk][e]
-//   k_route_scan   one CTA: totals, exclusive scan over experts, per-chunk
-//                  bases (scan over chunks for each expert), recv_cum, and the
-//                  GEMM m-block schedule
-//   k_route_rank   one CTA per chunk; recounts per warp, turns the counts into
-//                  per-warp bases and walks the slice again in order, giving
-//                  each route base + (same-expert lanes below it) and bumping
-//                  the base by the group size.
+// GB300 design (not the pages' O((BS*K)^2) per-route count).  Routes are cut
+// into chunks of at most 256 tokens that never cross a partition boundary.
+//   k_route_local  one CTA per chunk.  Each warp loads a contiguous slice of
+//                  the chunk (all its loads issued at once), then walks it in
+//                  order with __match_any_sync: one shared-memory add per
+//                  distinct expert per 32 routes gives every route its rank
+//                  among same-expert routes of the warp.  Warp counts are
+//                  then scanned across warps, giving each route its rank
+//                  inside the chunk (written to route_row) and the chunk's
+//                  per-expert histogram.
+//   k_route_scan   one CTA: per expert, the histograms of all chunks are
+//                  summed by several threads in parallel (contiguous chunk
+//                  ranges, independent loads), the totals are scanned over
+//                  experts (offsets), and every histogram entry is replaced
+//                  by its chunk base: offsets[e] + counts of earlier chunks.
+//                  It also writes recv_cum, the GEMM m-block schedule and the
+//                  call's status word.
+// The final row, base[chunk][e] + rank in chunk, is resolved by the kernel
+// that next touches each token (row copy, quantisation, or k_route_resolve
+// when no rows are copied), which also writes the triplet of the row.
 // No global atomics decide a position, so the result is deterministic.
 #include "common.cuh"
 
@@ -35,6 +42,7 @@ namespace moe {
 namespace {
 
 constexpr uint32_t kFull = 0xffffffffu;
+constexpr int kMaxWindows = (kRouteChunkTokens * kMaxTopK / kRouteWarps + 31) / 32;   // 16
 
 struct ChunkRange {
     int64_t r0, r1;   // route range [r0, r1) (flat index t*K + k)
@@ -52,66 +60,85 @@ __device__ __forceinline__ ChunkRange chunk_range(const RouteDev &a, int64_t c) 
     return cr;
 }
 
-// Expert of route i, -1 if masked off, -2 if active but the id is not an expert.
-__device__ __forceinline__ int route_expert(const RouteDev &a, int64_t i) {
-    if (a.mask_kind == 1 && a.mask[i / a.K] == 0) return -1;
-    if (a.mask_kind == 2 && a.mask[i] == 0) return -1;
-    int e = a.ids[i];
-    if (e < 0 || e >= a.E) return -2;
-    return e;
-}
-
-__device__ __forceinline__ void warp_slice(const ChunkRange &cr, int warp, int64_t &w0, int64_t &w1) {
-    int64_t n = cr.r1 - cr.r0;
-    int64_t per = ((n + kRouteWarps - 1) / kRouteWarps + 31) / 32 * 32;
-    w0 = min(cr.r0 + warp * per, cr.r1);
-    w1 = min(w0 + per, cr.r1);
-}
-
-// Per-warp histogram of the warp's slice into sh[warp*E + e].  Returns whether
-// the warp saw an invalid expert id.
-__device__ __forceinline__ bool warp_count(const RouteDev &a, int64_t w0, int64_t w1, int32_t *row,
-                                           int lane) {
-    bool bad = false;
-    for (int64_t base = w0; base < w1; base += 32) {
-        int64_t i = base + lane;
-        int e = (i < w1) ? route_expert(a, i) : -1;
-        if (e == -2) { bad = true; e = -1; }
-        uint32_t grp = __match_any_sync(kFull, e);
-        if (e >= 0 && lane == __ffs(grp) - 1) row[e] += __popc(grp);
-        __syncwarp();
-    }
-    return bad;
-}
-
 __global__ void __launch_bounds__(kRouteThreads)
-k_route_count(RouteDev a) {
-    extern __shared__ int32_t sh[];   // [kRouteWarps][E]
+k_route_local(RouteDev a, int32_t *local_rank) {
+    extern __shared__ int32_t hw[];   // [kRouteWarps][E] warp counts, then warp bases
+    __shared__ int any_bad;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t c = blockIdx.x;
-    for (int64_t i = tid; i < kRouteWarps * a.E; i += blockDim.x) sh[i] = 0;
-    __syncthreads();
-    ChunkRange cr = chunk_range(a, c);
-    int64_t w0, w1;
-    warp_slice(cr, warp, w0, w1);
-    bool bad = warp_count(a, w0, w1, sh + warp * a.E, lane);
-    __shared__ int any_bad;
+    for (int64_t i = tid; i < kRouteWarps * a.E; i += blockDim.x) hw[i] = 0;
     if (tid == 0) any_bad = 0;
-    __syncthreads();
+    pdl_wait();
+
+    const ChunkRange cr = chunk_range(a, c);
+    const int64_t n = cr.r1 - cr.r0;
+    const int64_t per = ((n + kRouteWarps - 1) / kRouteWarps + 31) / 32 * 32;
+    const int64_t w0 = min(cr.r0 + warp * per, cr.r1);
+    const int64_t w1 = min(w0 + per, cr.r1);
+
+    // all loads of the slice first (independent, so they are in flight together)
+    int e_reg[kMaxWindows];
+    int m_reg[kMaxWindows];
+    const int32_t K32 = (int32_t)a.K;
+#pragma unroll
+    for (int j = 0; j < kMaxWindows; ++j) {
+        const int64_t i = w0 + 32 * j + lane;
+        e_reg[j] = -1;
+        m_reg[j] = 1;
+        if (i < w1) {
+            e_reg[j] = __ldg(a.ids + i);
+            if (a.mask_kind == 1) m_reg[j] = __ldg(a.mask + (cr.r0 / K32 + (int32_t)(i - cr.r0) / K32));
+            else if (a.mask_kind == 2) m_reg[j] = __ldg(a.mask + i);
+        }
+    }
+    bool bad = false;
+#pragma unroll
+    for (int j = 0; j < kMaxWindows; ++j) {
+        int e = e_reg[j];
+        if (w0 + 32 * j + lane >= w1 || m_reg[j] == 0) e = -1;
+        else if (e < 0 || e >= a.E) { bad = true; e = -1; }
+        e_reg[j] = e;
+    }
+    __syncthreads();   // hw cleared
+
+    int32_t *mine = hw + warp * a.E;
+    int rl[kMaxWindows];
+#pragma unroll
+    for (int j = 0; j < kMaxWindows; ++j) {
+        rl[j] = -1;
+        if (w0 + 32 * j >= w1) continue;   // warp-uniform
+        const int e = e_reg[j];
+        const uint32_t grp = __match_any_sync(kFull, e);
+        if (e >= 0) rl[j] = mine[e] + __popc(grp & lanemask_lt());
+        __syncwarp();
+        if (e >= 0 && lane == __ffs(grp) - 1) mine[e] += __popc(grp);
+        __syncwarp();
+    }
     if (__any_sync(kFull, bad) && lane == 0) any_bad = 1;
     __syncthreads();
-    if (tid == 0) a.bad[c] = any_bad;
+    // warp counts -> exclusive warp bases; chunk totals -> hist
     for (int64_t e = tid; e < a.E; e += blockDim.x) {
-        int32_t s = 0;
+        int32_t run = 0;
 #pragma unroll
-        for (int w = 0; w < kRouteWarps; ++w) s += sh[w * a.E + e];
-        a.hist[c * a.E + e] = s;
+        for (int w = 0; w < kRouteWarps; ++w) {
+            const int32_t v = hw[w * a.E + e];
+            hw[w * a.E + e] = run;
+            run += v;
+        }
+        a.hist[c * a.E + e] = run;
+    }
+    if (tid == 0) a.bad[c] = any_bad;
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kMaxWindows; ++j) {
+        const int64_t i = w0 + 32 * j + lane;
+        if (i < w1) local_rank[i] = (e_reg[j] >= 0) ? rl[j] + mine[e_reg[j]] : -1;
     }
 }
 
 // Exclusive scan over a block of exactly 1024 threads; returns the thread's
 // exclusive prefix and writes the block total to *total.
-__device__ int block_exclusive_scan_1024(int v, int *scratch /*[32]*/, int *total) {
+__device__ int block_exclusive_scan_1024(int v, int *scratch /*[33]*/, int *total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int incl = v;
 #pragma unroll
@@ -143,92 +170,110 @@ __global__ void __launch_bounds__(1024)
 k_route_scan(RouteDev a, int64_t chunks, int64_t *counts, int32_t *offsets, int32_t *recv_cum,
              int32_t *sched) {
     __shared__ int scratch[33];
-    const int e = threadIdx.x;   // E <= 1024 = blockDim.x
-    int tot = 0;
-    if (e < a.E)
-        for (int64_t c = 0; c < chunks; ++c) tot += a.hist[c * a.E + e];
-    int total;
-    int off = block_exclusive_scan_1024(e < a.E ? tot : 0, scratch, &total);
-    int mblocks = (tot + kGemmBM - 1) / kGemmBM;
-    int mtotal;
-    int mstart = block_exclusive_scan_1024(e < a.E ? mblocks : 0, scratch, &mtotal);
+    __shared__ int tot_s[kMaxExperts];
+    __shared__ int off_s[kMaxExperts];
+    pdl_wait();
+    // tpe threads per expert, each over a contiguous range of chunks
+    int tpe = 1;
+    while (tpe * 2 * a.E <= 1024 && tpe < 32) tpe *= 2;
+    const int e = threadIdx.x / tpe, j = threadIdx.x % tpe;
+    const int64_t per = (chunks + tpe - 1) / tpe;
+    const int64_t c0 = min((int64_t)j * per, chunks), c1 = min(c0 + per, chunks);
+    // the first 8 chunk counts of the range stay in registers for the second pass
+    int part = 0;
+    int first[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+        first[u] = (e < a.E && c0 + u < c1) ? a.hist[(c0 + u) * a.E + e] : 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) part += first[u];
     if (e < a.E) {
-        counts[e] = tot;
-        offsets[e] = off;
-        if (sched) sched[e] = mstart;
-        int run = off;
-        for (int64_t c = 0; c < chunks; ++c) {
-            int v = a.hist[c * a.E + e];
-            a.hist[c * a.E + e] = run;
-            run += v;
-            if ((c + 1) % a.chunks_per_partition == 0 && recv_cum)
-                recv_cum[e * a.P + c / a.chunks_per_partition] = run;
+        for (int64_t c = c0 + 8; c < c1; c += 8) {
+            int v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = (c + u < c1) ? a.hist[(c + u) * a.E + e] : 0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) part += v[u];
+        }
+    }
+    // exclusive scan of the parts within the tpe-group (consecutive lanes)
+    const int lane = threadIdx.x & 31;
+    int incl = part;
+    for (int o = 1; o < tpe; o <<= 1) {
+        int v = __shfl_up_sync(kFull, incl, o);
+        if ((lane % tpe) >= o) incl += v;
+    }
+    const int excl = incl - part;
+    const int group_total = __shfl_sync(kFull, incl, (lane / tpe) * tpe + tpe - 1);
+    if (e < a.E && j == 0) tot_s[e] = group_total;
+    __syncthreads();
+    const int t = threadIdx.x;
+    const int tv = (t < a.E) ? tot_s[t] : 0;
+    int total;
+    const int off = block_exclusive_scan_1024(tv, scratch, &total);
+    int mtotal;
+    const int mstart = block_exclusive_scan_1024((t < a.E) ? (tv + kGemmBM - 1) / kGemmBM : 0,
+                                                 scratch, &mtotal);
+    if (t < a.E) {
+        off_s[t] = off;
+        counts[t] = tv;
+        offsets[t] = off;
+        if (sched) sched[t] = mstart;
+    }
+    __syncthreads();
+    if (e < a.E) {
+        int run = off_s[e] + excl;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int64_t c = c0 + u;
+            if (c < c1) {
+                a.hist[c * a.E + e] = run;
+                run += first[u];
+                if ((c + 1) % a.chunks_per_partition == 0)
+                    recv_cum[e * a.P + c / a.chunks_per_partition] = run;
+            }
+        }
+        for (int64_t cb = c0 + 8; cb < c1; cb += 8) {
+            int v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = (cb + u < c1) ? a.hist[(cb + u) * a.E + e] : 0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int64_t c = cb + u;
+                if (c < c1) {
+                    a.hist[c * a.E + e] = run;
+                    run += v[u];
+                    if ((c + 1) % a.chunks_per_partition == 0)
+                        recv_cum[e * a.P + c / a.chunks_per_partition] = run;
+                }
+            }
         }
     }
     // status word of this call: invalid ids seen by any chunk
     int bad = 0;
-    for (int64_t c = e; c < chunks; c += blockDim.x) bad |= a.bad[c];
+    for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x) bad |= a.bad[c];
     bad = __syncthreads_or(bad);
-    if (e == 0) {
+    if (threadIdx.x == 0) {
         offsets[a.E] = total;
         if (sched) sched[a.E] = mtotal;
         *a.status = bad ? MOE_DEV_BAD_EXPERT_ID : 0;
     }
 }
 
-__global__ void __launch_bounds__(kRouteThreads)
-k_route_rank(RouteDev a, int32_t *route_row, int32_t *assist) {
-    extern __shared__ int32_t sh[];   // [kRouteWarps][E]
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t c = blockIdx.x;
-    for (int64_t i = tid; i < kRouteWarps * a.E; i += blockDim.x) sh[i] = 0;
-    __syncthreads();
-    ChunkRange cr = chunk_range(a, c);
-    int64_t w0, w1;
-    warp_slice(cr, warp, w0, w1);
-    warp_count(a, w0, w1, sh + warp * a.E, lane);
-    __syncthreads();
-    // per-warp bases: chunk base from the scan plus the counts of earlier warps
-    for (int64_t e = tid; e < a.E; e += blockDim.x) {
-        int32_t run = a.hist[c * a.E + e];
-#pragma unroll
-        for (int w = 0; w < kRouteWarps; ++w) {
-            int32_t v = sh[w * a.E + e];
-            sh[w * a.E + e] = run;
-            run += v;
-        }
-    }
-    __syncthreads();
-    int32_t *base = sh + warp * a.E;
-    const int32_t pl = (int32_t)cr.p;
-    for (int64_t b = w0; b < w1; b += 32) {
-        int64_t i = b + lane;
-        int e = (i < w1) ? route_expert(a, i) : -1;
-        if (e < 0) e = -1;
-        uint32_t grp = __match_any_sync(kFull, e);
-        int row = -1;
-        if (e >= 0) row = base[e] + __popc(grp & lanemask_lt());
-        __syncwarp();
-        if (e >= 0 && lane == __ffs(grp) - 1) base[e] += __popc(grp);
-        __syncwarp();
-        if (i < w1) {
-            route_row[i] = row;
-            if (row >= 0 && assist) {
-                int64_t t = i / a.K;
-                assist[3 * (int64_t)row + 0] = pl;
-                assist[3 * (int64_t)row + 1] = (int32_t)(t - cr.p * a.M);
-                assist[3 * (int64_t)row + 2] = (int32_t)(i - t * a.K);
-            }
-        }
-    }
+__global__ void k_route_resolve(RouteDev a, int32_t *route_row, int32_t *assist) {
+    pdl_wait();
+    const int64_t n = a.T * a.K;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        resolve_route_row(a, i / a.K, (int)(i % a.K), route_row, assist);
 }
 
 // m-block schedule from offsets alone (for moe_grouped_ffn, which gets only
-// the offsets from its caller).
-// It also starts the call's status word at 0.
+// the offsets from its caller).  It also starts the call's status word at 0.
 __global__ void __launch_bounds__(1024)
 k_sched(const int32_t *offsets, int64_t E, int32_t *sched, int32_t *status) {
     __shared__ int scratch[33];
+    pdl_wait();
     const int e = threadIdx.x;
     int mb = 0;
     if (e < E) mb = max(0, offsets[e + 1] - offsets[e] + kGemmBM - 1) / kGemmBM;
@@ -244,18 +289,27 @@ k_sched(const int32_t *offsets, int64_t E, int32_t *sched, int32_t *status) {
 }  // namespace
 
 moe_status launch_route(const RouteDev &r, int64_t chunks, int64_t *counts, int32_t *offsets,
-                        int32_t *recv_cum, int32_t *sched, int32_t *route_row, int32_t *assist,
+                        int32_t *recv_cum, int32_t *sched, int32_t *route_row,
                         cudaStream_t stream) {
-    size_t smem = (size_t)kRouteWarps * r.E * sizeof(int32_t);
+    const size_t smem = (size_t)kRouteWarps * r.E * sizeof(int32_t);
     if (chunks > 0) {
-        MOE_LAUNCH("route_count", k_route_count, (unsigned)chunks, kRouteThreads, smem, stream, r);
+        MOE_LAUNCH("route_local", k_route_local, (unsigned)chunks, kRouteThreads, smem, stream, r,
+                   route_row);
     }
     MOE_LAUNCH("route_scan", k_route_scan, 1, 1024, 0, stream, r, chunks, counts, offsets,
                recv_cum, sched);
-    if (chunks > 0) {
-        MOE_LAUNCH("route_rank", k_route_rank, (unsigned)chunks, kRouteThreads, smem, stream, r,
-                   route_row, assist);
-    }
+    return MOE_OK;
+}
+
+moe_status launch_route_resolve(const RouteDev &r, int32_t *route_row, int32_t *assist,
+                                cudaStream_t stream) {
+    const int64_t n = r.T * r.K;
+    if (n == 0) return MOE_OK;
+    int64_t blocks = (n + 255) / 256;
+    const int64_t cap = (int64_t)num_sms() * 8;
+    if (blocks > cap) blocks = cap;
+    MOE_LAUNCH("route_resolve", k_route_resolve, (unsigned)blocks, 256, 0, stream, r, route_row,
+               assist);
     return MOE_OK;
 }
 

@@ -63,12 +63,15 @@ __device__ __forceinline__ float quant_code(float v, float s) {
 // ---------------------------------------------------------------- dispatch copy
 // expand_x[route_row[t*K+k]] = x[t] for every active route of token t.
 __global__ void __launch_bounds__(kRowThreads)
-k_dispatch_rows(const uint4 *__restrict__ x, const int32_t *__restrict__ route_row,
-                uint4 *__restrict__ expand_x, int64_t T, int K, int64_t H8) {
+k_dispatch_rows(RouteDev ra, const uint4 *__restrict__ x, int32_t *__restrict__ route_row,
+                int32_t *__restrict__ assist, uint4 *__restrict__ expand_x, int64_t H8) {
     __shared__ int32_t rows[kMaxTopK];
+    const int64_t T = ra.T;
+    const int K = (int)ra.K;
+    pdl_wait();
     for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
         __syncthreads();
-        if (threadIdx.x < K) rows[threadIdx.x] = route_row[t * K + threadIdx.x];
+        if (threadIdx.x < K) rows[threadIdx.x] = resolve_route_row(ra, t, threadIdx.x, route_row, assist);
         __syncthreads();
         for (int64_t j0 = threadIdx.x; j0 < H8; j0 += (int64_t)kRowThreads * kVec) {
             uint4 v[kVec];
@@ -91,94 +94,19 @@ k_dispatch_rows(const uint4 *__restrict__ x, const int32_t *__restrict__ route_r
     }
 }
 
-// ---------------------------------------------------------------- combine
-// out[t] = bf16( sum_{k active, ascending} p[t,k] * float(y[row]) + float(shared[t]) )
-// with separately rounded fp32 multiply and add (no FMA) so the result is the
-// same as the slot-ordered fp32 loop of the pages' combine.
-__global__ void __launch_bounds__(kRowThreads)
-k_combine(const uint4 *__restrict__ y, const int32_t *__restrict__ route_row,
-          const float *__restrict__ probs, const uint8_t *__restrict__ mask, int mask_kind,
-          const uint4 *__restrict__ shared, uint4 *__restrict__ out, int64_t T, int K, int64_t H8,
-          int64_t cap_rows) {
-    __shared__ int32_t rows[kMaxTopK];
-    __shared__ float ps[kMaxTopK];
-    for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
-        __syncthreads();
-        if (threadIdx.x < K) {
-            int k = threadIdx.x;
-            int32_t r = route_row[t * K + k];
-            bool on = r >= 0 && r < cap_rows;
-            if (mask_kind == 1) on = on && mask[t] != 0;
-            if (mask_kind == 2) on = on && mask[t * K + k] != 0;
-            rows[k] = on ? r : -1;
-            ps[k] = probs[t * K + k];
-        }
-        __syncthreads();
-        for (int64_t j0 = threadIdx.x; j0 < H8; j0 += (int64_t)kRowThreads * kVec) {
-            float acc[kVec][8];
-#pragma unroll
-            for (int u = 0; u < kVec; ++u)
-#pragma unroll
-                for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
-            for (int k = 0; k < K; ++k) {
-                int32_t r = rows[k];
-                if (r < 0) continue;
-                const float p = ps[k];
-                const uint4 *src = y + (int64_t)r * H8;
-                uint4 v[kVec];
-#pragma unroll
-                for (int u = 0; u < kVec; ++u) {
-                    int64_t j = j0 + (int64_t)u * kRowThreads;
-                    if (j < H8) v[u] = ld_stream(src + j);
-                }
-#pragma unroll
-                for (int u = 0; u < kVec; ++u) {
-                    float f[8];
-                    unpack_bf16x8(v[u], f);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[u][i] = __fadd_rn(acc[u][i], __fmul_rn(p, f[i]));
-                }
-            }
-            if (shared) {
-#pragma unroll
-                for (int u = 0; u < kVec; ++u) {
-                    int64_t j = j0 + (int64_t)u * kRowThreads;
-                    if (j < H8) {
-                        float f[8];
-                        unpack_bf16x8(ld_stream(shared + t * H8 + j), f);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) acc[u][i] = __fadd_rn(acc[u][i], f[i]);
-                    }
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < kVec; ++u) {
-                int64_t j = j0 + (int64_t)u * kRowThreads;
-                if (j < H8) {
-                    uint4 o;
-                    o.x = pack_bf16x2(acc[u][0], acc[u][1]);
-                    o.y = pack_bf16x2(acc[u][2], acc[u][3]);
-                    o.z = pack_bf16x2(acc[u][4], acc[u][5]);
-                    o.w = pack_bf16x2(acc[u][6], acc[u][7]);
-                    out[t * H8 + j] = o;
-                }
-            }
-        }
-    }
-}
-
 // ---------------------------------------------------------------- quantisation of bf16 rows
 // One source row (bf16, H8 vectors) -> int8 codes stored as fp16 images plus
 // the fp32 scale, written to every destination row in rows[0..ndst).
 // The whole row stays in registers: H8 <= kRowThreads * kVec (H <= 8192).
 template <bool kFromRouteTable>
 __global__ void __launch_bounds__(kRowThreads)
-k_quant_bf16_rows(const uint4 *__restrict__ src, const int32_t *__restrict__ route_row,
-                  const int32_t *__restrict__ offsets, int64_t E, int64_t T, int K,
-                  uint4 *__restrict__ q, float *__restrict__ s_out, int64_t H8) {
+k_quant_bf16_rows(RouteDev ra, const uint4 *__restrict__ src, int32_t *__restrict__ route_row,
+                  int32_t *__restrict__ assist, const int32_t *__restrict__ offsets, int64_t E,
+                  int64_t T, int K, uint4 *__restrict__ q, float *__restrict__ s_out, int64_t H8) {
     __shared__ int32_t rows[kMaxTopK];
     __shared__ int32_t nrows;
     __shared__ float scratch[32];
+    pdl_wait();
     // kFromRouteTable: one iteration per token t, destinations = its active routes.
     // otherwise:       one iteration per dispatched row r < offsets[E], destination = r.
     const int64_t n_items = kFromRouteTable ? T : min((int64_t)offsets[E], T);
@@ -188,7 +116,7 @@ k_quant_bf16_rows(const uint4 *__restrict__ src, const int32_t *__restrict__ rou
             int n = 0;
             if (kFromRouteTable) {
                 for (int k = 0; k < K; ++k) {
-                    int32_t r = route_row[it * K + k];
+                    int32_t r = resolve_route_row(ra, it, k, route_row, assist);
                     if (r >= 0) rows[n++] = r;
                 }
             } else {
@@ -241,39 +169,65 @@ k_quant_bf16_rows(const uint4 *__restrict__ src, const int32_t *__restrict__ rou
 
 // ---------------------------------------------------------------- second quantisation
 // g fp32 [rows, Nh] -> q2 fp16 images + s2, for rows r < offsets[E].
-// Each thread holds up to kQ2Vec float4 of the row (Nh <= 256 * 4 * kQ2Vec).
+// One warp per row: the row's amax is a warp reduction, no block barrier, and
+// a CTA keeps 8 rows in flight.  Rows up to 32 * 4 * kQ2Vec floats stay in
+// registers; longer rows are read twice (the second read hits L2).
 constexpr int kQ2Threads = 256;
-constexpr int kQ2Vec = 4;
+constexpr int kQ2Vec = 16;
 __global__ void __launch_bounds__(kQ2Threads)
 k_quant2(const float4 *__restrict__ g, const int32_t *__restrict__ offsets, int64_t E,
          uint2 *__restrict__ q2, float *__restrict__ s2, int64_t Nh4, int64_t cap_rows) {
-    __shared__ float scratch[32];
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
     const int64_t R = min((int64_t)offsets[E], cap_rows);
-    for (int64_t r = blockIdx.x; r < R; r += gridDim.x) {
-        float4 v[kQ2Vec];
+    const int64_t warps = (int64_t)gridDim.x * (kQ2Threads / 32);
+    for (int64_t r = blockIdx.x * (int64_t)(kQ2Threads / 32) + (threadIdx.x >> 5); r < R;
+         r += warps) {
+        const float4 *src = g + r * Nh4;
+        uint2 *dst = q2 + r * Nh4;
         float amax = 0.0f;
+        if (Nh4 <= 32 * kQ2Vec) {
+            float4 v[kQ2Vec];
 #pragma unroll
-        for (int u = 0; u < kQ2Vec; ++u) {
-            int64_t j = threadIdx.x + (int64_t)u * kQ2Threads;
-            if (j < Nh4) {
-                v[u] = __ldcs(g + r * Nh4 + j);
+            for (int u = 0; u < kQ2Vec; ++u) {
+                const int64_t j = lane + 32 * u;
+                v[u] = (j < Nh4) ? __ldcs(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < kQ2Vec; ++u)
                 amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)),
                                          fmaxf(fabsf(v[u].z), fabsf(v[u].w))));
-            }
-        }
-        amax = block_max(amax, scratch);
-        const float s = __fdiv_rn(amax, 127.0f);
 #pragma unroll
-        for (int u = 0; u < kQ2Vec; ++u) {
-            int64_t j = threadIdx.x + (int64_t)u * kQ2Threads;
-            if (j < Nh4) {
-                uint2 o;
-                o.x = pack_half2(quant_code(v[u].x, s), quant_code(v[u].y, s));
-                o.y = pack_half2(quant_code(v[u].z, s), quant_code(v[u].w, s));
-                q2[r * Nh4 + j] = o;
+            for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+            const float s = __fdiv_rn(amax, 127.0f);
+#pragma unroll
+            for (int u = 0; u < kQ2Vec; ++u) {
+                const int64_t j = lane + 32 * u;
+                if (j < Nh4) {
+                    uint2 o;
+                    o.x = pack_half2(quant_code(v[u].x, s), quant_code(v[u].y, s));
+                    o.y = pack_half2(quant_code(v[u].z, s), quant_code(v[u].w, s));
+                    dst[j] = o;
+                }
             }
+            if (lane == 0) s2[r] = s;
+        } else {
+            for (int64_t j = lane; j < Nh4; j += 32) {
+                const float4 v = src[j];
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+            const float s = __fdiv_rn(amax, 127.0f);
+            for (int64_t j = lane; j < Nh4; j += 32) {
+                const float4 v = src[j];
+                uint2 o;
+                o.x = pack_half2(quant_code(v.x, s), quant_code(v.y, s));
+                o.y = pack_half2(quant_code(v.z, s), quant_code(v.w, s));
+                dst[j] = o;
+            }
+            if (lane == 0) s2[r] = s;
         }
-        if (threadIdx.x == 0) s2[r] = s;
     }
 }
 
@@ -289,6 +243,7 @@ __device__ __forceinline__ void i8x16_to_f16(const int4 &in, uint4 &lo, uint4 &h
 }
 
 __global__ void k_i8_to_f16(const int4 *__restrict__ src, uint4 *__restrict__ dst, int64_t n16) {
+    pdl_wait();
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16;
          i += (int64_t)gridDim.x * blockDim.x) {
         uint4 lo, hi;
@@ -300,6 +255,7 @@ __global__ void k_i8_to_f16(const int4 *__restrict__ src, uint4 *__restrict__ ds
 
 __global__ void k_i8_to_f16_tail(const int8_t *__restrict__ src, __half *__restrict__ dst,
                                  int64_t start, int64_t n) {
+    pdl_wait();
     int64_t i = start + blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
     if (i < n) dst[i] = __float2half_rn((float)src[i]);
 }
@@ -311,6 +267,7 @@ __global__ void k_i8_to_f16_tail(const int8_t *__restrict__ src, __half *__restr
 // so one 256-column GEMM tile carries 128 complete SwiGLU pairs.
 __global__ void k_pack_w1(const int8_t *__restrict__ w1, uint4 *__restrict__ out, int64_t E,
                           int64_t N, int64_t H) {
+    pdl_wait();
     const int64_t H16 = H / 16;
     const int64_t total = E * N * H16;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
@@ -336,30 +293,21 @@ int grid_for(int64_t items, int per_sm) {
 
 }  // namespace
 
-moe_status launch_dispatch_rows(const void *x, const int32_t *route_row, void *expand_x,
-                                int64_t T, int64_t K, int64_t H, cudaStream_t stream) {
-    if (T == 0) return MOE_OK;
-    MOE_LAUNCH("dispatch_rows", k_dispatch_rows, grid_for(T, 16), kRowThreads, 0, stream,
-               (const uint4 *)x, route_row, (uint4 *)expand_x, T, (int)K, H / 8);
+moe_status launch_dispatch_rows(const RouteDev &r, const void *x, int32_t *route_row,
+                                int32_t *assist, void *expand_x, int64_t H, cudaStream_t stream) {
+    if (r.T == 0) return MOE_OK;
+    MOE_LAUNCH("dispatch_rows", k_dispatch_rows, grid_for(r.T, 16), kRowThreads, 0, stream, r,
+               (const uint4 *)x, route_row, assist, (uint4 *)expand_x, H / 8);
     return MOE_OK;
 }
 
-moe_status launch_combine(const void *y, const int32_t *route_row, const float *probs,
-                          const uint8_t *mask, int mask_kind, const void *shared, void *out,
-                          int64_t T, int64_t K, int64_t H, int64_t cap_rows, cudaStream_t stream) {
-    if (T == 0) return MOE_OK;
-    MOE_LAUNCH("combine", k_combine, grid_for(T, 16), kRowThreads, 0, stream, (const uint4 *)y,
-               route_row, probs, mask, mask_kind, (const uint4 *)shared, (uint4 *)out, T, (int)K,
-               H / 8, cap_rows);
-    return MOE_OK;
-}
-
-moe_status launch_quant_scatter(const void *x, const int32_t *route_row, void *q1, float *s1,
-                                int64_t T, int64_t K, int64_t H, cudaStream_t stream) {
-    if (T == 0) return MOE_OK;
-    MOE_LAUNCH("quant_scatter", k_quant_bf16_rows<true>, grid_for(T, 16), kRowThreads, 0, stream,
-               (const uint4 *)x, route_row, (const int32_t *)nullptr, (int64_t)0, T, (int)K,
-               (uint4 *)q1, s1, H / 8);
+moe_status launch_quant_scatter(const RouteDev &r, const void *x, int32_t *route_row,
+                                int32_t *assist, void *q1, float *s1, int64_t H,
+                                cudaStream_t stream) {
+    if (r.T == 0) return MOE_OK;
+    MOE_LAUNCH("quant_scatter", k_quant_bf16_rows<true>, grid_for(r.T, 16), kRowThreads, 0, stream,
+               r, (const uint4 *)x, route_row, assist, (const int32_t *)nullptr, (int64_t)0, r.T,
+               (int)r.K, (uint4 *)q1, s1, H / 8);
     return MOE_OK;
 }
 
@@ -368,7 +316,8 @@ moe_status launch_quant_rows(const void *x_rows, const int32_t *offsets, int64_t
     if (cap_rows == 0) return MOE_OK;
     // T carries the row capacity here: rows >= cap_rows are never touched
     MOE_LAUNCH("quant_rows", k_quant_bf16_rows<false>, grid_for(cap_rows, 16), kRowThreads, 0,
-               stream, (const uint4 *)x_rows, (const int32_t *)nullptr, offsets, E, cap_rows, 1,
+               stream, RouteDev{}, (const uint4 *)x_rows, (int32_t *)nullptr, (int32_t *)nullptr,
+               offsets, E, cap_rows, 1,
                (uint4 *)q1, s1, H / 8);
     return MOE_OK;
 }
@@ -376,7 +325,7 @@ moe_status launch_quant_rows(const void *x_rows, const int32_t *offsets, int64_t
 moe_status launch_quant2(const float *g, const int32_t *offsets, int64_t E, void *q2, float *s2,
                          int64_t cap_rows, int64_t Nh, cudaStream_t stream) {
     if (cap_rows == 0) return MOE_OK;
-    MOE_LAUNCH("quant2", k_quant2, grid_for(cap_rows, 8), kQ2Threads, 0, stream,
+    MOE_LAUNCH("quant2", k_quant2, grid_for((cap_rows + 7) / 8, 8), kQ2Threads, 0, stream,
                (const float4 *)g, offsets, E, (uint2 *)q2, s2, Nh / 4, cap_rows);
     return MOE_OK;
 }
