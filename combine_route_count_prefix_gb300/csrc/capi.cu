@@ -71,7 +71,8 @@ int num_sms() {
 int64_t route_chunks(const moe_shape &s) {
     if (s.num_tokens == 0) return 0;
     const int64_t M = s.num_tokens / s.num_partitions;
-    return s.num_partitions * ((M + kRouteChunkTokens - 1) / kRouteChunkTokens);
+    const int64_t ct = route_chunk_tokens(s.num_tokens);
+    return s.num_partitions * ((M + ct - 1) / ct);
 }
 
 moe_status check_shape(const moe_shape *s, bool need_ffn) {
@@ -147,7 +148,8 @@ static RouteDev route_dev(const moe_shape &s, const int32_t *ids, const uint8_t 
     r.M = s.num_tokens / s.num_partitions;
     r.K = s.topk;
     r.E = s.num_experts;
-    r.chunks_per_partition = (r.M + kRouteChunkTokens - 1) / kRouteChunkTokens;
+    r.chunk_tokens = route_chunk_tokens(r.T);
+    r.chunks_per_partition = (r.M + r.chunk_tokens - 1) / r.chunk_tokens;
     if (r.chunks_per_partition == 0) r.chunks_per_partition = 1;
     const int64_t C = route_chunks(s);
     r.hist = at<int32_t>(ws, L.hist);

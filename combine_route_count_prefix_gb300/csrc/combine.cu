@@ -8,27 +8,60 @@
 // expert term of "aclnnMoeDistributeCombineV4" (Function/Formula) added once
 // after the routed sum, back in token order ("PTO MegaMoE ...", Unpermute).
 //
-// GB300 design: the work item is one part (at most 512 16-byte vectors, i.e.
-// half of a 7168-wide row) of one token, so a 2048-token batch has 4096 items
-// and the last wave is short.  A CTA of 256 threads takes one item at a time:
-// threads 0..K-1 fetch the token's route rows and probabilities into shared
-// memory, then every thread issues the loads of its two vectors of ALL active
-// rows (and of the shared-expert row) before it accumulates them in slot
-// order, so 8 rows x 7 KB per CTA, two CTAs per SM, are in flight at once.
+// GB300 design: a persistent kernel, one CTA per SM, that moves whole
+// contiguous row segments through shared memory with bulk (TMA) copies.  A
+// work item is one segment (about half of a 7168-wide row) of one token; each
+// CTA owns a contiguous block of tokens.  Warp 0 produces: its lanes load the
+// route rows, mask bits and probabilities of 32 tokens into registers (all
+// loads issued together, and the next batch's loads in flight while the
+// current batch is issued), and lane 0 walks the items: wait for a free stage,
+// write the item header (active slot count and their probabilities), arm the
+// stage's mbarrier with the byte count, and issue one bulk copy per active row
+// segment and one for the shared-expert segment.  Warps 1..8 consume a stage:
+// each thread owns up to two 16-byte vectors of the segment, accumulates the
+// rows from shared memory in slot order and stores the bf16 result.  Several
+// segments of ~7 KB per row are in flight per SM; the copies bypass the SM's
+// load-tracking limits and keep DRAM reads long and contiguous.  CTA b takes
+// tokens b, b + G, b + 2G, ... (G CTAs), so the tokens in flight at any time
+// are close together and so are their rows inside each expert's block.
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kSlots = 2;                          // 16-byte vectors per thread per row
-constexpr int kPartVecs = kThreads * kSlots;       // vectors per work item
-constexpr int kRowsInFlight = 8;                   // rows loaded before accumulating
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = 32 * (1 + kConsumerWarps);
+constexpr int kVecsPerThread = 2;
+constexpr int kMaxSegVecs = kConsumerWarps * 32 * kVecsPerThread;   // 512 vectors = 8 KB
+constexpr int kMaxStages = 8;
+constexpr size_t kStageTarget = 64 * 1024;
+constexpr size_t kSmemBudget = 196 * 1024;
+constexpr uint32_t kFull = 0xffffffffu;
 
-__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+struct ItemHdr {
+    int32_t n;
+    int32_t pad[3];
+    float p[kMaxTopK];
+};
+
+struct CombineArgs {
+    const uint4 *y;
+    const int32_t *route_row;
+    const float *probs;
+    const uint8_t *mask;
+    const uint4 *shared;
+    uint4 *out;
+    int64_t T, H8, cap_rows, tokens_per_cta;
+    int K, mask_kind, stages, nseg, seg_vecs;
+    int32_t *status;
+};
+
+__device__ __forceinline__ uint4 lds128(const void *p) {
     uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(smem_u32(p)));
     return v;
 }
 
@@ -46,87 +79,188 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
-k_combine(const uint4 *__restrict__ y, const int32_t *__restrict__ route_row,
-          const float *__restrict__ probs, const uint8_t *__restrict__ mask, int mask_kind,
-          const uint4 *__restrict__ shared, uint4 *__restrict__ out, int64_t T, int K, int64_t H8,
-          int64_t cap_rows, int nparts) {
-    __shared__ int32_t rows_s[kMaxTopK];
-    __shared__ float ps_s[kMaxTopK];
+__host__ __device__ inline size_t stage_bytes(int K, int seg_vecs) { return (size_t)(K + 1) * seg_vecs * 16; }
+
+size_t smem_bytes(int K, int stages, int seg_vecs) {
+    return 128 + (size_t)stages * stage_bytes(K, seg_vecs) + stages * sizeof(ItemHdr) +
+           2 * stages * sizeof(uint64_t) + 16 + 2 * 32 * (size_t)K * (sizeof(int32_t) + sizeof(float));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+k_combine(CombineArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                                ~(uintptr_t)127);
+    const size_t sbytes = stage_bytes(a.K, a.seg_vecs);
+    uint8_t *bufs = smem;
+    ItemHdr *hdrs = reinterpret_cast<ItemHdr *>(bufs + a.stages * sbytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(hdrs + a.stages);
+    uint64_t *empty = full + a.stages;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + a.stages);
+    int32_t *meta_row = reinterpret_cast<int32_t *>(empty + a.stages) + 4;   // [2][32*K]
+    float *meta_p = reinterpret_cast<float *>(meta_row + 2 * 32 * a.K);    // [2][32*K]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
     pdl_wait();
-    const int64_t items = T * nparts;
-    const int64_t per = (H8 + nparts - 1) / nparts;
-    for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
-        const int64_t t = it / nparts;
-        const int64_t v0 = (it % nparts) * per;
-        const int64_t v1 = min(v0 + per, H8);
-        __syncthreads();
-        if (threadIdx.x < K) {
-            const int k = threadIdx.x;
-            const int32_t r = route_row[t * K + k];
-            bool on = r >= 0 && r < cap_rows;
-            if (mask_kind == 1) on = on && mask[t] != 0;
-            if (mask_kind == 2) on = on && mask[t * K + k] != 0;
-            rows_s[k] = on ? r : -1;
-            ps_s[k] = probs[t * K + k];
-        }
-        __syncthreads();
-        float acc[kSlots][8];
+
+    // this CTA's tokens: blockIdx.x + G * i for i in [0, ntok)
+    const int64_t G = gridDim.x;
+    const int64_t ntok = (a.T - blockIdx.x + G - 1) / G;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued_phase[kMaxStages];
 #pragma unroll
-        for (int u = 0; u < kSlots; ++u)
+        for (int s = 0; s < kMaxStages; ++s) issued_phase[s] = -1;
+        bool ok = true;
+        int32_t rr[kMaxTopK];
+        float pp[kMaxTopK];
+        // metadata of the batch starting at tb, for token tb + lane, into registers
+        auto load_meta = [&](int64_t ib) {
+            const bool in = ib + lane < ntok;
+            const int64_t t = blockIdx.x + G * (ib + lane);
+            const bool tok = in && (a.mask_kind != 1 || a.mask[t] != 0);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
-        // the shared-expert vectors are requested together with the rows
-        uint4 sv[kSlots];
-#pragma unroll
-        for (int u = 0; u < kSlots; ++u) {
-            const int64_t j = v0 + threadIdx.x + (int64_t)u * kThreads;
-            sv[u] = make_uint4(0, 0, 0, 0);
-            if (shared && j < v1) sv[u] = ld_stream(shared + t * H8 + j);
-        }
-        for (int kb = 0; kb < K; kb += kRowsInFlight) {
-            uint4 v[kRowsInFlight][kSlots];
-#pragma unroll
-            for (int q = 0; q < kRowsInFlight; ++q) {
-                const int k = kb + q;
-                const int32_t r = (k < K) ? rows_s[k] : -1;
-#pragma unroll
-                for (int u = 0; u < kSlots; ++u) {
-                    const int64_t j = v0 + threadIdx.x + (int64_t)u * kThreads;
-                    v[q][u] = make_uint4(0, 0, 0, 0);
-                    if (r >= 0 && j < v1) v[q][u] = ld_stream(y + (int64_t)r * H8 + j);
+            for (int k = 0; k < kMaxTopK; ++k) {
+                rr[k] = -1;
+                pp[k] = 0.0f;
+                if (k < a.K && in) {
+                    rr[k] = a.route_row[t * a.K + k];
+                    pp[k] = a.probs[t * a.K + k];
                 }
             }
 #pragma unroll
-            for (int q = 0; q < kRowsInFlight; ++q) {
-                const int k = kb + q;
-                if (k >= K || rows_s[k] < 0) continue;
-                const float p = ps_s[k];
+            for (int k = 0; k < kMaxTopK; ++k) {
+                if (k >= a.K) break;
+                bool on = tok && rr[k] >= 0 && rr[k] < a.cap_rows;
+                if (a.mask_kind == 2 && in) on = on && a.mask[t * a.K + k] != 0;
+                rr[k] = on ? rr[k] : -1;
+            }
+        };
+        auto store_meta = [&](int buf) {
+            int32_t *mr = meta_row + buf * 32 * a.K + lane * a.K;
+            float *mp = meta_p + buf * 32 * a.K + lane * a.K;
 #pragma unroll
-                for (int u = 0; u < kSlots; ++u) {
-                    float f[8];
-                    unpack8(v[q][u], f);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[u][i] = __fadd_rn(acc[u][i], __fmul_rn(p, f[i]));
+            for (int k = 0; k < kMaxTopK; ++k) {
+                if (k >= a.K) break;
+                mr[k] = rr[k];
+                mp[k] = pp[k];
+            }
+        };
+        if (ntok > 0) {
+            load_meta(0);
+            store_meta(0);
+        }
+        __syncwarp();
+        int buf = 0;
+        for (int64_t ib = 0; ib < ntok; ib += 32) {
+            const bool more = ib + 32 < ntok;
+            if (more) load_meta(ib + 32);          // in flight while this batch is issued
+            if (lane == 0 && ok) {
+                const int64_t ie = min(ib + 32, ntok);
+                for (int64_t ii = ib; ok && ii < ie; ++ii) {
+                    const int64_t tt = blockIdx.x + G * ii;
+                    const int32_t *rows = meta_row + buf * 32 * a.K + (ii - ib) * a.K;
+                    const float *ps = meta_p + buf * 32 * a.K + (ii - ib) * a.K;
+                    for (int seg = 0; seg < a.nseg; ++seg) {
+                        if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, a.status)) {
+                            ok = false;
+                            break;
+                        }
+                        const int64_t v0 = (int64_t)seg * a.seg_vecs;
+                        const uint32_t bytes = (uint32_t)(min((int64_t)a.seg_vecs, a.H8 - v0) * 16);
+                        ItemHdr *h = hdrs + stage;
+                        uint8_t *dst = bufs + stage * sbytes;
+                        int n = 0;
+                        for (int k = 0; k < a.K; ++k)
+                            if (rows[k] >= 0) h->p[n++] = ps[k];
+                        h->n = n;
+                        mbar_arrive_expect_tx(&full[stage], (uint32_t)(n + (a.shared ? 1 : 0)) * bytes);
+                        int jj = 0;
+                        for (int k = 0; k < a.K; ++k) {
+                            if (rows[k] < 0) continue;
+                            bulk_load(dst + (size_t)jj * a.seg_vecs * 16,
+                                      a.y + (int64_t)rows[k] * a.H8 + v0, bytes, &full[stage]);
+                            ++jj;
+                        }
+                        if (a.shared)
+                            bulk_load(dst + (size_t)a.K * a.seg_vecs * 16, a.shared + tt * a.H8 + v0,
+                                      bytes, &full[stage]);
+                        issued_phase[stage] = (int)phase;
+                        if (++stage == a.stages) { stage = 0; phase ^= 1u; }
+                    }
                 }
             }
+            ok = __shfl_sync(kFull, ok, 0);
+            __syncwarp();
+            if (more) store_meta(buf ^ 1);
+            __syncwarp();
+            buf ^= 1;
+            if (!ok) break;
         }
+        // every copy issued must have landed before the CTA exits
+        if (lane == 0)
+            for (int s = 0; s < a.stages; ++s)
+                if (issued_phase[s] >= 0)
+                    wait_bounded(&full[s], (uint32_t)issued_phase[s], abort_flag, a.status, false);
+    } else {
+        // ------------------------------------------------------------ consumers
+        const int c = threadIdx.x - 32;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int64_t ii = 0; ok && ii < ntok; ++ii) {
+            const int64_t tt = blockIdx.x + G * ii;
+            for (int seg = 0; seg < a.nseg; ++seg) {
+                const bool w = wait_bounded(&full[stage], phase, abort_flag, a.status);
+                if (!__all_sync(kFull, w)) { ok = false; break; }
+                const ItemHdr *h = hdrs + stage;
+                const uint8_t *src = bufs + stage * sbytes;
+                const int64_t v0 = (int64_t)seg * a.seg_vecs;
+                const int len = (int)min((int64_t)a.seg_vecs, a.H8 - v0);
+                const int n = h->n;
 #pragma unroll
-        for (int u = 0; u < kSlots; ++u) {
-            const int64_t j = v0 + threadIdx.x + (int64_t)u * kThreads;
-            if (j >= v1) continue;
-            if (shared) {
-                float f[8];
-                unpack8(sv[u], f);
+                for (int u = 0; u < kVecsPerThread; ++u) {
+                    const int v = c + u * kConsumerWarps * 32;
+                    if (v >= len) continue;
+                    float acc[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) acc[u][i] = __fadd_rn(acc[u][i], f[i]);
+                    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+                    for (int jj = 0; jj < n; ++jj) {
+                        float f[8];
+                        unpack8(lds128(src + ((size_t)jj * a.seg_vecs + v) * 16), f);
+                        const float p = h->p[jj];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(p, f[i]));
+                    }
+                    if (a.shared) {
+                        float f[8];
+                        unpack8(lds128(src + ((size_t)a.K * a.seg_vecs + v) * 16), f);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], f[i]);
+                    }
+                    uint4 o;
+                    o.x = pack_bf16x2(acc[0], acc[1]);
+                    o.y = pack_bf16x2(acc[2], acc[3]);
+                    o.z = pack_bf16x2(acc[4], acc[5]);
+                    o.w = pack_bf16x2(acc[6], acc[7]);
+                    a.out[tt * a.H8 + v0 + v] = o;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[stage]);
+                if (++stage == a.stages) { stage = 0; phase ^= 1u; }
             }
-            uint4 o;
-            o.x = pack_bf16x2(acc[u][0], acc[u][1]);
-            o.y = pack_bf16x2(acc[u][2], acc[u][3]);
-            o.z = pack_bf16x2(acc[u][4], acc[u][5]);
-            o.w = pack_bf16x2(acc[u][6], acc[u][7]);
-            out[t * H8 + j] = o;
         }
     }
 }
@@ -137,15 +271,39 @@ moe_status launch_combine(const void *y, const int32_t *route_row, const float *
                           const uint8_t *mask, int mask_kind, const void *shared, void *out,
                           int64_t T, int64_t K, int64_t H, int64_t cap_rows, int32_t *status,
                           cudaStream_t stream) {
-    (void)status;
     if (T == 0) return MOE_OK;
-    const int64_t H8 = H / 8;
-    const int nparts = (int)((H8 + kPartVecs - 1) / kPartVecs);
-    int64_t grid = (int64_t)num_sms() * 2;
-    if (grid > T * nparts) grid = T * nparts;
-    MOE_LAUNCH("combine", k_combine, (unsigned)grid, kThreads, 0, stream, (const uint4 *)y,
-               route_row, probs, mask, mask_kind, (const uint4 *)shared, (uint4 *)out, T, (int)K,
-               H8, cap_rows, nparts);
+    CombineArgs a;
+    a.y = static_cast<const uint4 *>(y);
+    a.route_row = route_row;
+    a.probs = probs;
+    a.mask = mask;
+    a.shared = static_cast<const uint4 *>(shared);
+    a.out = static_cast<uint4 *>(out);
+    a.T = T;
+    a.H8 = H / 8;
+    a.cap_rows = cap_rows;
+    a.K = (int)K;
+    a.mask_kind = mask_kind;
+    // segment length: at most 512 vectors and about 64 KB per stage over K+1 rows
+    int64_t maxv = (int64_t)(kStageTarget / ((size_t)(K + 1) * 16));
+    if (maxv > kMaxSegVecs) maxv = kMaxSegVecs;
+    a.nseg = (int)((a.H8 + maxv - 1) / maxv);
+    a.seg_vecs = (int)((a.H8 + a.nseg - 1) / a.nseg);
+    a.stages = (int)(kSmemBudget / stage_bytes(a.K, a.seg_vecs));
+    if (a.stages > kMaxStages) a.stages = kMaxStages;
+    if (a.stages < 2) a.stages = 2;
+    const int64_t grid = T < num_sms() ? T : (int64_t)num_sms();
+    a.tokens_per_cta = 0;
+    a.status = status;
+    const size_t smem = smem_bytes(a.K, a.stages, a.seg_vecs);
+    static size_t configured = 0;
+    if (smem > configured) {
+        if (cudaFuncSetAttribute(k_combine, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        configured = smem;
+    }
+    MOE_LAUNCH("combine", k_combine, (unsigned)grid, kThreads, smem, stream, a);
     return MOE_OK;
 }
 

@@ -16,7 +16,7 @@ constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 16;
 constexpr int kRouteThreads = 256;
 constexpr int kRouteWarps = kRouteThreads / 32;
-constexpr int kRouteChunkTokens = 256;   // tokens per routing chunk (within one partition)
+constexpr int kRouteChunkTokensMax = 256;   // routing chunks never cross a partition
 constexpr int kGemmBM = 128;             // GEMM tile rows (routed rows)
 constexpr int kGemmBN = 256;             // GEMM tile columns (output channels)
 constexpr size_t kAlign = 1024;
@@ -62,8 +62,13 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
         if (_err != cudaSuccess) return MOE_ERR_CUDA;                                     \
     } while (0)
 
+// Waits for the predecessor grid (its writes are visible afterwards), then
+// lets the next kernel on the stream be launched: its CTAs are scheduled as
+// resources free up and wait in their own pdl_wait, so its launch latency
+// overlaps this kernel's execution.
 __device__ __forceinline__ void pdl_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 #define MOE_TRY(expr)                                                         \
@@ -117,11 +122,20 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 // (host functions implemented in the .cu files, used by capi.cu)
 namespace moe {
 
+// Tokens per routing chunk: small batches use small chunks (more CTAs, a
+// shorter serial walk per warp), large ones up to 256.  A function of T only.
+inline int64_t route_chunk_tokens(int64_t T) {
+    int64_t c = 64;
+    while (c < kRouteChunkTokensMax && c * 128 < T) c *= 2;
+    return c;
+}
+
 struct RouteDev {
     const int32_t *ids;
     const uint8_t *mask;
     int mask_kind;
     int64_t T, P, M, K, E;
+    int64_t chunk_tokens;
     int64_t chunks_per_partition;
     int32_t *hist;     // [chunks][E]
     int32_t *bad;      // [chunks] 1 if the chunk saw an invalid expert id
@@ -139,13 +153,16 @@ __device__ __forceinline__ int32_t resolve_route_row(const RouteDev &a, int64_t 
     const int32_t lr = route_row[i];
     if (lr < 0) return -1;
     const int e = a.ids[i];
-    const int64_t p = t / a.M;
-    const int64_t c = p * a.chunks_per_partition + (t - p * a.M) / kRouteChunkTokens;
-    const int32_t row = a.hist[c * a.E + e] + lr;
+    // T * K < 2^31, so token, partition and chunk indices fit in 32 bits
+    const int32_t t32 = (int32_t)t, M32 = (int32_t)a.M;
+    const int32_t p = t32 / M32;
+    const int32_t tl = t32 - p * M32;
+    const int32_t c = p * (int32_t)a.chunks_per_partition + tl / (int32_t)a.chunk_tokens;
+    const int32_t row = a.hist[(int64_t)c * a.E + e] + lr;
     route_row[i] = row;
     if (assist) {
-        assist[3 * (int64_t)row + 0] = (int32_t)p;
-        assist[3 * (int64_t)row + 1] = (int32_t)(t - p * a.M);
+        assist[3 * (int64_t)row + 0] = p;
+        assist[3 * (int64_t)row + 1] = tl;
         assist[3 * (int64_t)row + 2] = k;
     }
     return row;

@@ -99,7 +99,8 @@ moe_status moe_dispatch_noalloc(const moe_shape *shape, const void *x, const int
     r.M = s.num_tokens / s.num_partitions;
     r.K = s.topk;
     r.E = s.num_experts;
-    r.chunks_per_partition = (r.M + kRouteChunkTokens - 1) / kRouteChunkTokens;
+    r.chunk_tokens = route_chunk_tokens(r.T);
+    r.chunks_per_partition = (r.M + r.chunk_tokens - 1) / r.chunk_tokens;
     if (r.chunks_per_partition == 0) r.chunks_per_partition = 1;
     r.status = reinterpret_cast<int32_t *>(scratch);
     r.hist = reinterpret_cast<int32_t *>(scratch + kNoAllocHeaderBytes);

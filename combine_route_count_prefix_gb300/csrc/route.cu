@@ -16,7 +16,8 @@
 // of the send loop, computed here as a stable counting sort.
 //
 // GB300 design (not the pages' O((BS*K)^2) per-route count).  Routes are cut
-// into chunks of at most 256 tokens that never cross a partition boundary.
+// into chunks of 32..256 tokens (route_chunk_tokens) that never cross a
+// partition boundary.
 //   k_route_local  one CTA per chunk.  Each warp loads a contiguous slice of
 //                  the chunk (all its loads issued at once), then walks it in
 //                  order with __match_any_sync: one shared-memory add per
@@ -42,7 +43,7 @@ namespace moe {
 namespace {
 
 constexpr uint32_t kFull = 0xffffffffu;
-constexpr int kMaxWindows = (kRouteChunkTokens * kMaxTopK / kRouteWarps + 31) / 32;   // 16
+constexpr int kMaxWindows = (kRouteChunkTokensMax * kMaxTopK / kRouteWarps + 31) / 32;   // 16
 
 struct ChunkRange {
     int64_t r0, r1;   // route range [r0, r1) (flat index t*K + k)
@@ -53,8 +54,8 @@ __device__ __forceinline__ ChunkRange chunk_range(const RouteDev &a, int64_t c) 
     ChunkRange cr;
     cr.p = c / a.chunks_per_partition;
     int64_t j = c % a.chunks_per_partition;
-    int64_t t0 = cr.p * a.M + j * kRouteChunkTokens;
-    int64_t t1 = cr.p * a.M + min((j + 1) * (int64_t)kRouteChunkTokens, a.M);
+    int64_t t0 = cr.p * a.M + j * a.chunk_tokens;
+    int64_t t1 = cr.p * a.M + min((j + 1) * a.chunk_tokens, a.M);
     cr.r0 = t0 * a.K;
     cr.r1 = t1 * a.K;
     return cr;
@@ -80,8 +81,10 @@ k_route_local(RouteDev a, int32_t *local_rank) {
     int e_reg[kMaxWindows];
     int m_reg[kMaxWindows];
     const int32_t K32 = (int32_t)a.K;
+    const int nwin = (int)((w1 - w0 + 31) / 32);   // warp-uniform
 #pragma unroll
     for (int j = 0; j < kMaxWindows; ++j) {
+        if (j >= nwin) break;
         const int64_t i = w0 + 32 * j + lane;
         e_reg[j] = -1;
         m_reg[j] = 1;
@@ -94,6 +97,7 @@ k_route_local(RouteDev a, int32_t *local_rank) {
     bool bad = false;
 #pragma unroll
     for (int j = 0; j < kMaxWindows; ++j) {
+        if (j >= nwin) break;
         int e = e_reg[j];
         if (w0 + 32 * j + lane >= w1 || m_reg[j] == 0) e = -1;
         else if (e < 0 || e >= a.E) { bad = true; e = -1; }
@@ -105,8 +109,8 @@ k_route_local(RouteDev a, int32_t *local_rank) {
     int rl[kMaxWindows];
 #pragma unroll
     for (int j = 0; j < kMaxWindows; ++j) {
+        if (j >= nwin) break;
         rl[j] = -1;
-        if (w0 + 32 * j >= w1) continue;   // warp-uniform
         const int e = e_reg[j];
         const uint32_t grp = __match_any_sync(kFull, e);
         if (e >= 0) rl[j] = mine[e] + __popc(grp & lanemask_lt());
@@ -131,6 +135,7 @@ k_route_local(RouteDev a, int32_t *local_rank) {
     __syncthreads();
 #pragma unroll
     for (int j = 0; j < kMaxWindows; ++j) {
+        if (j >= nwin) break;
         const int64_t i = w0 + 32 * j + lane;
         if (i < w1) local_rank[i] = (e_reg[j] >= 0) ? rl[j] + mine[e_reg[j]] : -1;
     }
@@ -166,94 +171,115 @@ __device__ int block_exclusive_scan_1024(int v, int *scratch /*[33]*/, int *tota
     return res;
 }
 
+__device__ long long block_exclusive_scan64_1024(long long v, long long *scratch, long long *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    long long incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        long long n = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) scratch[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        long long w = scratch[lane];
+        long long wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            long long n = __shfl_up_sync(kFull, wi, o);
+            if (lane >= o) wi += n;
+        }
+        scratch[lane] = wi - w;
+        if (lane == 31) scratch[32] = wi;
+    }
+    __syncthreads();
+    const long long res = scratch[warp] + incl - v;
+    *total = scratch[32];
+    return res;
+}
+
+constexpr int kScanRegs = 32;   // chunk counts a scan thread keeps in registers
+
 __global__ void __launch_bounds__(1024)
 k_route_scan(RouteDev a, int64_t chunks, int64_t *counts, int32_t *offsets, int32_t *recv_cum,
              int32_t *sched) {
-    __shared__ int scratch[33];
+    __shared__ long long scratch64[33];
     __shared__ int tot_s[kMaxExperts];
     __shared__ int off_s[kMaxExperts];
+    __shared__ int part_s[1024];
     pdl_wait();
-    // tpe threads per expert, each over a contiguous range of chunks
+    // tpe threads per expert; thread (e, j) owns the contiguous chunk range j.
+    // Experts vary fastest across threads, so every load and store of a
+    // chunk's histogram row is coalesced.
     int tpe = 1;
     while (tpe * 2 * a.E <= 1024 && tpe < 32) tpe *= 2;
-    const int e = threadIdx.x / tpe, j = threadIdx.x % tpe;
+    const int tid = threadIdx.x;
+    const bool on = tid < tpe * a.E;
+    const int e = on ? tid % (int)a.E : 0, j = on ? tid / (int)a.E : 0;
     const int64_t per = (chunks + tpe - 1) / tpe;
-    const int64_t c0 = min((int64_t)j * per, chunks), c1 = min(c0 + per, chunks);
-    // the first 8 chunk counts of the range stay in registers for the second pass
+    const int64_t c0 = min((int64_t)j * per, chunks), c1 = on ? min(c0 + per, chunks) : c0;
+    int vals[kScanRegs];
     int part = 0;
-    int first[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u)
-        first[u] = (e < a.E && c0 + u < c1) ? a.hist[(c0 + u) * a.E + e] : 0;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) part += first[u];
-    if (e < a.E) {
-        for (int64_t c = c0 + 8; c < c1; c += 8) {
-            int v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = (c + u < c1) ? a.hist[(c + u) * a.E + e] : 0;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) part += v[u];
+    for (int u = 0; u < kScanRegs; ++u) {
+        vals[u] = (c0 + u < c1) ? a.hist[(c0 + u) * a.E + e] : 0;
+        part += vals[u];
+    }
+    for (int64_t c = c0 + kScanRegs; c < c1; ++c) part += a.hist[c * a.E + e];   // long ranges
+    part_s[tid] = part;
+    __syncthreads();
+    int excl = 0, total_e = 0;
+    if (on) {
+        for (int jj = 0; jj < tpe; ++jj) {
+            const int v = part_s[jj * a.E + e];
+            if (jj < j) excl += v;
+            total_e += v;
         }
-    }
-    // exclusive scan of the parts within the tpe-group (consecutive lanes)
-    const int lane = threadIdx.x & 31;
-    int incl = part;
-    for (int o = 1; o < tpe; o <<= 1) {
-        int v = __shfl_up_sync(kFull, incl, o);
-        if ((lane % tpe) >= o) incl += v;
-    }
-    const int excl = incl - part;
-    const int group_total = __shfl_sync(kFull, incl, (lane / tpe) * tpe + tpe - 1);
-    if (e < a.E && j == 0) tot_s[e] = group_total;
-    __syncthreads();
-    const int t = threadIdx.x;
-    const int tv = (t < a.E) ? tot_s[t] : 0;
-    int total;
-    const int off = block_exclusive_scan_1024(tv, scratch, &total);
-    int mtotal;
-    const int mstart = block_exclusive_scan_1024((t < a.E) ? (tv + kGemmBM - 1) / kGemmBM : 0,
-                                                 scratch, &mtotal);
-    if (t < a.E) {
-        off_s[t] = off;
-        counts[t] = tv;
-        offsets[t] = off;
-        if (sched) sched[t] = mstart;
+        if (j == 0) tot_s[e] = total_e;
     }
     __syncthreads();
-    if (e < a.E) {
+    const int tv = (tid < a.E) ? tot_s[tid] : 0;
+    // offsets (low half) and m-block starts (high half) in one 64-bit scan;
+    // both sums stay below 2^31, so the halves never carry into each other
+    const long long packed = (long long)tv | ((long long)((tv + kGemmBM - 1) / kGemmBM) << 32);
+    long long ptotal;
+    const long long pscan = block_exclusive_scan64_1024(packed, scratch64, &ptotal);
+    const int total = (int)(ptotal & 0xffffffffll), mtotal = (int)(ptotal >> 32);
+    if (tid < a.E) {
+        off_s[tid] = (int)(pscan & 0xffffffffll);
+        counts[tid] = tv;
+        offsets[tid] = (int)(pscan & 0xffffffffll);
+        if (sched) sched[tid] = (int)(pscan >> 32);
+    }
+    __syncthreads();
+    if (on) {
         int run = off_s[e] + excl;
+        // partition of chunk c0 and position inside it, then advanced by one per chunk
+        const int cpp = (int)a.chunks_per_partition;
+        int p = (int)(c0 / cpp), q = (int)(c0 - (int64_t)p * cpp);
+        int32_t *rc = recv_cum + (int64_t)e * a.P;
+        int32_t *h = a.hist + e;
+        const int n = (int)(c1 - c0);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int64_t c = c0 + u;
-            if (c < c1) {
-                a.hist[c * a.E + e] = run;
-                run += first[u];
-                if ((c + 1) % a.chunks_per_partition == 0)
-                    recv_cum[e * a.P + c / a.chunks_per_partition] = run;
+        for (int u = 0; u < kScanRegs; ++u) {
+            if (u < n) {
+                h[(c0 + u) * a.E] = run;
+                run += vals[u];
+                if (++q == cpp) { rc[p] = run; ++p; q = 0; }
             }
         }
-        for (int64_t cb = c0 + 8; cb < c1; cb += 8) {
-            int v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = (cb + u < c1) ? a.hist[(cb + u) * a.E + e] : 0;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int64_t c = cb + u;
-                if (c < c1) {
-                    a.hist[c * a.E + e] = run;
-                    run += v[u];
-                    if ((c + 1) % a.chunks_per_partition == 0)
-                        recv_cum[e * a.P + c / a.chunks_per_partition] = run;
-                }
-            }
+        for (int u = kScanRegs; u < n; ++u) {
+            const int v = h[(c0 + u) * a.E];
+            h[(c0 + u) * a.E] = run;
+            run += v;
+            if (++q == cpp) { rc[p] = run; ++p; q = 0; }
         }
     }
     // status word of this call: invalid ids seen by any chunk
     int bad = 0;
-    for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x) bad |= a.bad[c];
+    for (int64_t c = tid; c < chunks; c += blockDim.x) bad |= a.bad[c];
     bad = __syncthreads_or(bad);
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
         offsets[a.E] = total;
         if (sched) sched[a.E] = mtotal;
         *a.status = bad ? MOE_DEV_BAD_EXPERT_ID : 0;

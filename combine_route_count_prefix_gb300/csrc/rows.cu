@@ -52,12 +52,20 @@ __device__ __forceinline__ float block_max(float v, float *scratch /*[32]*/) {
     return r;
 }
 
-// Dynamic int8 quantisation code of v with scale s (s = amax / 127): rint(v/s)
-// clamped to [-127, 127], 0 when s == 0.  IEEE division and round-half-even.
-__device__ __forceinline__ float quant_code(float v, float s) {
+// Dynamic int8 quantisation code of v with scale s (s = amax / 127): the
+// round-half-even integer of the IEEE quotient v/s, clamped to [-127, 127];
+// 0 when s == 0.  rs = 1/s rounded to nearest.
+// Fast path: x = v * rs differs from the exact quotient by at most 2^-23
+// relatively, i.e. by less than 1.6e-5 for |v/s| <= 128, so rint(x) equals
+// rint(v/s) unless x lies within that distance of a half-integer.  Those
+// rare cases (and non-finite x) take the IEEE division, so the code is the
+// same as rint(__fdiv_rn(v, s)) for every input.
+__device__ __forceinline__ float quant_code(float v, float s, float rs) {
     if (s == 0.0f) return 0.0f;
-    float r = rintf(__fdiv_rn(v, s));
-    return fminf(fmaxf(r, -127.0f), 127.0f);
+    const float x = __fmul_rn(v, rs);
+    float q = rintf(x);
+    if (!(fabsf(fabsf(x - q) - 0.5f) >= 3.0e-5f)) q = rintf(__fdiv_rn(v, s));
+    return fminf(fmaxf(q, -127.0f), 127.0f);
 }
 
 // ---------------------------------------------------------------- dispatch copy
@@ -143,16 +151,17 @@ k_quant_bf16_rows(RouteDev ra, const uint4 *__restrict__ src, int32_t *__restric
         }
         amax = block_max(amax, scratch);
         const float s = __fdiv_rn(amax, 127.0f);
+        const float rs = __frcp_rn(s);
         // 8 bf16 in -> 8 fp16 codes out: one 16-byte vector in, one out
         uint4 qv[kVec];
 #pragma unroll
         for (int u = 0; u < kVec; ++u) {
             float f[8];
             unpack_bf16x8(v[u], f);
-            qv[u].x = pack_half2(quant_code(f[0], s), quant_code(f[1], s));
-            qv[u].y = pack_half2(quant_code(f[2], s), quant_code(f[3], s));
-            qv[u].z = pack_half2(quant_code(f[4], s), quant_code(f[5], s));
-            qv[u].w = pack_half2(quant_code(f[6], s), quant_code(f[7], s));
+            qv[u].x = pack_half2(quant_code(f[0], s, rs), quant_code(f[1], s, rs));
+            qv[u].y = pack_half2(quant_code(f[2], s, rs), quant_code(f[3], s, rs));
+            qv[u].z = pack_half2(quant_code(f[4], s, rs), quant_code(f[5], s, rs));
+            qv[u].w = pack_half2(quant_code(f[6], s, rs), quant_code(f[7], s, rs));
         }
         for (int d = 0; d < n; ++d) {
             const int64_t r = rows[d];
@@ -200,13 +209,14 @@ k_quant2(const float4 *__restrict__ g, const int32_t *__restrict__ offsets, int6
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
             const float s = __fdiv_rn(amax, 127.0f);
+            const float rs = __frcp_rn(s);
 #pragma unroll
             for (int u = 0; u < kQ2Vec; ++u) {
                 const int64_t j = lane + 32 * u;
                 if (j < Nh4) {
                     uint2 o;
-                    o.x = pack_half2(quant_code(v[u].x, s), quant_code(v[u].y, s));
-                    o.y = pack_half2(quant_code(v[u].z, s), quant_code(v[u].w, s));
+                    o.x = pack_half2(quant_code(v[u].x, s, rs), quant_code(v[u].y, s, rs));
+                    o.y = pack_half2(quant_code(v[u].z, s, rs), quant_code(v[u].w, s, rs));
                     dst[j] = o;
                 }
             }
@@ -219,11 +229,12 @@ k_quant2(const float4 *__restrict__ g, const int32_t *__restrict__ offsets, int6
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
             const float s = __fdiv_rn(amax, 127.0f);
+            const float rs = __frcp_rn(s);
             for (int64_t j = lane; j < Nh4; j += 32) {
                 const float4 v = src[j];
                 uint2 o;
-                o.x = pack_half2(quant_code(v.x, s), quant_code(v.y, s));
-                o.y = pack_half2(quant_code(v.z, s), quant_code(v.w, s));
+                o.x = pack_half2(quant_code(v.x, s, rs), quant_code(v.y, s, rs));
+                o.y = pack_half2(quant_code(v.z, s, rs), quant_code(v.w, s, rs));
                 dst[j] = o;
             }
             if (lane == 0) s2[r] = s;

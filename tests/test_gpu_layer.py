@@ -189,3 +189,46 @@ def test_full_layer_sampled(B):
 
 def test_large_prefill_sampled(B):
     _sampled_full_size(B, "large_prefill", n_tokens=4)
+
+
+def test_quantisation_codes_exact_on_ties_and_many_scales(B):
+    """Per-row int8 codes and scales of dispatched rows (moe_grouped_ffn's first
+    step) equal the oracle's rint(v / s) with IEEE division, bit for bit, on
+    rows built to land on and next to rounding ties, and on random rows of
+    many magnitudes."""
+    H, N, E = 512, 256, 2
+    g = np.random.default_rng(11)
+    rows = []
+    base = np.zeros(H, np.float32)                 # amax 127 -> s = 1: exact ties
+    base[0] = 127.0
+    base[1:64] = np.arange(63) + 0.5
+    base[64:128] = -(np.arange(64) + 0.5)
+    rows.append(base)
+    for scale in [1e-3, 0.07, 1.0, 3.3, 250.0, 1e4]:
+        for _ in range(20):
+            rows.append((g.standard_normal(H) * scale).astype(np.float32))
+    for _ in range(20):                            # values at s*(n + 0.5) for inexact s
+        amax = np.float32(g.uniform(0.5, 4.0))
+        s = np.float32(amax / np.float32(127.0))
+        r = (g.integers(-126, 126, H) + 0.5).astype(np.float32) * s
+        r[0] = amax
+        rows.append(r)
+    X = wl.f32_to_bf16_bits(np.stack(rows))
+    R = X.shape[0]
+    T, K, P = R, 1, 1
+    offsets = np.array([0, R // 2, R], np.int32)
+    shape = B.make_shape(T, P, H, E, K, N)
+    W1 = g.integers(-127, 128, (E, N, H), dtype=np.int8)
+    W2 = g.integers(-127, 128, (E, H, N // 2), dtype=np.int8)
+    S1 = g.uniform(1e-3, 1e-2, (E, N)).astype(np.float32)
+    S2 = g.uniform(1e-3, 1e-2, (E, H)).astype(np.float32)
+    (o1, w1p), (o2, w2p) = B.pack_weights(shape, dev(W1), dev(W2))
+    y, ws = B.grouped_ffn(shape, dev_bf16(X), dev(offsets), w1p, dev(S1), w2p, dev(S2))
+    torch.cuda.synchronize()
+    v = B.stage_views(shape, ws, for_layer=False)
+    q1 = host_f16_as_i8(v["q1"][:R])
+    s1 = v["s1"][:R].cpu().numpy()
+    for i in range(R):
+        q, s = oracle.quant_row(wl.bf16_bits_to_f32(X[i]))
+        assert s1[i] == np.float32(s), i
+        np.testing.assert_array_equal(q1[i], q, err_msg=f"row {i}")
