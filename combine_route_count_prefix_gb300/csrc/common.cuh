@@ -36,6 +36,9 @@ int num_sms();
 // pdl_wait() (griddepcontrol.wait) before it reads anything the predecessor
 // wrote.  Every kernel of this library calls pdl_wait() before its first
 // dependent read.
+#ifndef MOE_PDL_ATTRS
+#define MOE_PDL_ATTRS 1
+#endif
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                        cudaStream_t stream, Args... args) {
@@ -48,7 +51,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = MOE_PDL_ATTRS;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
