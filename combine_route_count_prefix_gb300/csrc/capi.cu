@@ -155,6 +155,7 @@ static RouteDev route_dev(const moe_shape &s, const int32_t *ids, const uint8_t 
     r.hist = at<int32_t>(ws, L.hist);
     r.bad = r.hist + C * s.num_experts;
     r.status = at<int32_t>(ws, L.status);
+    r.rows_final = 0;
     return r;
 }
 
@@ -262,8 +263,8 @@ moe_status moe_dispatch(const moe_shape *shape, const void *x, const int32_t *ex
     const Layout L = layout_for(s, Op::Dispatch);
     if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
     RouteDev r = route_dev(s, expert_ids, x_active_mask, workspace, L);
-    MOE_TRY(launch_route(r, route_chunks(s), expert_token_nums, expert_offsets, ep_recv_counts,
-                         nullptr, route_row, stream));
+    MOE_TRY(launch_route_fused(r, route_chunks(s), expert_token_nums, expert_offsets,
+                               ep_recv_counts, nullptr, route_row, assist, stream));
     if (expand_x) return launch_dispatch_rows(r, x, route_row, assist, expand_x, s.hidden, stream);
     return launch_route_resolve(r, route_row, assist, stream);
 }
@@ -416,9 +417,9 @@ moe_status moe_layer(const moe_shape *shape, const void *x, const int32_t *exper
     RouteDev r = route_dev(s, expert_ids, x_active_mask, workspace, L);
     int32_t *route_row = at<int32_t>(workspace, L.route_row);
     int32_t *offsets = at<int32_t>(workspace, L.offsets);
-    MOE_TRY(launch_route(r, route_chunks(s), at<int64_t>(workspace, L.counts), offsets,
-                         at<int32_t>(workspace, L.recv_cum), at<int32_t>(workspace, L.sched),
-                         route_row, stream));
+    MOE_TRY(launch_route_fused(r, route_chunks(s), at<int64_t>(workspace, L.counts), offsets,
+                               at<int32_t>(workspace, L.recv_cum), at<int32_t>(workspace, L.sched),
+                               route_row, at<int32_t>(workspace, L.assist), stream));
     if (s.num_tokens == 0) return MOE_OK;
     MOE_TRY(launch_quant_scatter(r, x, route_row, at<int32_t>(workspace, L.assist),
                                  at<void>(workspace, L.q1), at<float>(workspace, L.s1), s.hidden,

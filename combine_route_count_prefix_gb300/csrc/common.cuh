@@ -143,6 +143,7 @@ struct RouteDev {
     int32_t *hist;     // [chunks][E]
     int32_t *bad;      // [chunks] 1 if the chunk saw an invalid expert id
     int32_t *status;
+    int rows_final;    // 1: route_row already holds final rows (single-kernel routing)
 };
 
 // Final row of route (t, k): route_row holds the route's rank inside its
@@ -155,6 +156,7 @@ __device__ __forceinline__ int32_t resolve_route_row(const RouteDev &a, int64_t 
     const int64_t i = t * a.K + k;
     const int32_t lr = route_row[i];
     if (lr < 0) return -1;
+    if (a.rows_final) return lr;
     const int e = a.ids[i];
     // T * K < 2^31, so token, partition and chunk indices fit in 32 bits
     const int32_t t32 = (int32_t)t, M32 = (int32_t)a.M;
@@ -176,6 +178,12 @@ __device__ __forceinline__ int32_t resolve_route_row(const RouteDev &a, int64_t 
 moe_status launch_route(const RouteDev &r, int64_t chunks, int64_t *counts, int32_t *offsets,
                         int32_t *recv_cum, int32_t *sched, int32_t *route_row,
                         cudaStream_t stream);
+// Single-kernel routing (count, rank, grid barrier, prefix, final rows and
+// triplets) when all chunks fit on the GPU at once; otherwise launch_route.
+// Sets r.rows_final accordingly.
+moe_status launch_route_fused(RouteDev &r, int64_t chunks, int64_t *counts, int32_t *offsets,
+                              int32_t *recv_cum, int32_t *sched, int32_t *route_row,
+                              int32_t *assist, cudaStream_t stream);
 // Resolution alone, when no kernel copies or quantises the rows.
 moe_status launch_route_resolve(const RouteDev &r, int32_t *route_row, int32_t *assist,
                                 cudaStream_t stream);

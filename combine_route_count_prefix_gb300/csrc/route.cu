@@ -39,6 +39,8 @@
 // No global atomics decide a position, so the result is deterministic.
 #include "common.cuh"
 
+#include <cooperative_groups.h>
+
 namespace moe {
 namespace {
 
@@ -286,6 +288,197 @@ k_route_scan(RouteDev a, int64_t chunks, int64_t *counts, int32_t *offsets, int3
     }
 }
 
+// ---------------------------------------------------------------- single-kernel routing
+// One CTA per chunk, launched cooperatively (all CTAs resident).  Phase 1 is
+// k_route_local's count and rank, keeping each route's rank in registers.
+// After a grid-wide barrier every CTA reads all chunk histograms and computes
+// the per-expert totals, their exclusive scan (offsets) and its own chunk's
+// bases, then writes the final row and triplet of each of its routes.  CTA 0
+// also writes counts, offsets, recv_cum, the GEMM schedule and the status.
+constexpr int kFusedLoads = 32;   // chunk counts loaded at once per expert
+
+__global__ void __launch_bounds__(kRouteThreads)
+k_route_fused(RouteDev a, int64_t chunks, int64_t *counts, int32_t *offsets, int32_t *recv_cum,
+              int32_t *sched, int32_t *route_row, int32_t *assist) {
+    extern __shared__ int32_t hw[];   // [kRouteWarps][E]; reused after the barrier
+    __shared__ int any_bad;
+    __shared__ long long scratch64[kRouteWarps + 1];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t c = blockIdx.x;
+    for (int64_t i = tid; i < kRouteWarps * a.E; i += blockDim.x) hw[i] = 0;
+    if (tid == 0) any_bad = 0;
+    pdl_wait();
+
+    // ---------------- phase 1: count and rank inside the chunk
+    const ChunkRange cr = chunk_range(a, c);
+    const int64_t n = cr.r1 - cr.r0;
+    const int64_t per = ((n + kRouteWarps - 1) / kRouteWarps + 31) / 32 * 32;
+    const int64_t w0 = min(cr.r0 + warp * per, cr.r1);
+    const int64_t w1 = min(w0 + per, cr.r1);
+    const int nwin = (int)((w1 - w0 + 31) / 32);
+    const int32_t K32 = (int32_t)a.K;
+    int e_reg[kMaxWindows];
+    int m_reg[kMaxWindows];
+#pragma unroll
+    for (int j = 0; j < kMaxWindows; ++j) {
+        if (j >= nwin) break;
+        const int64_t i = w0 + 32 * j + lane;
+        e_reg[j] = -1;
+        m_reg[j] = 1;
+        if (i < w1) {
+            e_reg[j] = __ldg(a.ids + i);
+            if (a.mask_kind == 1) m_reg[j] = __ldg(a.mask + (cr.r0 / K32 + (int32_t)(i - cr.r0) / K32));
+            else if (a.mask_kind == 2) m_reg[j] = __ldg(a.mask + i);
+        }
+    }
+    bool bad = false;
+#pragma unroll
+    for (int j = 0; j < kMaxWindows; ++j) {
+        if (j >= nwin) break;
+        int e = e_reg[j];
+        if (w0 + 32 * j + lane >= w1 || m_reg[j] == 0) e = -1;
+        else if (e < 0 || e >= a.E) { bad = true; e = -1; }
+        e_reg[j] = e;
+    }
+    __syncthreads();
+    int32_t *mine = hw + warp * a.E;
+    int rl[kMaxWindows];
+#pragma unroll
+    for (int j = 0; j < kMaxWindows; ++j) {
+        if (j >= nwin) break;
+        rl[j] = -1;
+        const int e = e_reg[j];
+        const uint32_t grp = __match_any_sync(kFull, e);
+        if (e >= 0) rl[j] = mine[e] + __popc(grp & lanemask_lt());
+        __syncwarp();
+        if (e >= 0 && lane == __ffs(grp) - 1) mine[e] += __popc(grp);
+        __syncwarp();
+    }
+    if (__any_sync(kFull, bad) && lane == 0) any_bad = 1;
+    __syncthreads();
+    for (int64_t e = tid; e < a.E; e += blockDim.x) {
+        int32_t run = 0;
+#pragma unroll
+        for (int w = 0; w < kRouteWarps; ++w) {
+            const int32_t v = hw[w * a.E + e];
+            hw[w * a.E + e] = run;
+            run += v;
+        }
+        a.hist[c * a.E + e] = run;
+    }
+    if (tid == 0) a.bad[c] = any_bad;
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kMaxWindows; ++j) {
+        if (j >= nwin) break;
+        if (e_reg[j] >= 0) rl[j] += mine[e_reg[j]];   // rank inside the chunk
+    }
+    __threadfence();
+    cooperative_groups::this_grid().sync();
+
+    // ---------------- phase 2: totals, offsets, this chunk's bases
+    int32_t *tot_s = hw;                 // [E]
+    int32_t *below_s = hw + a.E;         // [E], later the chunk bases
+    const bool lead = blockIdx.x == 0;
+    const int cpp = (int)a.chunks_per_partition;
+    for (int64_t e = tid; e < a.E; e += blockDim.x) {
+        int tot = 0, below = 0;
+        for (int64_t cb = 0; cb < chunks; cb += kFusedLoads) {
+            int v[kFusedLoads];
+#pragma unroll
+            for (int u = 0; u < kFusedLoads; ++u)
+                v[u] = (cb + u < chunks) ? a.hist[(cb + u) * a.E + e] : 0;
+#pragma unroll
+            for (int u = 0; u < kFusedLoads; ++u) {
+                tot += v[u];
+                if (cb + u < c) below += v[u];
+            }
+        }
+        tot_s[e] = tot;
+        below_s[e] = below;
+    }
+    __syncthreads();
+    // exclusive scan over experts of (total, m-blocks), packed in 64 bits
+    const int per_t = (int)((a.E + blockDim.x - 1) / blockDim.x);
+    const int64_t e0 = (int64_t)tid * per_t, e1 = min(e0 + per_t, a.E);
+    long long local = 0;
+    for (int64_t e = e0; e < e1; ++e)
+        local += (long long)tot_s[e] | ((long long)((tot_s[e] + kGemmBM - 1) / kGemmBM) << 32);
+    long long incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long v = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) scratch64[warp] = incl;
+    __syncthreads();
+    if (tid == 0) {
+        long long run = 0;
+        for (int w = 0; w < kRouteWarps; ++w) {
+            const long long v = scratch64[w];
+            scratch64[w] = run;
+            run += v;
+        }
+        scratch64[kRouteWarps] = run;
+    }
+    __syncthreads();
+    long long ex = scratch64[warp] + incl - local;
+    int bad_all = 0;
+    if (lead)
+        for (int64_t cc = tid; cc < chunks; cc += blockDim.x) bad_all |= a.bad[cc];
+    for (int64_t e = e0; e < e1; ++e) {
+        const int off = (int)(ex & 0xffffffffll);
+        const int tv = tot_s[e];
+        below_s[e] += off;   // this chunk's base of expert e
+        if (lead) {
+            counts[e] = tv;
+            offsets[e] = off;
+            if (sched) sched[e] = (int)(ex >> 32);
+            // receive counts: running sum over the chunks, written at partition ends
+            int run = off, q = 0, pidx = 0;
+            int32_t *rc = recv_cum + e * a.P;
+            const int nch = (int)chunks;
+            const int32_t *hcol = a.hist + e;
+            for (int cb = 0; cb < nch; cb += 16) {
+                int v[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) v[u] = (cb + u < nch) ? hcol[(int64_t)(cb + u) * a.E] : 0;
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    if (cb + u < nch) {
+                        run += v[u];
+                        if (++q == cpp) { rc[pidx++] = run; q = 0; }
+                    }
+                }
+            }
+        }
+        ex += (long long)tv | ((long long)((tv + kGemmBM - 1) / kGemmBM) << 32);
+    }
+    bad_all = __syncthreads_or(bad_all);
+    if (lead && tid == 0) {
+        const long long tot_all = scratch64[kRouteWarps];
+        offsets[a.E] = (int)(tot_all & 0xffffffffll);
+        if (sched) sched[a.E] = (int)(tot_all >> 32);
+        *a.status = bad_all ? MOE_DEV_BAD_EXPERT_ID : 0;
+    }
+    // ---------------- final rows and triplets of this chunk's routes
+#pragma unroll
+    for (int j = 0; j < kMaxWindows; ++j) {
+        if (j >= nwin) break;
+        const int64_t i = w0 + 32 * j + lane;
+        if (i >= w1) continue;
+        int32_t row = -1;
+        if (e_reg[j] >= 0) {
+            row = below_s[e_reg[j]] + rl[j];
+            const int32_t t32 = (int32_t)(i / K32);
+            assist[3 * (int64_t)row + 0] = (int32_t)cr.p;
+            assist[3 * (int64_t)row + 1] = t32 - (int32_t)(cr.p * a.M);
+            assist[3 * (int64_t)row + 2] = (int32_t)(i - (int64_t)t32 * K32);
+        }
+        route_row[i] = row;
+    }
+}
+
 __global__ void k_route_resolve(RouteDev a, int32_t *route_row, int32_t *assist) {
     pdl_wait();
     const int64_t n = a.T * a.K;
@@ -327,10 +520,43 @@ moe_status launch_route(const RouteDev &r, int64_t chunks, int64_t *counts, int3
     return MOE_OK;
 }
 
+moe_status launch_route_fused(RouteDev &r, int64_t chunks, int64_t *counts, int32_t *offsets,
+                              int32_t *recv_cum, int32_t *sched, int32_t *route_row,
+                              int32_t *assist, cudaStream_t stream) {
+    const size_t smem = (size_t)kRouteWarps * r.E * sizeof(int32_t);
+    int per_sm = 0;
+    if (chunks > 0 &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_route_fused, kRouteThreads, smem) ==
+            cudaSuccess &&
+        chunks <= (int64_t)per_sm * num_sms()) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)chunks);
+        cfg.blockDim = dim3(kRouteThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        r.rows_final = 1;
+        const int tok = launch_begin("route_fused", stream);
+        cudaError_t err = cudaLaunchKernelEx(&cfg, k_route_fused, r, chunks, counts, offsets,
+                                             recv_cum, sched, route_row, assist);
+        if (err == cudaSuccess) err = cudaGetLastError();
+        launch_end(tok, stream);
+        if (err == cudaSuccess) return MOE_OK;
+        return MOE_ERR_CUDA;
+    }
+    cudaGetLastError();
+    r.rows_final = 0;
+    return launch_route(r, chunks, counts, offsets, recv_cum, sched, route_row, stream);
+}
+
 moe_status launch_route_resolve(const RouteDev &r, int32_t *route_row, int32_t *assist,
                                 cudaStream_t stream) {
     const int64_t n = r.T * r.K;
-    if (n == 0) return MOE_OK;
+    if (n == 0 || r.rows_final) return MOE_OK;
     int64_t blocks = (n + 255) / 256;
     const int64_t cap = (int64_t)num_sms() * 8;
     if (blocks > cap) blocks = cap;
