@@ -30,6 +30,10 @@ CASES = {
     "max_e_k": wl.custom(P=5, M=113, H=64, E=1024, K=16, has_shared=True),
     "zipf_skew": wl.custom(P=4, M=256, H=256, E=128, K=8, mask_kind=2, mask_p=0.95,
                            has_shared=True, routing="zipf", zipf_zero=10),
+    # more routing chunks than can be resident at once: the count/scan kernels
+    # and row resolution in the row kernel are used instead of the fused kernel
+    "many_partitions": wl.custom(P=640, M=2, H=64, E=16, K=4, mask_kind=1, mask_p=0.8,
+                                 has_shared=True),
 }
 
 

@@ -96,6 +96,11 @@ def test_layer_route_mask_empty_experts(B):
     _stage_check(B, w, seed=2)
 
 
+def test_layer_many_partitions_unfused_routing(B):
+    w = wl.custom(P=640, M=1, H=128, E=8, K=2, N=256, has_shared=True)
+    _stage_check(B, w, seed=3)
+
+
 def test_grouped_ffn_entry_on_dispatched_rows(B):
     """moe_grouped_ffn on the bf16 rows of moe_dispatch gives the same y as the
     fused layer (quantising each dispatched copy equals quantising the token)."""
