@@ -56,7 +56,7 @@ def _load():
     lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
     lib.oracle_silu.argtypes = [ctypes.c_float]
     lib.oracle_silu.restype = ctypes.c_float
-    lib.oracle_route.argtypes = [I64, I64, I64, I64, P, ctypes.c_int, P,
+    lib.oracle_route.argtypes = [I64, I64, I64, I64, I64, I64, P, ctypes.c_int, P,
                                  P, P, P, P, P, P, P]
     lib.oracle_route.restype = I64
     lib.oracle_gather.argtypes = [I64, I64, I64, P, P, P]
@@ -68,12 +68,12 @@ def _load():
     lib.oracle_ffn_row.restype = ctypes.c_int
     lib.oracle_grouped_gemm_s32.argtypes = [I64, I64, I64, P, P, P, P]
     lib.oracle_grouped_gemm_s32.restype = ctypes.c_int
-    lib.oracle_combine.argtypes = [I64, I64, I64, P, P, P, P, P]
+    lib.oracle_combine.argtypes = [I64, I64, I64, P, P, P, P, P, P]
     lib.oracle_combine.restype = None
-    lib.oracle_layer_tokens.argtypes = [I64, I64, I64, I64, I64, P, P, ctypes.c_int,
+    lib.oracle_layer_tokens.argtypes = [I64, I64, I64, I64, I64, I64, I64, P, P, ctypes.c_int,
                                         P, P, P, P, P, P, P, I64, P, P]
     lib.oracle_layer_tokens.restype = ctypes.c_int
-    lib.oracle_identity_tokens.argtypes = [I64, I64, I64, I64, P, P, ctypes.c_int,
+    lib.oracle_identity_tokens.argtypes = [I64, I64, I64, I64, I64, I64, P, P, ctypes.c_int,
                                            P, P, P, I64, P, P]
     lib.oracle_identity_tokens.restype = None
     _lib = lib
@@ -130,10 +130,12 @@ def silu(v: float) -> float:
 # path steps
 # --------------------------------------------------------------------------
 
-def route(ids: np.ndarray, num_experts: int, num_partitions: int, mask=None):
+def route(ids: np.ndarray, num_experts: int, num_partitions: int, mask=None, zero_experts=0,
+          copy_experts=0):
     """Dispatch bookkeeping.  Returns a dict with counts (int64 [E]),
-    offsets (int32 [E+1]), recv_cum (int32 [E*P]), route_row (int32 [T*K]),
-    assist (int32 [R, 3]), row_token (int32 [R]), R and num_invalid."""
+    offsets (int32 [E+1]), recv_cum (int32 [E*P]), route_row (int32 [T*K];
+    -1 inactive, -2 zero expert, -3 copy expert), assist (int32 [R, 3]),
+    row_token (int32 [R]), R and num_invalid."""
     lib = _load()
     ids = _c(ids, np.int32)
     T, K = ids.shape
@@ -146,7 +148,8 @@ def route(ids: np.ndarray, num_experts: int, num_partitions: int, mask=None):
     assist = np.zeros((T * K, 3), np.int32)
     row_token = np.zeros(T * K, np.int32)
     ninv = np.zeros(1, np.int64)
-    R = lib.oracle_route(T, P, K, E, _p(ids), kind, _p(m), _p(counts), _p(offsets),
+    R = lib.oracle_route(T, P, K, E, int(zero_experts), int(copy_experts), _p(ids), kind, _p(m),
+                         _p(counts), _p(offsets),
                          _p(recv_cum), _p(route_row), _p(assist), _p(row_token), _p(ninv))
     return dict(counts=counts, offsets=offsets, recv_cum=recv_cum, route_row=route_row,
                 assist=assist[:R].copy(), row_token=row_token[:R].copy(), R=int(R),
@@ -207,8 +210,9 @@ def grouped_gemm_s32(offsets, A, W):
     return C, bool(ovf)
 
 
-def combine(y, route_row, probs, shared=None):
-    """out[t] = bf16(sum_k probs*y[row] + shared).  Returns uint16 [T, H]."""
+def combine(y, route_row, probs, shared=None, ori_x=None):
+    """out[t] = bf16(sum_k probs*y[row] + shared); zero-expert slots add
+    probs*0, copy-expert slots probs*ori_x[t].  Returns uint16 [T, H]."""
     lib = _load()
     y = _c(y, np.uint16)
     probs = _c(probs, np.float32)
@@ -216,12 +220,14 @@ def combine(y, route_row, probs, shared=None):
     H = y.shape[1]
     rr = _c(route_row, np.int32)
     sh = _c(shared, np.uint16)
+    ox = _c(ori_x, np.uint16)
     out = np.zeros((T, H), np.uint16)
-    lib.oracle_combine(T, H, K, _p(y), _p(rr), _p(probs), _p(sh), _p(out))
+    lib.oracle_combine(T, H, K, _p(y), _p(rr), _p(probs), _p(sh), _p(ox), _p(out))
     return out
 
 
-def layer_tokens(x, ids, probs, w1, scale1, w2, scale2, tokens, mask=None, shared=None):
+def layer_tokens(x, ids, probs, w1, scale1, w2, scale2, tokens, mask=None, shared=None,
+                 zero_experts=0, copy_experts=0):
     """out[t] of the whole layer for the listed tokens (uint16 [n, H])."""
     lib = _load()
     x = _c(x, np.uint16)
@@ -233,7 +239,8 @@ def layer_tokens(x, ids, probs, w1, scale1, w2, scale2, tokens, mask=None, share
     kind, m = _mask_kind(mask, T, K)
     tok = _c(tokens, np.int64)
     out = np.zeros((tok.shape[0], H), np.uint16)
-    ovf = lib.oracle_layer_tokens(T, H, E, K, N, _p(x), _p(ids), kind, _p(m),
+    ovf = lib.oracle_layer_tokens(T, H, E, int(zero_experts), int(copy_experts), K, N, _p(x),
+                                  _p(ids), kind, _p(m),
                                   _p(_c(probs, np.float32)), _p(_c(shared, np.uint16)),
                                   _p(w1), _p(_c(scale1, np.float32)),
                                   _p(_c(w2, np.int8)), _p(_c(scale2, np.float32)),
@@ -241,7 +248,8 @@ def layer_tokens(x, ids, probs, w1, scale1, w2, scale2, tokens, mask=None, share
     return out, bool(ovf)
 
 
-def identity_tokens(x, ids, probs, num_experts, tokens, mask=None, shared=None):
+def identity_tokens(x, ids, probs, num_experts, tokens, mask=None, shared=None, zero_experts=0,
+                    copy_experts=0):
     """out[t] with an identity expert, for the listed tokens (uint16 [n, H])."""
     lib = _load()
     x = _c(x, np.uint16)
@@ -251,18 +259,19 @@ def identity_tokens(x, ids, probs, num_experts, tokens, mask=None, shared=None):
     kind, m = _mask_kind(mask, T, K)
     tok = _c(tokens, np.int64)
     out = np.zeros((tok.shape[0], H), np.uint16)
-    lib.oracle_identity_tokens(T, H, int(num_experts), K, _p(x), _p(ids), kind, _p(m),
+    lib.oracle_identity_tokens(T, H, int(num_experts), int(zero_experts), int(copy_experts), K,
+                               _p(x), _p(ids), kind, _p(m),
                                _p(_c(probs, np.float32)), _p(_c(shared, np.uint16)),
                                tok.shape[0], _p(tok), _p(out))
     return out
 
 
 def dispatch_combine_identity(x, ids, probs, num_experts, num_partitions,
-                              mask=None, shared=None):
-    """The identity-expert path in full: route, gather, combine.
-    Returns (route dict, expand_x uint16 [R, H], out uint16 [T, H])."""
-    r = route(ids, num_experts, num_partitions, mask)
+                              mask=None, shared=None, zero_experts=0, copy_experts=0):
+    """The identity-expert path in full: route, gather, combine (copy experts
+    read x itself).  Returns (route dict, expand_x uint16 [R, H], out uint16 [T, H])."""
+    r = route(ids, num_experts, num_partitions, mask, zero_experts, copy_experts)
     T, K = np.shape(ids)
     ex = gather(x, r["route_row"], K, r["R"])
-    out = combine(ex, r["route_row"], probs, shared)
+    out = combine(ex, r["route_row"], probs, shared, ori_x=x if copy_experts else None)
     return r, ex, out

@@ -71,17 +71,33 @@ uint16_t oracle_f32_to_bf16(float f)
 /* row order, triplets and the inverse index.                            */
 /* ------------------------------------------------------------------ */
 
-/* A route (t, k) takes part when the mask lets it and its expert id is a
- * real expert.  P2 (xActiveMask parameter): a 1-D mask [BS] switches a whole
- * token, a 2-D mask [BS, K] switches single routes.  Ids outside [0, E) are
- * treated as inactive and counted as invalid. */
+/* A route (t, k) takes part when the mask lets it and its expert id names
+ * an expert.  P2 (xActiveMask parameter): a 1-D mask [BS] switches a whole
+ * token, a 2-D mask [BS, K] switches single routes.  Expert ids
+ * ("aclnnMoeDistributeCombineV4", zeroExpertNum / copyExpertNum):
+ *   [0, E)           MoE experts, each with its own FFN and rows
+ *   [E, E+Z)         zero experts: their output is zero
+ *   [E+Z, E+Z+C)     copy experts: their output is the unprocessed token (oriX)
+ * anything else is not an expert; such routes are inactive and counted as
+ * invalid. */
+enum { ROUTE_OFF = 0, ROUTE_EXPERT = 1, ROUTE_ZERO = 2, ROUTE_COPY = 3, ROUTE_INVALID = 4 };
+
+static int route_class(int64_t t, int64_t k, int64_t K, int64_t E, int64_t Z, int64_t C,
+                       const int32_t *ids, int mask_kind, const uint8_t *mask)
+{
+    if (mask_kind == 1 && mask[t] == 0) return ROUTE_OFF;
+    if (mask_kind == 2 && mask[t * K + k] == 0) return ROUTE_OFF;
+    int64_t e = ids[t * K + k];
+    if (e >= 0 && e < E) return ROUTE_EXPERT;
+    if (e >= E && e < E + Z) return ROUTE_ZERO;
+    if (e >= E + Z && e < E + Z + C) return ROUTE_COPY;
+    return ROUTE_INVALID;
+}
+
 static int route_active(int64_t t, int64_t k, int64_t K, int64_t E,
                         const int32_t *ids, int mask_kind, const uint8_t *mask)
 {
-    if (mask_kind == 1 && mask[t] == 0) return 0;
-    if (mask_kind == 2 && mask[t * K + k] == 0) return 0;
-    int32_t e = ids[t * K + k];
-    return e >= 0 && e < E;
+    return route_class(t, k, K, E, 0, 0, ids, mask_kind, mask) == ROUTE_EXPERT;
 }
 
 /*
@@ -99,16 +115,18 @@ static int route_active(int64_t t, int64_t k, int64_t K, int64_t E,
  *   (P1 "Local data copy" walks status index local_expert*W + src_rank in
  *    increasing order and copies each source's rows in arrival order; the
  *    arrival order inside one source is the route order of the send loop).
- * route_row[t*K+k] = row of route (t, k), or -1 if inactive
- *   (P3 Memory Layout: expandedRowIdx, route -> expert-major row).
+ * route_row[t*K+k] = row of route (t, k) (P3 Memory Layout: expandedRowIdx,
+ *   route -> expert-major row); -1 if inactive, -2 for a zero expert and -3
+ *   for a copy expert (special experts have no rows).
  * assist[3r..3r+2] = (p, t - p*M, k) for row r (P1 send loop triplet:
  *   rank, token index local to the rank, slot k).
  * row_token[r] = t (the global token of row r).
  *
- * Returns R, the number of active routes.  *num_invalid receives the number
- * of routes whose id lies outside [0, E) and whose mask (if any) was set.
+ * Returns R, the number of routed rows.  *num_invalid receives the number
+ * of routes whose id names no expert (outside [0, E+Z+C)) and whose mask (if
+ * any) was set.  Z zero experts and C copy experts follow the E MoE experts.
  */
-int64_t oracle_route(int64_t T, int64_t P, int64_t K, int64_t E,
+int64_t oracle_route(int64_t T, int64_t P, int64_t K, int64_t E, int64_t Z, int64_t C,
                      const int32_t *ids, int mask_kind, const uint8_t *mask,
                      int64_t *counts, int32_t *offsets, int32_t *recv_cum,
                      int32_t *route_row, int32_t *assist, int32_t *row_token,
@@ -120,13 +138,11 @@ int64_t oracle_route(int64_t T, int64_t P, int64_t K, int64_t E,
 
     for (int64_t t = 0; t < T; ++t) {
         for (int64_t k = 0; k < K; ++k) {
-            int masked_off = (mask_kind == 1 && mask[t] == 0) ||
-                             (mask_kind == 2 && mask[t * K + k] == 0);
-            int32_t e = ids[t * K + k];
-            if (!masked_off && (e < 0 || e >= E)) invalid++;
-            if (!route_active(t, k, K, E, ids, mask_kind, mask)) continue;
+            int cls = route_class(t, k, K, E, Z, C, ids, mask_kind, mask);
+            if (cls == ROUTE_INVALID) invalid++;
+            if (cls != ROUTE_EXPERT) continue;
             int64_t p = t / M;
-            counts_pe[e * P + p] += 1;
+            counts_pe[(int64_t)ids[t * K + k] * P + p] += 1;
         }
     }
 
@@ -147,7 +163,13 @@ int64_t oracle_route(int64_t T, int64_t P, int64_t K, int64_t E,
     }
     offsets[E] = (int32_t)acc;
 
-    for (int64_t i = 0; i < T * K; ++i) route_row[i] = -1;
+    /* route_row codes for routes without a row: -1 inactive, -2 zero expert,
+     * -3 copy expert */
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t k = 0; k < K; ++k) {
+            int cls = route_class(t, k, K, E, Z, C, ids, mask_kind, mask);
+            route_row[t * K + k] = cls == ROUTE_ZERO ? -2 : cls == ROUTE_COPY ? -3 : -1;
+        }
 
     /* Emit rows in (expert, partition, token, slot) order. */
     int64_t r = 0;
@@ -326,20 +348,27 @@ int oracle_grouped_gemm_s32(int64_t E, int64_t N, int64_t Kd,
  * P2 Function/Formula: xOut = Sum(expertScales * ataOut) plus the shared
  * expert term, read here as added once, unscaled, after the routed sum.
  * P3 Unpermute: topK weighted accumulation back into the original order.
- * y: bf16 [rows, H]; route_row: [T*K] (-1 = inactive); probs fp32 [T, K];
- * shared: bf16 [T, H] or NULL; out: bf16 [T, H].
+ * A zero-expert slot (route_row -2) contributes probs * 0 and a copy-expert
+ * slot (-3) probs * oriX[t] ("aclnnMoeDistributeCombineV4", zeroExpertNum,
+ * copyExpertNum, oriXOptional), in their slot position.
+ * y: bf16 [rows, H]; route_row: [T*K]; probs fp32 [T, K]; shared: bf16
+ * [T, H] or NULL; ori_x: bf16 [T, H] or NULL (needed if a slot is -3);
+ * out: bf16 [T, H].
  */
 void oracle_combine(int64_t T, int64_t H, int64_t K, const uint16_t *y,
                     const int32_t *route_row, const float *probs,
-                    const uint16_t *shared, uint16_t *out)
+                    const uint16_t *shared, const uint16_t *ori_x, uint16_t *out)
 {
     for (int64_t t = 0; t < T; ++t) {
         for (int64_t h = 0; h < H; ++h) {
             float acc = 0.0f;
             for (int64_t k = 0; k < K; ++k) {
                 int32_t r = route_row[t * K + k];
-                if (r < 0) continue;
-                float v = oracle_bf16_to_f32(y[(int64_t)r * H + h]);
+                float v;
+                if (r >= 0) v = oracle_bf16_to_f32(y[(int64_t)r * H + h]);
+                else if (r == -2) v = 0.0f;                                  /* zero expert */
+                else if (r == -3) v = oracle_bf16_to_f32(ori_x[t * H + h]);  /* copy expert */
+                else continue;
                 float prod = probs[t * K + k] * v;
                 acc = acc + prod;
             }
@@ -362,7 +391,8 @@ void oracle_combine(int64_t T, int64_t H, int64_t K, const uint16_t *y,
  * scale2 [E, H].  out_rows: bf16 [n_tokens, H].  Returns 1 on an int32
  * overflow in any accumulator.
  */
-int oracle_layer_tokens(int64_t T, int64_t H, int64_t E, int64_t K, int64_t N,
+int oracle_layer_tokens(int64_t T, int64_t H, int64_t E, int64_t Z, int64_t C,
+                        int64_t K, int64_t N,
                         const uint16_t *x, const int32_t *ids, int mask_kind,
                         const uint8_t *mask, const float *probs,
                         const uint16_t *shared,
@@ -379,14 +409,19 @@ int oracle_layer_tokens(int64_t T, int64_t H, int64_t E, int64_t K, int64_t N,
         int64_t t = tokens[i];
         for (int64_t h = 0; h < H; ++h) acc[h] = 0.0f;
         for (int64_t k = 0; k < K; ++k) {
-            if (!route_active(t, k, K, E, ids, mask_kind, mask)) continue;
-            int64_t e = ids[t * K + k];
-            overflow |= oracle_ffn_row(H, N, x + t * H,
-                                       w1 + e * N * H, scale1 + e * N,
-                                       w2 + e * H * Nh, scale2 + e * H,
-                                       NULL, NULL, NULL, NULL, NULL, NULL, NULL, y);
+            int cls = route_class(t, k, K, E, Z, C, ids, mask_kind, mask);
+            if (cls == ROUTE_OFF || cls == ROUTE_INVALID) continue;
+            if (cls == ROUTE_EXPERT) {
+                int64_t e = ids[t * K + k];
+                overflow |= oracle_ffn_row(H, N, x + t * H,
+                                           w1 + e * N * H, scale1 + e * N,
+                                           w2 + e * H * Nh, scale2 + e * H,
+                                           NULL, NULL, NULL, NULL, NULL, NULL, NULL, y);
+            }
             for (int64_t h = 0; h < H; ++h) {
-                float prod = probs[t * K + k] * oracle_bf16_to_f32(y[h]);
+                float v = cls == ROUTE_EXPERT ? oracle_bf16_to_f32(y[h])
+                        : cls == ROUTE_COPY ? oracle_bf16_to_f32(x[t * H + h]) : 0.0f;
+                float prod = probs[t * K + k] * v;
                 acc[h] = acc[h] + prod;
             }
         }
@@ -401,10 +436,11 @@ int oracle_layer_tokens(int64_t T, int64_t H, int64_t E, int64_t K, int64_t N,
     return overflow;
 }
 
-/* Identity-expert version of the above (y = the dispatched row itself):
- * out[t] = bf16(sum_k probs[t,k] * float(x[t]) + float(shared[t])). */
-void oracle_identity_tokens(int64_t T, int64_t H, int64_t E, int64_t K,
-                            const uint16_t *x, const int32_t *ids, int mask_kind,
+/* Identity-expert version of the above (y = the dispatched row itself; a
+ * copy expert also returns x[t], a zero expert returns 0):
+ * out[t] = bf16(sum_k probs[t,k] * v_k + float(shared[t])). */
+void oracle_identity_tokens(int64_t T, int64_t H, int64_t E, int64_t Z, int64_t C,
+                            int64_t K, const uint16_t *x, const int32_t *ids, int mask_kind,
                             const uint8_t *mask, const float *probs,
                             const uint16_t *shared, int64_t n_tokens,
                             const int64_t *tokens, uint16_t *out_rows)
@@ -414,8 +450,10 @@ void oracle_identity_tokens(int64_t T, int64_t H, int64_t E, int64_t K,
         for (int64_t h = 0; h < H; ++h) {
             float acc = 0.0f;
             for (int64_t k = 0; k < K; ++k) {
-                if (!route_active(t, k, K, E, ids, mask_kind, mask)) continue;
-                float prod = probs[t * K + k] * oracle_bf16_to_f32(x[t * H + h]);
+                int cls = route_class(t, k, K, E, Z, C, ids, mask_kind, mask);
+                if (cls == ROUTE_OFF || cls == ROUTE_INVALID) continue;
+                float v = cls == ROUTE_ZERO ? 0.0f : oracle_bf16_to_f32(x[t * H + h]);
+                float prod = probs[t * K + k] * v;
                 acc = acc + prod;
             }
             if (shared) acc = acc + oracle_bf16_to_f32(shared[t * H + h]);

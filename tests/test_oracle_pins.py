@@ -405,3 +405,74 @@ def test_layer_against_float64_restatement():
     gf = wl.bf16_bits_to_f32(got).astype(np.float64)
     rel = np.linalg.norm(gf - ref) / np.linalg.norm(ref)
     assert rel < 1e-2, rel
+
+
+# ---------------------------------------------------------------- special experts
+
+def test_route_special_expert_codes_brute_force():
+    """Ids in [E, E+Z) are zero experts (code -2), [E+Z, E+Z+C) copy experts
+    (code -3); neither gets a row or a count; anything beyond is invalid
+    ("aclnnMoeDistributeCombineV4", zeroExpertNum / copyExpertNum)."""
+    g = np.random.default_rng(12)
+    T, K, E, Z, C, P = 20, 4, 6, 2, 3, 4
+    ids = g.integers(-1, E + Z + C + 2, (T, K)).astype(np.int32)
+    mask = (g.random((T, K)) < 0.85).astype(np.uint8)
+    r = oracle.route(ids, E, P, mask, zero_experts=Z, copy_experts=C)
+    for t in range(T):
+        for k in range(K):
+            e, rr = ids[t, k], r["route_row"][t * K + k]
+            if not mask[t, k] or e < 0 or e >= E + Z + C:
+                assert rr == -1
+            elif e < E:
+                assert rr >= 0
+            elif e < E + Z:
+                assert rr == -2
+            else:
+                assert rr == -3
+    real = mask.astype(bool) & (ids >= 0) & (ids < E)
+    assert r["R"] == int(real.sum())
+    np.testing.assert_array_equal(r["counts"], np.bincount(ids[real], minlength=E))
+    bad = mask.astype(bool) & ((ids < 0) | (ids >= E + Z + C))
+    assert r["num_invalid"] == int(bad.sum())
+
+
+def test_combine_special_experts_closed_forms():
+    T, H, K, E, P = 16, 40, 4, 8, 2
+    g = np.random.default_rng(13)
+    x = wl.normal_bf16(4, "x", (T, H))
+    x[x == 0x8000] = 0
+    sh = wl.normal_bf16(5, "shared", (T, H))
+    probs = wl.softmax_probs(6, T, K)
+    # every slot a copy expert, probs summing to one: out == x bit for bit
+    ids = np.full((T, K), E + 1, np.int32)
+    r, ex, out = oracle.dispatch_combine_identity(x, ids, probs, E, P, zero_experts=1, copy_experts=1)
+    assert r["R"] == 0
+    np.testing.assert_array_equal(out, x)
+    # every slot a zero expert: the routed sum is zero, out = bf16(shared)
+    ids = np.full((T, K), E, np.int32)
+    r, ex, out = oracle.dispatch_combine_identity(x, ids, probs, E, P, shared=sh, zero_experts=1,
+                                                  copy_experts=1)
+    np.testing.assert_array_equal(out, sh)
+
+
+def test_combine_special_experts_against_float64():
+    T, H, K, E, Z, C, P = 24, 48, 4, 6, 2, 2, 3
+    g = np.random.default_rng(14)
+    ids = np.stack([g.permutation(E + Z + C)[:K] for _ in range(T)]).astype(np.int32)
+    x = wl.normal_bf16(7, "x", (T, H))
+    probs = g.uniform(-1, 1, (T, K)).astype(np.float32)
+    r = oracle.route(ids, E, P, zero_experts=Z, copy_experts=C)
+    y = wl.normal_bf16(8, "x", (max(r["R"], 1), H))[: r["R"]]
+    out = oracle.combine(y, r["route_row"], probs, ori_x=x)
+    yf = wl.bf16_bits_to_f32(y).astype(np.float64)
+    xf = wl.bf16_bits_to_f32(x).astype(np.float64)
+    ref = np.zeros((T, H))
+    for t in range(T):
+        for k in range(K):
+            e = ids[t, k]
+            if e < E:
+                ref[t] += probs[t, k] * yf[r["route_row"][t * K + k]]
+            elif e >= E + Z:
+                ref[t] += probs[t, k] * xf[t]
+    got = wl.bf16_bits_to_f32(out).astype(np.float64)
+    assert np.all(np.abs(got - ref) <= np.abs(ref) * 2 ** -8 + 1e-5)
