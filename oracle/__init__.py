@@ -76,6 +76,8 @@ def _load():
     lib.oracle_identity_tokens.argtypes = [I64, I64, I64, I64, I64, I64, P, P, ctypes.c_int,
                                            P, P, P, I64, P, P]
     lib.oracle_identity_tokens.restype = None
+    lib.oracle_dispatch_quant.argtypes = [I64, I64, I64, P, P, P, P, P, P]
+    lib.oracle_dispatch_quant.restype = None
     _lib = lib
     return lib
 
@@ -165,6 +167,20 @@ def gather(x: np.ndarray, route_row: np.ndarray, K: int, rows: int) -> np.ndarra
     out = np.zeros((max(rows, 0), H), np.uint16)
     lib.oracle_gather(T, H, int(K), _p(x), _p(rr), _p(out) if rows > 0 else None)
     return out
+
+
+def dispatch_quant(x, ids, route_row, rows, smooth=None):
+    """Quantised dispatch rows: (int8 [rows, H], fp32 scales [rows])."""
+    lib = _load()
+    x = _c(x, np.uint16)
+    ids = _c(ids, np.int32)
+    T, H = x.shape
+    K = ids.shape[1]
+    q = np.zeros((max(rows, 1), H), np.int8)
+    sc = np.zeros(max(rows, 1), np.float32)
+    lib.oracle_dispatch_quant(T, H, K, _p(x), _p(ids), _p(_c(route_row, np.int32)),
+                              _p(_c(smooth, np.float32)), _p(q), _p(sc))
+    return q[:rows], sc[:rows]
 
 
 def quant_row(v: np.ndarray):

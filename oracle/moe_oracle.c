@@ -210,6 +210,38 @@ void oracle_gather(int64_t T, int64_t H, int64_t K, const uint16_t *x,
 }
 
 /* ------------------------------------------------------------------ */
+/* Quantised dispatch: int8 rows with one dynamic scale per row.         */
+/* ------------------------------------------------------------------ */
+
+void oracle_quant_row(int64_t n, const float *v, int8_t *q, float *s_out);
+
+/* The dispatch of P2's sample run with a quantisation mode ("aclnnMoe-
+ * DistributeCombineV4", Example: DispatchV4 takes smooth scales [experts, H]
+ * when quantMode > 0 and returns int8 expandX with dynamicScales [A]): row r
+ * of token t routed to expert e holds the dynamic int8 quantisation of
+ * v = float(x[t]) * smooth[e] (or of float(x[t]) when smooth is NULL), and
+ * scales[r] its scale.  route_row comes from oracle_route.
+ * q: int8 [rows, H]; scales: fp32 [rows]. */
+void oracle_dispatch_quant(int64_t T, int64_t H, int64_t K, const uint16_t *x,
+                           const int32_t *ids, const int32_t *route_row,
+                           const float *smooth, int8_t *q, float *scales)
+{
+    float *v = (float *)malloc((size_t)H * sizeof(float));
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t k = 0; k < K; ++k) {
+            int32_t r = route_row[t * K + k];
+            if (r < 0) continue;
+            int64_t e = ids[t * K + k];
+            for (int64_t h = 0; h < H; ++h) {
+                float xv = oracle_bf16_to_f32(x[t * H + h]);
+                v[h] = smooth ? xv * smooth[e * H + h] : xv;
+            }
+            oracle_quant_row(H, v, q + (int64_t)r * H, &scales[r]);
+        }
+    free(v);
+}
+
+/* ------------------------------------------------------------------ */
 /* Dynamic per-row int8 quantisation (P3 FrontReorder Stage writes       */
 /* quantised rows with a per-row scale; SwiGLU: "dynamic quantization" */
 /* -> int8 + perTokenScale).                                             */

@@ -476,3 +476,34 @@ def test_combine_special_experts_against_float64():
                 ref[t] += probs[t, k] * xf[t]
     got = wl.bf16_bits_to_f32(out).astype(np.float64)
     assert np.all(np.abs(got - ref) <= np.abs(ref) * 2 ** -8 + 1e-5)
+
+
+# ---------------------------------------------------------------- quantised dispatch
+
+def test_dispatch_quant_matches_row_quantisation_and_scaling():
+    """Without smooth scales every row of a token carries the token's own
+    quantisation; with smooth scales row r is quant(x[t] * smooth[e]) -- checked
+    against a numpy restatement (float32 products, IEEE division, rint)."""
+    T, H, K, E, P = 24, 64, 3, 5, 2
+    g = np.random.default_rng(15)
+    ids = np.stack([g.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+    x = wl.normal_bf16(30, "x", (T, H))
+    r = oracle.route(ids, E, P)
+    q, s = oracle.dispatch_quant(x, ids, r["route_row"], r["R"])
+    xf = wl.bf16_bits_to_f32(x)
+    for row in range(r["R"]):
+        t = r["row_token"][row]
+        qq, ss = oracle.quant_row(xf[t])
+        np.testing.assert_array_equal(q[row], qq)
+        assert s[row] == np.float32(ss)
+    smooth = g.uniform(0.5, 2.0, (E, H)).astype(np.float32)
+    q, s = oracle.dispatch_quant(x, ids, r["route_row"], r["R"], smooth=smooth)
+    e_of_row = np.searchsorted(r["offsets"], np.arange(r["R"]), side="right") - 1
+    for row in range(r["R"]):
+        v = xf[r["row_token"][row]] * smooth[e_of_row[row]]
+        sc = np.float32(np.abs(v).max()) / np.float32(127.0)
+        ref = np.clip(np.rint(v / sc), -127, 127).astype(np.int8)
+        np.testing.assert_array_equal(q[row], ref)
+        assert s[row] == sc
+        # dequantised row within half a step of v
+        assert np.all(np.abs(q[row].astype(np.float64) * s[row] - v) <= 0.5 * s[row] * (1 + 1e-6))
