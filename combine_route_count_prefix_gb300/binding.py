@@ -35,6 +35,7 @@ EXPORTED = [
     "moe_read_device_status", "moe_launch_count", "moe_profile_enable",
     "moe_profile_report", "moe_status_string",
     "moe_dispatch_noalloc", "moe_dispatch_noalloc_scratch_bytes",
+    "moe_dispatch_quant", "moe_grouped_ffn_q",
 ]
 
 
@@ -48,7 +49,8 @@ class MoeShape(ctypes.Structure):
     _fields_ = [("num_tokens", ctypes.c_int64), ("num_partitions", ctypes.c_int64),
                 ("hidden", ctypes.c_int64), ("num_experts", ctypes.c_int64),
                 ("topk", ctypes.c_int64), ("ffn", ctypes.c_int64),
-                ("mask_kind", ctypes.c_int32), ("has_shared", ctypes.c_int32)]
+                ("mask_kind", ctypes.c_int32), ("has_shared", ctypes.c_int32),
+                ("zero_experts", ctypes.c_int64), ("copy_experts", ctypes.c_int64)]
 
 
 class StageViews(ctypes.Structure):
@@ -74,7 +76,7 @@ def lib():
     sig = {
         "moe_dispatch_workspace_size": [SP, ctypes.POINTER(SZ)],
         "moe_dispatch": [SP, P, P, P, P, P, P, P, P, P, P, SZ, P],
-        "moe_combine": [SP, P, P, P, P, P, P, P],
+        "moe_combine": [SP, P, P, P, P, P, P, P, P],
         "moe_packed_weight_bytes": [SP, ctypes.POINTER(SZ), ctypes.POINTER(SZ)],
         "moe_pack_weights": [SP, P, P, P, P, P],
         "moe_grouped_ffn_workspace_size": [SP, ctypes.POINTER(SZ)],
@@ -88,6 +90,8 @@ def lib():
         "moe_profile_enable": [ctypes.c_int],
         "moe_profile_report": [ctypes.c_char_p, SZ],
         "moe_dispatch_noalloc": [SP, P, P, P, P, P, P, P, P, P, P],
+        "moe_dispatch_quant": [SP, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P],
+        "moe_grouped_ffn_q": [SP, P, P, P, P, P, P, P, P, P, SZ, P],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -131,9 +135,10 @@ def _check(t, dtype, shape, name):
         raise ValueError(f"{name}: must be a CUDA tensor")
 
 
-def make_shape(T, P, H, E, K, N=0, mask_kind=0, has_shared=False) -> MoeShape:
+def make_shape(T, P, H, E, K, N=0, mask_kind=0, has_shared=False, zero_experts=0,
+               copy_experts=0) -> MoeShape:
     return MoeShape(int(T), int(P), int(H), int(E), int(K), int(N), int(mask_kind),
-                    int(bool(has_shared)))
+                    int(bool(has_shared)), int(zero_experts), int(copy_experts))
 
 
 def mask_kind_of(mask, T, K):
@@ -187,14 +192,15 @@ def workspace(nbytes, device=None):
 # ----------------------------------------------------------------- ops
 
 def dispatch(x, expert_ids, num_experts, num_partitions, mask=None, ws=None, out=None,
-             with_rows=True, stream=None):
+             with_rows=True, stream=None, zero_experts=0, copy_experts=0):
     """moe_dispatch.  Returns dict(expand_x, assist, expert_token_nums,
     expert_offsets, ep_recv_counts, route_row)."""
     T, K = expert_ids.shape
     H = x.shape[1] if x is not None else 8
     E, P = int(num_experts), int(num_partitions)
     dev = expert_ids.device
-    shape = make_shape(T, P, H, E, K, 0, mask_kind_of(mask, T, K))
+    shape = make_shape(T, P, H, E, K, 0, mask_kind_of(mask, T, K), False, zero_experts,
+                       copy_experts)
     _check(expert_ids, torch.int32, (T, K), "expert_ids")
     if x is not None:
         _check(x, torch.bfloat16, (T, H), "x")
@@ -245,13 +251,65 @@ def dispatch_noalloc(x, expert_ids, num_experts, num_partitions, mask=None, out=
     return out
 
 
+def dispatch_quant(x, expert_ids, num_experts, num_partitions, mask=None, smooth=None, ws=None,
+                   out=None, stream=None, zero_experts=0, copy_experts=0):
+    """moe_dispatch_quant: int8 rows + per-row dynamic scales (optional
+    per-expert smooth scales fp32 [E, H]).  Returns the dispatch dict with
+    expand_x int8 [T*K, H] and dynamic_scales fp32 [T*K]."""
+    T, K = expert_ids.shape
+    H = x.shape[1]
+    E, P = int(num_experts), int(num_partitions)
+    dev = expert_ids.device
+    shape = make_shape(T, P, H, E, K, 0, mask_kind_of(mask, T, K), False, zero_experts,
+                       copy_experts)
+    _check(expert_ids, torch.int32, (T, K), "expert_ids")
+    _check(x, torch.bfloat16, (T, H), "x")
+    _check(smooth, torch.float32, (E, H), "smooth")
+    if out is None:
+        out = dict(
+            expand_x=torch.empty((T * K, H), dtype=torch.int8, device=dev),
+            dynamic_scales=torch.empty(T * K, dtype=torch.float32, device=dev),
+            assist=torch.empty((T * K, 3), dtype=torch.int32, device=dev),
+            expert_token_nums=torch.empty(E, dtype=torch.int64, device=dev),
+            expert_offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+            ep_recv_counts=torch.empty(E * P, dtype=torch.int32, device=dev),
+            route_row=torch.empty(T * K, dtype=torch.int32, device=dev))
+    if ws is None:
+        _, ws = _alloc_ws(dispatch_workspace_size(shape), dev)
+    _call("moe_dispatch_quant", ctypes.byref(shape), _ptr(x), _ptr(expert_ids), _ptr(mask),
+          _ptr(smooth), _ptr(out["expand_x"]), _ptr(out["dynamic_scales"]), _ptr(out["assist"]),
+          _ptr(out["expert_token_nums"]), _ptr(out["expert_offsets"]), _ptr(out["ep_recv_counts"]),
+          _ptr(out["route_row"]), _ptr(ws), ctypes.c_size_t(ws.numel()), _stream(stream))
+    out["workspace"] = ws
+    return out
+
+
+def grouped_ffn_q(shape: MoeShape, expand_x_q, dynamic_scales, expert_offsets, w1p, scale1,
+                  w2p, scale2, ws=None, y=None, stream=None):
+    """moe_grouped_ffn_q: the grouped FFN on int8 rows with per-row scales."""
+    T, K, H, E, N = shape.num_tokens, shape.topk, shape.hidden, shape.num_experts, shape.ffn
+    _check(expand_x_q, torch.int8, (T * K, H), "expand_x")
+    _check(dynamic_scales, torch.float32, (T * K,), "dynamic_scales")
+    _check(expert_offsets, torch.int32, (E + 1,), "expert_offsets")
+    if y is None:
+        y = torch.empty((T * K, H), dtype=torch.bfloat16, device=expand_x_q.device)
+    if ws is None:
+        _, ws = _alloc_ws(grouped_ffn_workspace_size(shape), expand_x_q.device)
+    _call("moe_grouped_ffn_q", ctypes.byref(shape), _ptr(expand_x_q), _ptr(dynamic_scales),
+          _ptr(expert_offsets), _ptr(w1p), _ptr(scale1), _ptr(w2p), _ptr(scale2), _ptr(y),
+          _ptr(ws), ctypes.c_size_t(ws.numel()), _stream(stream))
+    return y, ws
+
+
 def combine(expand_x, route_row, expert_scales, num_experts, num_partitions, mask=None,
-            shared=None, out=None, stream=None):
-    """moe_combine.  Returns x_out bf16 [T, H]."""
+            shared=None, out=None, stream=None, ori_x=None, zero_experts=0, copy_experts=0):
+    """moe_combine.  ori_x: the tokens before the FFN, read by copy experts.
+    Returns x_out bf16 [T, H]."""
     T, K = expert_scales.shape
     H = expand_x.shape[1]
     shape = make_shape(T, num_partitions, H, num_experts, K, 0, mask_kind_of(mask, T, K),
-                       shared is not None)
+                       shared is not None, zero_experts, copy_experts)
+    _check(ori_x, torch.bfloat16, (T, H), "ori_x")
     _check(expand_x, torch.bfloat16, (T * K, H), "expand_x")
     _check(route_row, torch.int32, (T * K,), "route_row")
     _check(expert_scales, torch.float32, (T, K), "expert_scales")
@@ -259,7 +317,7 @@ def combine(expand_x, route_row, expert_scales, num_experts, num_partitions, mas
     if out is None:
         out = torch.empty((T, H), dtype=torch.bfloat16, device=expand_x.device)
     _call("moe_combine", ctypes.byref(shape), _ptr(expand_x), _ptr(route_row), _ptr(expert_scales),
-          _ptr(mask), _ptr(shared), _ptr(out), _stream(stream))
+          _ptr(mask), _ptr(shared), _ptr(ori_x), _ptr(out), _stream(stream))
     return out
 
 

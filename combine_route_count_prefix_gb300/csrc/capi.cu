@@ -83,6 +83,9 @@ moe_status check_shape(const moe_shape *s, bool need_ffn) {
     if (s->num_experts < 1 || s->num_experts > kMaxExperts) return MOE_ERR_SHAPE;
     if (s->topk < 1 || s->topk > kMaxTopK) return MOE_ERR_SHAPE;
     if (s->mask_kind < 0 || s->mask_kind > 2) return MOE_ERR_PARAM_INVALID;
+    if (s->zero_experts < 0 || s->copy_experts < 0 ||
+        s->num_experts + s->zero_experts + s->copy_experts > INT32_MAX)
+        return MOE_ERR_SHAPE;
     if (s->has_shared != 0 && s->has_shared != 1) return MOE_ERR_PARAM_INVALID;
     const int64_t cap = s->num_tokens * s->topk;
     if (cap > INT32_MAX) return MOE_ERR_SHAPE;
@@ -148,6 +151,8 @@ static RouteDev route_dev(const moe_shape &s, const int32_t *ids, const uint8_t 
     r.M = s.num_tokens / s.num_partitions;
     r.K = s.topk;
     r.E = s.num_experts;
+    r.Z = s.zero_experts;
+    r.C = s.copy_experts;
     r.chunk_tokens = route_chunk_tokens(r.T);
     r.chunks_per_partition = (r.M + r.chunk_tokens - 1) / r.chunk_tokens;
     if (r.chunks_per_partition == 0) r.chunks_per_partition = 1;
@@ -269,14 +274,44 @@ moe_status moe_dispatch(const moe_shape *shape, const void *x, const int32_t *ex
     return launch_route_resolve(r, route_row, assist, stream);
 }
 
+moe_status moe_dispatch_quant(const moe_shape *shape, const void *x, const int32_t *expert_ids,
+                              const uint8_t *x_active_mask, const float *smooth_scales,
+                              int8_t *expand_x, float *dynamic_scales, int32_t *assist,
+                              int64_t *expert_token_nums, int32_t *expert_offsets,
+                              int32_t *ep_recv_counts, int32_t *route_row, void *workspace,
+                              size_t workspace_bytes, cudaStream_t stream) {
+    MOE_TRY(check_shape(shape, false));
+    const moe_shape &s = *shape;
+    const bool empty = s.num_tokens == 0;
+    if (s.hidden > 8192) return MOE_ERR_SHAPE;
+    if (!expert_token_nums || !expert_offsets || !ep_recv_counts || !workspace) return MOE_ERR_NULLPTR;
+    if (!empty && (!x || !expert_ids || !assist || !route_row || !expand_x || !dynamic_scales))
+        return MOE_ERR_NULLPTR;
+    if (!empty && s.mask_kind != 0 && !x_active_mask) return MOE_ERR_NULLPTR;
+    if (s.mask_kind == 0 && x_active_mask) return MOE_ERR_PARAM_INVALID;
+    if (!aligned(x, 16) || !aligned(expand_x, 16) || !aligned(smooth_scales, 16) ||
+        !aligned(workspace, kAlign) || !aligned(dynamic_scales, 4))
+        return MOE_ERR_ALIGNMENT;
+    const Layout L = layout_for(s, Op::Dispatch);
+    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+    RouteDev r = route_dev(s, expert_ids, x_active_mask, workspace, L);
+    MOE_TRY(launch_route_fused(r, route_chunks(s), expert_token_nums, expert_offsets,
+                               ep_recv_counts, nullptr, route_row, assist, stream));
+    return launch_dispatch_quant(r, x, smooth_scales, route_row, assist, expand_x, dynamic_scales,
+                                 s.hidden, stream);
+}
+
 // ---------------------------------------------------------------- combine
 moe_status moe_combine(const moe_shape *shape, const void *expand_x, const int32_t *route_row,
                        const float *expert_scales, const uint8_t *x_active_mask,
-                       const void *shared_expert_x, void *x_out, cudaStream_t stream) {
+                       const void *shared_expert_x, const void *ori_x, void *x_out,
+                       cudaStream_t stream) {
     MOE_TRY(check_shape(shape, false));
     const moe_shape &s = *shape;
     if (s.num_tokens == 0) return MOE_OK;
     if (!expand_x || !route_row || !expert_scales || !x_out) return MOE_ERR_NULLPTR;
+    if (s.copy_experts > 0 && !ori_x) return MOE_ERR_NULLPTR;
+    if (ori_x && !aligned(ori_x, 16)) return MOE_ERR_ALIGNMENT;
     if (s.has_shared && !shared_expert_x) return MOE_ERR_NULLPTR;
     if (!s.has_shared && shared_expert_x) return MOE_ERR_PARAM_INVALID;
     if (s.mask_kind != 0 && !x_active_mask) return MOE_ERR_NULLPTR;
@@ -286,8 +321,9 @@ moe_status moe_combine(const moe_shape *shape, const void *expand_x, const int32
         !aligned(expert_scales, 4))
         return MOE_ERR_ALIGNMENT;
     return launch_combine(expand_x, route_row, expert_scales, x_active_mask, s.mask_kind,
-                          shared_expert_x, x_out, s.num_tokens, s.topk, s.hidden,
-                          s.num_tokens * s.topk, nullptr, stream);
+                          shared_expert_x, s.copy_experts > 0 ? ori_x : nullptr,
+                          s.zero_experts + s.copy_experts > 0, x_out, s.num_tokens, s.topk,
+                          s.hidden, s.num_tokens * s.topk, nullptr, stream);
 }
 
 // ---------------------------------------------------------------- weights
@@ -384,6 +420,32 @@ moe_status moe_grouped_ffn(const moe_shape *shape, const void *expand_x,
                         stream);
 }
 
+moe_status moe_grouped_ffn_q(const moe_shape *shape, const int8_t *expand_x,
+                             const float *dynamic_scales, const int32_t *expert_offsets,
+                             const void *w1_packed, const float *scale1, const void *w2_packed,
+                             const float *scale2, void *y, void *workspace,
+                             size_t workspace_bytes, cudaStream_t stream) {
+    MOE_TRY(check_shape(shape, true));
+    const moe_shape &s = *shape;
+    if (!expand_x || !dynamic_scales || !expert_offsets || !w1_packed || !scale1 || !w2_packed ||
+        !scale2 || !y || !workspace)
+        return MOE_ERR_NULLPTR;
+    if (!aligned(expand_x, 16) || !aligned(y, 16) || !aligned(scale1, 16) || !aligned(scale2, 16) ||
+        !aligned(w1_packed, kAlign) || !aligned(w2_packed, kAlign) || !aligned(workspace, kAlign))
+        return MOE_ERR_ALIGNMENT;
+    const Layout L = layout_for(s, Op::Ffn);
+    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+    if (s.num_tokens == 0) return MOE_OK;
+    const int64_t cap = s.num_tokens * s.topk;
+    MOE_TRY(launch_sched(expert_offsets, s.num_experts, at<int32_t>(workspace, L.sched),
+                         at<int32_t>(workspace, L.status), stream));
+    MOE_TRY(launch_rows_i8_to_f16(expand_x, dynamic_scales, expert_offsets, s.num_experts,
+                                  at<void>(workspace, L.q1), at<float>(workspace, L.s1), cap,
+                                  s.hidden, stream));
+    return run_ffn_core(s, L, workspace, expert_offsets, w1_packed, scale1, w2_packed, scale2, y,
+                        stream);
+}
+
 // ---------------------------------------------------------------- whole layer
 moe_status moe_layer_workspace_size(const moe_shape *shape, size_t *bytes) {
     MOE_TRY(check_shape(shape, true));
@@ -427,6 +489,7 @@ moe_status moe_layer(const moe_shape *shape, const void *x, const int32_t *exper
     void *y = at<void>(workspace, L.y);
     MOE_TRY(run_ffn_core(s, L, workspace, offsets, w1_packed, scale1, w2_packed, scale2, y, stream));
     return launch_combine(y, route_row, expert_scales, x_active_mask, s.mask_kind, shared_expert_x,
+                          s.copy_experts > 0 ? x : nullptr, s.zero_experts + s.copy_experts > 0,
                           x_out, s.num_tokens, s.topk, s.hidden, cap,
                           at<int32_t>(workspace, L.status), stream);
 }

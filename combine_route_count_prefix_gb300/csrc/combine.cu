@@ -39,10 +39,14 @@ constexpr size_t kStageTarget = 64 * 1024;
 constexpr size_t kSmemBudget = 196 * 1024;
 constexpr uint32_t kFull = 0xffffffffu;
 
+// One work item: n terms in slot order with their probabilities; with
+// special experts, term j adds p[j] * (stage slot src[j], or 0 when
+// src[j] < 0: a zero expert).
 struct ItemHdr {
     int32_t n;
     int32_t pad[3];
     float p[kMaxTopK];
+    int32_t src[kMaxTopK];
 };
 
 struct CombineArgs {
@@ -51,9 +55,10 @@ struct CombineArgs {
     const float *probs;
     const uint8_t *mask;
     const uint4 *shared;
+    const uint4 *ori_x;
     uint4 *out;
     int64_t T, H8, cap_rows, tokens_per_cta;
-    int K, mask_kind, stages, nseg, seg_vecs;
+    int K, mask_kind, stages, nseg, seg_vecs, slots;
     int32_t *status;
 };
 
@@ -79,19 +84,42 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
 }
 
-__host__ __device__ inline size_t stage_bytes(int K, int seg_vecs) { return (size_t)(K + 1) * seg_vecs * 16; }
+// Stage slots: up to K row segments, the shared-expert segment (slot K) and,
+// when copy experts exist, the oriX segment (slot K + 1).
+__host__ __device__ inline size_t stage_bytes(int slots, int seg_vecs) {
+    return (size_t)slots * seg_vecs * 16;
+}
 
-size_t smem_bytes(int K, int stages, int seg_vecs) {
-    return 128 + (size_t)stages * stage_bytes(K, seg_vecs) + stages * sizeof(ItemHdr) +
+size_t smem_bytes(int K, int slots, int stages, int seg_vecs) {
+    return 128 + (size_t)stages * stage_bytes(slots, seg_vecs) + stages * sizeof(ItemHdr) +
            2 * stages * sizeof(uint64_t) + 16 + 2 * 32 * (size_t)K * (sizeof(int32_t) + sizeof(float));
 }
 
+// Adds the shared-expert vector (slot K) if present, rounds to bf16, stores.
+__device__ __forceinline__ void store_result(const CombineArgs &a, const uint8_t *src, int v,
+                                             int64_t out_idx, float (&acc)[8]) {
+    if (a.shared) {
+        float f[8];
+        unpack8(lds128(src + ((size_t)a.K * a.seg_vecs + v) * 16), f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], f[i]);
+    }
+    uint4 o;
+    o.x = pack_bf16x2(acc[0], acc[1]);
+    o.y = pack_bf16x2(acc[2], acc[3]);
+    o.z = pack_bf16x2(acc[4], acc[5]);
+    o.w = pack_bf16x2(acc[6], acc[7]);
+    a.out[out_idx] = o;
+}
+
+// kSpecial: the shape has zero or copy experts (route_row codes -2 / -3).
+template <bool kSpecial>
 __global__ void __launch_bounds__(kThreads, 1)
 k_combine(CombineArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
                                                 ~(uintptr_t)127);
-    const size_t sbytes = stage_bytes(a.K, a.seg_vecs);
+    const size_t sbytes = stage_bytes(a.slots, a.seg_vecs);
     uint8_t *bufs = smem;
     ItemHdr *hdrs = reinterpret_cast<ItemHdr *>(bufs + a.stages * sbytes);
     uint64_t *full = reinterpret_cast<uint64_t *>(hdrs + a.stages);
@@ -143,7 +171,9 @@ k_combine(CombineArgs a) {
 #pragma unroll
             for (int k = 0; k < kMaxTopK; ++k) {
                 if (k >= a.K) break;
-                bool on = tok && rr[k] >= 0 && rr[k] < a.cap_rows;
+                // a row; with special experts also a zero (-2) or copy (-3) slot
+                bool on = tok && ((rr[k] >= 0 && rr[k] < a.cap_rows) ||
+                                  (kSpecial && (rr[k] == -2 || (rr[k] == -3 && a.ori_x))));
                 if (a.mask_kind == 2 && in) on = on && a.mask[t * a.K + k] != 0;
                 rr[k] = on ? rr[k] : -1;
             }
@@ -182,11 +212,27 @@ k_combine(CombineArgs a) {
                         const uint32_t bytes = (uint32_t)(min((int64_t)a.seg_vecs, a.H8 - v0) * 16);
                         ItemHdr *h = hdrs + stage;
                         uint8_t *dst = bufs + stage * sbytes;
-                        int n = 0;
-                        for (int k = 0; k < a.K; ++k)
-                            if (rows[k] >= 0) h->p[n++] = ps[k];
+                        int n = 0, nrow = 0;
+                        bool need_ori = false;
+                        if (kSpecial) {
+                            for (int k = 0; k < a.K; ++k) {
+                                const int32_t code = rows[k];
+                                if (code == -1) continue;
+                                h->p[n] = ps[k];
+                                if (code >= 0) h->src[n] = nrow++;
+                                else if (code == -2) h->src[n] = -1;
+                                else { h->src[n] = a.K + 1; need_ori = true; }
+                                ++n;
+                            }
+                        } else {
+                            for (int k = 0; k < a.K; ++k)
+                                if (rows[k] >= 0) h->p[n++] = ps[k];
+                            nrow = n;
+                        }
                         h->n = n;
-                        mbar_arrive_expect_tx(&full[stage], (uint32_t)(n + (a.shared ? 1 : 0)) * bytes);
+                        const uint32_t loads =
+                            (uint32_t)(nrow + (a.shared ? 1 : 0) + (need_ori ? 1 : 0));
+                        mbar_arrive_expect_tx(&full[stage], loads * bytes);
                         int jj = 0;
                         for (int k = 0; k < a.K; ++k) {
                             if (rows[k] < 0) continue;
@@ -197,6 +243,9 @@ k_combine(CombineArgs a) {
                         if (a.shared)
                             bulk_load(dst + (size_t)a.K * a.seg_vecs * 16, a.shared + tt * a.H8 + v0,
                                       bytes, &full[stage]);
+                        if (need_ori)
+                            bulk_load(dst + (size_t)(a.K + 1) * a.seg_vecs * 16,
+                                      a.ori_x + tt * a.H8 + v0, bytes, &full[stage]);
                         issued_phase[stage] = (int)phase;
                         if (++stage == a.stages) { stage = 0; phase ^= 1u; }
                     }
@@ -230,32 +279,51 @@ k_combine(CombineArgs a) {
                 const int64_t v0 = (int64_t)seg * a.seg_vecs;
                 const int len = (int)min((int64_t)a.seg_vecs, a.H8 - v0);
                 const int n = h->n;
+                if (kSpecial) {
+                    // the item's terms in registers; a zero-expert term adds p * 0
+                    int sl[kMaxTopK];
+                    float pr[kMaxTopK];
 #pragma unroll
-                for (int u = 0; u < kVecsPerThread; ++u) {
-                    const int v = c + u * kConsumerWarps * 32;
-                    if (v >= len) continue;
-                    float acc[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-                    for (int jj = 0; jj < n; ++jj) {
-                        float f[8];
-                        unpack8(lds128(src + ((size_t)jj * a.seg_vecs + v) * 16), f);
-                        const float p = h->p[jj];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(p, f[i]));
+                    for (int j = 0; j < kMaxTopK; ++j) {
+                        sl[j] = (j < n) ? h->src[j] : 0;
+                        pr[j] = (j < n) ? h->p[j] : 0.0f;
                     }
-                    if (a.shared) {
-                        float f[8];
-                        unpack8(lds128(src + ((size_t)a.K * a.seg_vecs + v) * 16), f);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], f[i]);
+                    for (int u = 0; u < kVecsPerThread; ++u) {
+                        const int v = c + u * kConsumerWarps * 32;
+                        if (v >= len) continue;
+                        float acc[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+#pragma unroll
+                        for (int j = 0; j < kMaxTopK; ++j) {
+                            if (j >= n) break;
+                            const bool zero = sl[j] < 0;
+                            float f[8];
+                            unpack8(lds128(src + ((size_t)(zero ? 0 : sl[j]) * a.seg_vecs + v) * 16), f);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                acc[i] = __fadd_rn(acc[i], __fmul_rn(pr[j], zero ? 0.0f : f[i]));
+                        }
+                        store_result(a, src, v, tt * a.H8 + v0 + v, acc);
                     }
-                    uint4 o;
-                    o.x = pack_bf16x2(acc[0], acc[1]);
-                    o.y = pack_bf16x2(acc[2], acc[3]);
-                    o.z = pack_bf16x2(acc[4], acc[5]);
-                    o.w = pack_bf16x2(acc[6], acc[7]);
-                    a.out[tt * a.H8 + v0 + v] = o;
+                } else {
+#pragma unroll
+                    for (int u = 0; u < kVecsPerThread; ++u) {
+                        const int v = c + u * kConsumerWarps * 32;
+                        if (v >= len) continue;
+                        float acc[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+                        for (int jj = 0; jj < n; ++jj) {
+                            float f[8];
+                            unpack8(lds128(src + ((size_t)jj * a.seg_vecs + v) * 16), f);
+                            const float p = h->p[jj];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(p, f[i]));
+                        }
+                        store_result(a, src, v, tt * a.H8 + v0 + v, acc);
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[stage]);
@@ -268,9 +336,9 @@ k_combine(CombineArgs a) {
 }  // namespace
 
 moe_status launch_combine(const void *y, const int32_t *route_row, const float *probs,
-                          const uint8_t *mask, int mask_kind, const void *shared, void *out,
-                          int64_t T, int64_t K, int64_t H, int64_t cap_rows, int32_t *status,
-                          cudaStream_t stream) {
+                          const uint8_t *mask, int mask_kind, const void *shared,
+                          const void *ori_x, bool special, void *out, int64_t T, int64_t K,
+                          int64_t H, int64_t cap_rows, int32_t *status, cudaStream_t stream) {
     if (T == 0) return MOE_OK;
     CombineArgs a;
     a.y = static_cast<const uint4 *>(y);
@@ -278,32 +346,42 @@ moe_status launch_combine(const void *y, const int32_t *route_row, const float *
     a.probs = probs;
     a.mask = mask;
     a.shared = static_cast<const uint4 *>(shared);
+    a.ori_x = static_cast<const uint4 *>(ori_x);
     a.out = static_cast<uint4 *>(out);
     a.T = T;
     a.H8 = H / 8;
     a.cap_rows = cap_rows;
     a.K = (int)K;
     a.mask_kind = mask_kind;
-    // segment length: at most 512 vectors and about 64 KB per stage over K+1 rows
-    int64_t maxv = (int64_t)(kStageTarget / ((size_t)(K + 1) * 16));
+    // segment length: at most 512 vectors, a multiple of 8 (128-byte aligned
+    // copies), about 64 KB per stage over all slots
+    a.slots = a.K + 1 + (ori_x ? 1 : 0);
+    int64_t maxv = (int64_t)(kStageTarget / ((size_t)a.slots * 16));
     if (maxv > kMaxSegVecs) maxv = kMaxSegVecs;
+    maxv = maxv / 8 * 8;
+    if (maxv < 8) maxv = 8;
     a.nseg = (int)((a.H8 + maxv - 1) / maxv);
-    a.seg_vecs = (int)((a.H8 + a.nseg - 1) / a.nseg);
-    a.stages = (int)(kSmemBudget / stage_bytes(a.K, a.seg_vecs));
+    a.seg_vecs = (int)(((a.H8 + a.nseg - 1) / a.nseg + 7) / 8 * 8);
+    a.stages = (int)(kSmemBudget / stage_bytes(a.slots, a.seg_vecs));
     if (a.stages > kMaxStages) a.stages = kMaxStages;
     if (a.stages < 2) a.stages = 2;
     const int64_t grid = T < num_sms() ? T : (int64_t)num_sms();
     a.tokens_per_cta = 0;
     a.status = status;
-    const size_t smem = smem_bytes(a.K, a.stages, a.seg_vecs);
-    static size_t configured = 0;
-    if (smem > configured) {
-        if (cudaFuncSetAttribute(k_combine, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const size_t smem = smem_bytes(a.K, a.slots, a.stages, a.seg_vecs);
+    static size_t configured[2] = {0, 0};
+    if (smem > configured[special]) {
+        if (cudaFuncSetAttribute(special ? k_combine<true> : k_combine<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem) != cudaSuccess)
             return MOE_ERR_CUDA;
-        configured = smem;
+        configured[special] = smem;
     }
-    MOE_LAUNCH("combine", k_combine, (unsigned)grid, kThreads, smem, stream, a);
+    if (special) {
+        MOE_LAUNCH("combine", k_combine<true>, (unsigned)grid, kThreads, smem, stream, a);
+    } else {
+        MOE_LAUNCH("combine", k_combine<false>, (unsigned)grid, kThreads, smem, stream, a);
+    }
     return MOE_OK;
 }
 

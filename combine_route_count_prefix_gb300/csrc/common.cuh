@@ -138,6 +138,7 @@ struct RouteDev {
     const uint8_t *mask;
     int mask_kind;
     int64_t T, P, M, K, E;
+    int64_t Z, C;          // zero and copy experts after the E MoE experts
     int64_t chunk_tokens;
     int64_t chunks_per_partition;
     int32_t *hist;     // [chunks][E]
@@ -145,6 +146,15 @@ struct RouteDev {
     int32_t *status;
     int rows_final;    // 1: route_row already holds final rows (single-kernel routing)
 };
+
+// Route code of an active route's expert id: the id itself for a MoE expert,
+// -2 for a zero expert, -3 for a copy expert, -4 for an id naming no expert.
+__device__ __forceinline__ int route_code(int e, const RouteDev &a) {
+    if (e >= 0 && e < a.E) return e;
+    if (e >= a.E && e < a.E + a.Z) return -2;
+    if (e >= a.E + a.Z && e < a.E + a.Z + a.C) return -3;
+    return -4;
+}
 
 // Final row of route (t, k): route_row holds the route's rank inside its
 // routing chunk (or -1) after launch_route; the chunk base of its expert is
@@ -155,7 +165,7 @@ __device__ __forceinline__ int32_t resolve_route_row(const RouteDev &a, int64_t 
                                                      int32_t *route_row, int32_t *assist) {
     const int64_t i = t * a.K + k;
     const int32_t lr = route_row[i];
-    if (lr < 0) return -1;
+    if (lr < 0) return lr;   // inactive (-1) or a special expert (-2, -3): no row
     if (a.rows_final) return lr;
     const int e = a.ids[i];
     // T * K < 2^31, so token, partition and chunk indices fit in 32 bits
@@ -193,10 +203,12 @@ moe_status launch_dispatch_rows(const RouteDev &r, const void *x, int32_t *route
                                 int32_t *assist, void *expand_x, int64_t H, cudaStream_t stream);
 
 // status may be NULL (bounded waits that give up then only abort the kernel).
+// special: the shape has zero or copy experts (route_row codes -2 / -3);
+// ori_x is read by copy experts.
 moe_status launch_combine(const void *y, const int32_t *route_row, const float *probs,
-                          const uint8_t *mask, int mask_kind, const void *shared, void *out,
-                          int64_t T, int64_t K, int64_t H, int64_t cap_rows, int32_t *status,
-                          cudaStream_t stream);
+                          const uint8_t *mask, int mask_kind, const void *shared,
+                          const void *ori_x, bool special, void *out, int64_t T, int64_t K,
+                          int64_t H, int64_t cap_rows, int32_t *status, cudaStream_t stream);
 
 // Resolves every route's row and writes the int8 codes (fp16 images) and
 // scale of the quantised token x[t] to each of its rows.
@@ -204,6 +216,13 @@ moe_status launch_quant_scatter(const RouteDev &r, const void *x, int32_t *route
                                 int32_t *assist, void *q1, float *s1, int64_t H,
                                 cudaStream_t stream);
 
+// Quantised dispatch rows (int8 bytes) and their scales; resolves the rows.
+moe_status launch_dispatch_quant(const RouteDev &r, const void *x, const float *smooth,
+                                 int32_t *route_row, int32_t *assist, int8_t *q, float *scales,
+                                 int64_t H, cudaStream_t stream);
+moe_status launch_rows_i8_to_f16(const int8_t *rows, const float *scales, const int32_t *offsets,
+                                 int64_t E, void *q1, float *s1, int64_t cap_rows, int64_t H,
+                                 cudaStream_t stream);
 moe_status launch_quant_rows(const void *x_rows, const int32_t *offsets, int64_t E, void *q1,
                              float *s1, int64_t cap_rows, int64_t H, cudaStream_t stream);
 

@@ -99,6 +99,8 @@ moe_status moe_dispatch_noalloc(const moe_shape *shape, const void *x, const int
     r.M = s.num_tokens / s.num_partitions;
     r.K = s.topk;
     r.E = s.num_experts;
+    r.Z = s.zero_experts;
+    r.C = s.copy_experts;
     r.chunk_tokens = route_chunk_tokens(r.T);
     r.chunks_per_partition = (r.M + r.chunk_tokens - 1) / r.chunk_tokens;
     if (r.chunks_per_partition == 0) r.chunks_per_partition = 1;

@@ -8,7 +8,8 @@
 //                       expert's block in "Local data copy")
 //   recv_cum[e*P + p]   inclusive running sum over (expert, partition)
 //                       (ep_receive_count)
-//   route_row[t*K + k]  row of route (t, k) (expandedRowIdx), -1 if inactive
+//   route_row[t*K + k]  row of route (t, k) (expandedRowIdx); -1 if inactive,
+//                       -2 / -3 for a zero / copy expert (no row)
 //   assist[row]         (partition, token in partition, slot)
 // Row order is expert, then partition, then token, then slot.  Within one
 // expert this is the route order, so a route's row is offsets[e] plus the
@@ -96,13 +97,16 @@ k_route_local(RouteDev a, int32_t *local_rank) {
             else if (a.mask_kind == 2) m_reg[j] = __ldg(a.mask + i);
         }
     }
+    // e_reg: the expert (>= 0), -1 inactive, -2 zero expert, -3 copy expert
     bool bad = false;
 #pragma unroll
     for (int j = 0; j < kMaxWindows; ++j) {
         if (j >= nwin) break;
-        int e = e_reg[j];
-        if (w0 + 32 * j + lane >= w1 || m_reg[j] == 0) e = -1;
-        else if (e < 0 || e >= a.E) { bad = true; e = -1; }
+        int e = -1;
+        if (w0 + 32 * j + lane < w1 && m_reg[j] != 0) {
+            e = route_code(e_reg[j], a);
+            if (e == -4) { bad = true; e = -1; }
+        }
         e_reg[j] = e;
     }
     __syncthreads();   // hw cleared
@@ -139,7 +143,7 @@ k_route_local(RouteDev a, int32_t *local_rank) {
     for (int j = 0; j < kMaxWindows; ++j) {
         if (j >= nwin) break;
         const int64_t i = w0 + 32 * j + lane;
-        if (i < w1) local_rank[i] = (e_reg[j] >= 0) ? rl[j] + mine[e_reg[j]] : -1;
+        if (i < w1) local_rank[i] = (e_reg[j] >= 0) ? rl[j] + mine[e_reg[j]] : e_reg[j];
     }
 }
 
@@ -331,13 +335,16 @@ k_route_fused(RouteDev a, int64_t chunks, int64_t *counts, int32_t *offsets, int
             else if (a.mask_kind == 2) m_reg[j] = __ldg(a.mask + i);
         }
     }
+    // e_reg: the expert (>= 0), -1 inactive, -2 zero expert, -3 copy expert
     bool bad = false;
 #pragma unroll
     for (int j = 0; j < kMaxWindows; ++j) {
         if (j >= nwin) break;
-        int e = e_reg[j];
-        if (w0 + 32 * j + lane >= w1 || m_reg[j] == 0) e = -1;
-        else if (e < 0 || e >= a.E) { bad = true; e = -1; }
+        int e = -1;
+        if (w0 + 32 * j + lane < w1 && m_reg[j] != 0) {
+            e = route_code(e_reg[j], a);
+            if (e == -4) { bad = true; e = -1; }
+        }
         e_reg[j] = e;
     }
     __syncthreads();
@@ -467,7 +474,7 @@ k_route_fused(RouteDev a, int64_t chunks, int64_t *counts, int32_t *offsets, int
         if (j >= nwin) break;
         const int64_t i = w0 + 32 * j + lane;
         if (i >= w1) continue;
-        int32_t row = -1;
+        int32_t row = e_reg[j];   // -1 inactive, -2 / -3 special expert
         if (e_reg[j] >= 0) {
             row = below_s[e_reg[j]] + rl[j];
             const int32_t t32 = (int32_t)(i / K32);

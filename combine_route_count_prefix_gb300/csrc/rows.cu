@@ -176,6 +176,120 @@ k_quant_bf16_rows(RouteDev ra, const uint4 *__restrict__ src, int32_t *__restric
     }
 }
 
+// ---------------------------------------------------------------- quantised dispatch
+// Row r of token t and expert e gets the dynamic int8 quantisation of
+// float(x[t]) * smooth[e] (kSmooth) or of float(x[t]), as int8 bytes, and its
+// scale.  Without smooth scales the token is quantised once and its codes are
+// written to every one of its rows.
+__device__ __forceinline__ uint2 pack_i8x8(const float (&c)[8]) {
+    uint32_t w[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i >> 2] |= ((uint32_t)((int32_t)c[i]) & 0xffu) << (8 * (i & 3));
+    return make_uint2(w[0], w[1]);
+}
+
+template <bool kSmooth>
+__global__ void __launch_bounds__(kRowThreads)
+k_dispatch_quant(RouteDev ra, const uint4 *__restrict__ x, const float4 *__restrict__ smooth,
+                 int32_t *__restrict__ route_row, int32_t *__restrict__ assist,
+                 uint2 *__restrict__ q, float *__restrict__ s_out, int64_t H8) {
+    __shared__ int32_t rows[kMaxTopK];
+    __shared__ int32_t experts[kMaxTopK];
+    __shared__ int32_t nrows;
+    __shared__ float scratch[32];
+    pdl_wait();
+    const int K = (int)ra.K;
+    for (int64_t t = blockIdx.x; t < ra.T; t += gridDim.x) {
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int n = 0;
+            for (int k = 0; k < K; ++k) {
+                const int32_t r = resolve_route_row(ra, t, k, route_row, assist);
+                if (r >= 0) {
+                    rows[n] = r;
+                    experts[n] = ra.ids[t * K + k];
+                    ++n;
+                }
+            }
+            nrows = n;
+        }
+        __syncthreads();
+        const int n = nrows;
+        if (n == 0) continue;
+        float f[kVec][8];
+#pragma unroll
+        for (int u = 0; u < kVec; ++u) {
+            const int64_t j = threadIdx.x + (int64_t)u * kRowThreads;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (j < H8) v = ld_stream(x + t * H8 + j);
+            unpack_bf16x8(v, f[u]);
+        }
+        for (int d = 0; d < (kSmooth ? n : 1); ++d) {
+            float v[kVec][8];
+            float amax = 0.0f;
+#pragma unroll
+            for (int u = 0; u < kVec; ++u) {
+                const int64_t j = threadIdx.x + (int64_t)u * kRowThreads;
+                if (kSmooth && j < H8) {
+                    const float4 a = __ldg(smooth + ((int64_t)experts[d] * H8 + j) * 2);
+                    const float4 b = __ldg(smooth + ((int64_t)experts[d] * H8 + j) * 2 + 1);
+                    const float sm[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) v[u][i] = __fmul_rn(f[u][i], sm[i]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) v[u][i] = f[u][i];
+                }
+                if (j < H8)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[u][i]));
+            }
+            amax = block_max(amax, scratch);
+            const float sc = __fdiv_rn(amax, 127.0f);
+            const float rs = __frcp_rn(sc);
+            uint2 packed[kVec];
+#pragma unroll
+            for (int u = 0; u < kVec; ++u) {
+                float c[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) c[i] = quant_code(v[u][i], sc, rs);
+                packed[u] = pack_i8x8(c);
+            }
+            const int d0 = kSmooth ? d : 0, d1 = kSmooth ? d + 1 : n;
+            for (int dd = d0; dd < d1; ++dd) {
+                const int64_t r = rows[dd];
+#pragma unroll
+                for (int u = 0; u < kVec; ++u) {
+                    const int64_t j = threadIdx.x + (int64_t)u * kRowThreads;
+                    if (j < H8) q[r * H8 + j] = packed[u];
+                }
+                if (threadIdx.x == 0) s_out[r] = sc;
+            }
+        }
+    }
+}
+
+// int8 rows (r < offsets[E]) -> fp16 images for the GEMM, scales copied.
+__global__ void k_rows_i8_to_f16(const int4 *__restrict__ src, const float *__restrict__ sc_in,
+                                 uint4 *__restrict__ dst, float *__restrict__ sc_out,
+                                 const int32_t *__restrict__ offsets, int64_t E, int64_t H16,
+                                 int64_t cap_rows) {
+    pdl_wait();
+    const int64_t R = min((int64_t)offsets[E], cap_rows);
+    const int64_t n = R * H16;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int4 in = src[i];
+        const int8_t *b = reinterpret_cast<const int8_t *>(&in);
+        uint32_t w[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) w[k] = pack_half2((float)b[2 * k], (float)b[2 * k + 1]);
+        dst[2 * i] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[2 * i + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+        if (i % H16 == 0) sc_out[i / H16] = sc_in[i / H16];
+    }
+}
+
 // ---------------------------------------------------------------- second quantisation
 // g fp32 [rows, Nh] -> q2 fp16 images + s2, for rows r < offsets[E].
 // One warp per row: the row's amax is a warp reduction, no block barrier, and
@@ -319,6 +433,32 @@ moe_status launch_quant_scatter(const RouteDev &r, const void *x, int32_t *route
     MOE_LAUNCH("quant_scatter", k_quant_bf16_rows<true>, grid_for(r.T, 16), kRowThreads, 0, stream,
                r, (const uint4 *)x, route_row, assist, (const int32_t *)nullptr, (int64_t)0, r.T,
                (int)r.K, (uint4 *)q1, s1, H / 8);
+    return MOE_OK;
+}
+
+moe_status launch_dispatch_quant(const RouteDev &r, const void *x, const float *smooth,
+                                 int32_t *route_row, int32_t *assist, int8_t *q, float *scales,
+                                 int64_t H, cudaStream_t stream) {
+    if (r.T == 0) return MOE_OK;
+    if (smooth) {
+        MOE_LAUNCH("dispatch_quant", k_dispatch_quant<true>, grid_for(r.T, 16), kRowThreads, 0,
+                   stream, r, (const uint4 *)x, (const float4 *)smooth, route_row, assist,
+                   (uint2 *)q, scales, H / 8);
+    } else {
+        MOE_LAUNCH("dispatch_quant", k_dispatch_quant<false>, grid_for(r.T, 16), kRowThreads, 0,
+                   stream, r, (const uint4 *)x, (const float4 *)nullptr, route_row, assist,
+                   (uint2 *)q, scales, H / 8);
+    }
+    return MOE_OK;
+}
+
+moe_status launch_rows_i8_to_f16(const int8_t *rows, const float *scales, const int32_t *offsets,
+                                 int64_t E, void *q1, float *s1, int64_t cap_rows, int64_t H,
+                                 cudaStream_t stream) {
+    if (cap_rows == 0) return MOE_OK;
+    const int64_t n16 = cap_rows * (H / 16);
+    MOE_LAUNCH("rows_i8_to_f16", k_rows_i8_to_f16, grid_for((n16 + 255) / 256, 8), 256, 0, stream,
+               (const int4 *)rows, scales, (uint4 *)q1, s1, offsets, E, H / 16, cap_rows);
     return MOE_OK;
 }
 

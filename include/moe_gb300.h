@@ -74,6 +74,10 @@ typedef enum moe_status {
  *   - N == 0 for dispatch/combine only; otherwise N % 256 == 0
  *   - mask_kind: 0 no xActiveMask, 1 per token uint8 [T], 2 per route uint8 [T, K]
  *   - has_shared: 1 if sharedExpertX is passed
+ *   - zero_experts, copy_experts >= 0 ("aclnnMoeDistributeCombineV4",
+ *     zeroExpertNum / copyExpertNum): a route to a zero expert contributes
+ *     probs * 0 and one to a copy expert probs * oriX[t] to the combine; neither
+ *     gets a row or a count.  Ids outside [0, E+Z+C) are invalid.
  *   - T * K * max(H, N) must stay below 2^31 elements per buffer row index space.
  */
 typedef struct moe_shape {
@@ -85,6 +89,8 @@ typedef struct moe_shape {
     int64_t ffn;             /* N, 0 = no expert FFN */
     int32_t mask_kind;
     int32_t has_shared;
+    int64_t zero_experts;    /* Z: ids [E, E+Z) are zero experts (output 0) */
+    int64_t copy_experts;    /* C: ids [E+Z, E+Z+C) are copy experts (output oriX) */
 } moe_shape;
 
 /* ------------------------------------------------------------------------
@@ -107,7 +113,8 @@ typedef struct moe_shape {
  *                    expert_offsets[E] = R
  * ep_recv_counts     int32 [E*P]; inclusive running sum of the per-(expert,
  *                    partition) counts, expert-major
- * route_row          int32 [T*K]; row of route (t, k), -1 if inactive
+ * route_row          int32 [T*K]; row of route (t, k); -1 if inactive,
+ *                    -2 for a zero expert, -3 for a copy expert
  * Row order: expert, then partition, then token, then slot.
  * expand_x may be NULL: only the bookkeeping is produced.
  * ------------------------------------------------------------------------ */
@@ -117,6 +124,26 @@ moe_status moe_dispatch(const moe_shape *shape, const void *x, const int32_t *ex
                         int64_t *expert_token_nums, int32_t *expert_offsets,
                         int32_t *ep_recv_counts, int32_t *route_row,
                         void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Quantised dispatch: the dispatch above with int8 rows and one dynamic
+ * scale per row ("aclnnMoeDistributeCombineV4", Example: the paired dispatch
+ * call with a quantisation mode takes smooth scales [experts, H] and returns
+ * int8 expandX and dynamicScales [A]).  Row r of token t routed to expert e
+ * holds q = clamp(rint(v / s), -127, 127) with v = float(x[t]) * smooth[e]
+ * (or float(x[t]) when smooth_scales is NULL) and s = max|v| / 127, both in
+ * fp32 with IEEE rounding; dynamic_scales[r] = s.
+ * smooth_scales   fp32 [E, H] or NULL
+ * expand_x        int8 [T*K, H]; dynamic_scales fp32 [T*K]; rows >= R untouched
+ * Other arguments and the workspace (moe_dispatch_workspace_size) as in
+ * moe_dispatch.  H <= 8192.
+ * ------------------------------------------------------------------------ */
+moe_status moe_dispatch_quant(const moe_shape *shape, const void *x, const int32_t *expert_ids,
+                              const uint8_t *x_active_mask, const float *smooth_scales,
+                              int8_t *expand_x, float *dynamic_scales, int32_t *assist,
+                              int64_t *expert_token_nums, int32_t *expert_offsets,
+                              int32_t *ep_recv_counts, int32_t *route_row, void *workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
  * Combine.
@@ -129,10 +156,13 @@ moe_status moe_dispatch(const moe_shape *shape, const void *x, const int32_t *ex
  *
  * No workspace is needed.
  * expand_x        bf16 [T*K, H] rows of the expert outputs (dispatch order)
- * route_row       int32 [T*K] from moe_dispatch (-1 = inactive)
+ * route_row       int32 [T*K] from moe_dispatch (-1 inactive, -2 zero expert,
+ *                 -3 copy expert)
  * expert_scales   fp32 [T, K]
  * x_active_mask   same mask as given to moe_dispatch, or NULL
  * shared_expert_x bf16 [T, H] or NULL (shape->has_shared must match)
+ * ori_x           bf16 [T, H], the tokens before the FFN (oriXOptional);
+ *                 required when shape->copy_experts > 0, else may be NULL
  * x_out           bf16 [T, H]; a token with no active route gets
  *                 bf16(shared) or +0
  * The multiply and add are separately rounded fp32 operations in slot order,
@@ -140,7 +170,8 @@ moe_status moe_dispatch(const moe_shape *shape, const void *x, const int32_t *ex
  * ------------------------------------------------------------------------ */
 moe_status moe_combine(const moe_shape *shape, const void *expand_x, const int32_t *route_row,
                        const float *expert_scales, const uint8_t *x_active_mask,
-                       const void *shared_expert_x, void *x_out, cudaStream_t stream);
+                       const void *shared_expert_x, const void *ori_x, void *x_out,
+                       cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
  * Expert weights.  "PTO MegaMoE ...", Specification: "per-local-expert int8
@@ -179,6 +210,15 @@ moe_status moe_grouped_ffn(const moe_shape *shape, const void *expand_x,
                            const void *w1_packed, const float *scale1,
                            const void *w2_packed, const float *scale2, void *y,
                            void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* The grouped FFN on rows that are already int8 (moe_dispatch_quant's
+ * expand_x and dynamic_scales): the same stages as moe_grouped_ffn from the
+ * GMM1 on; workspace from moe_grouped_ffn_workspace_size. */
+moe_status moe_grouped_ffn_q(const moe_shape *shape, const int8_t *expand_x,
+                             const float *dynamic_scales, const int32_t *expert_offsets,
+                             const void *w1_packed, const float *scale1, const void *w2_packed,
+                             const float *scale2, void *y, void *workspace,
+                             size_t workspace_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
  * The whole layer in one call ("PTO MegaMoE ...", Functionality:

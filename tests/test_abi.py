@@ -62,7 +62,7 @@ def test_null_pointers_rejected_before_launch(B):
     rc = L.moe_dispatch(ctypes.byref(s), None, None, None, None, None, None, None, None, None,
                         None, 0, None)
     assert rc == 161001
-    rc = L.moe_combine(ctypes.byref(s), None, None, None, None, None, None, None)
+    rc = L.moe_combine(ctypes.byref(s), None, None, None, None, None, None, None, None)
     assert rc == 161001
     rc = L.moe_read_device_status(None, None, None)
     assert rc == 161001

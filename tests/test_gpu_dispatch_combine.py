@@ -130,3 +130,37 @@ def test_full_size_workloads(B, name):
         counts = r["counts"]
         assert (counts == 0).sum() >= 10
         assert counts.max() / w.num_tokens > 0.15      # hottest expert serves > 15% of tokens
+
+
+@pytest.mark.parametrize("Z,C,mask_kind", [(3, 0, 0), (0, 2, 1), (2, 3, 2)])
+def test_special_experts_dispatch_combine(B, Z, C, mask_kind):
+    """Zero experts (ids [E, E+Z)) contribute probs*0 and copy experts (ids
+    [E+Z, E+Z+C)) probs*oriX[t]; neither gets a row ("aclnnMoeDistributeCombineV4",
+    zeroExpertNum / copyExpertNum / oriXOptional).  Bit-exact against the oracle."""
+    T, P, H, E, K = 192, 3, 264, 12, 6
+    g = np.random.default_rng(Z * 10 + C)
+    ids = wl.uniform_ids(21 + Z, T, E + Z + C, K)
+    x = wl.normal_bf16(22, "x", (T, H))
+    sh = wl.normal_bf16(23, "shared", (T, H))
+    probs = wl.softmax_probs(24, T, K)
+    mask = None
+    if mask_kind == 1:
+        mask = (g.random(T) < 0.8).astype(np.uint8)
+    elif mask_kind == 2:
+        mask = (g.random((T, K)) < 0.8).astype(np.uint8)
+    d = B.dispatch(dev_bf16(x), dev(ids), E, P, mask=dev(mask), zero_experts=Z, copy_experts=C)
+    out = B.combine(d["expand_x"], d["route_row"], dev(probs), E, P, mask=dev(mask),
+                    shared=dev_bf16(sh), ori_x=dev_bf16(x), zero_experts=Z, copy_experts=C)
+    torch.cuda.synchronize()
+    assert B.read_device_status(d["workspace"]) == 0
+    r = oracle.route(ids, E, P, mask, zero_experts=Z, copy_experts=C)
+    R = r["R"]
+    np.testing.assert_array_equal(d["route_row"].cpu().numpy(), r["route_row"])
+    np.testing.assert_array_equal(d["expert_token_nums"].cpu().numpy(), r["counts"])
+    np.testing.assert_array_equal(d["expert_offsets"].cpu().numpy(), r["offsets"])
+    np.testing.assert_array_equal(d["ep_recv_counts"].cpu().numpy(), r["recv_cum"])
+    np.testing.assert_array_equal(d["assist"][:R].cpu().numpy(), r["assist"])
+    ex = host_bits(d["expand_x"][:R])
+    np.testing.assert_array_equal(ex, x[r["row_token"]])
+    ref = oracle.combine(ex, r["route_row"], probs, sh, ori_x=x)
+    np.testing.assert_array_equal(host_bits(out), ref)

@@ -237,3 +237,25 @@ def test_quantisation_codes_exact_on_ties_and_many_scales(B):
         q, s = oracle.quant_row(wl.bf16_bits_to_f32(X[i]))
         assert s1[i] == np.float32(s), i
         np.testing.assert_array_equal(q1[i], q, err_msg=f"row {i}")
+
+
+def test_layer_with_zero_and_copy_experts(B):
+    """moe_layer with zero and copy experts: copy experts add probs * x[t]
+    (x is the layer's unprocessed input), zero experts add probs * 0."""
+    T, P, H, E, K, N, Z, C = 96, 2, 256, 8, 4, 256, 2, 2
+    w = wl.custom(P=P, M=T // P, H=H, E=E, K=K, N=N, has_shared=True)
+    inp = wl.make_inputs(w, seed=9)
+    ids = wl.uniform_ids(9, T, E + Z + C, K)
+    W1, S1, W2, S2 = wl.all_expert_weights(w, seed=9)
+    shape = B.make_shape(T, P, H, E, K, N, 0, True, Z, C)
+    (o1, w1p), (o2, w2p) = B.pack_weights(shape, dev(W1), dev(W2))
+    out, ws = B.layer(shape, dev_bf16(inp["x"]), dev(ids), dev(inp["probs"]), w1p, dev(S1), w2p,
+                      dev(S2), shared=dev_bf16(inp["shared"]))
+    torch.cuda.synchronize()
+    assert B.read_device_status(ws) == 0
+    ref, ovf = oracle.layer_tokens(inp["x"], ids, inp["probs"], W1, S1, W2, S2, np.arange(T),
+                                   shared=inp["shared"], zero_experts=Z, copy_experts=C)
+    ulp, rel = output_errors(host_bits(out), ref)
+    assert ulp <= 2.0 and rel <= 1e-3, (ulp, rel)
+    r = oracle.route(ids, E, P, zero_experts=Z, copy_experts=C)
+    np.testing.assert_array_equal(B.stage_views(shape, ws)["route_row"].cpu().numpy(), r["route_row"])
