@@ -128,12 +128,13 @@ moe_status moe_dispatch(const moe_shape *shape, const void *x, const int32_t *ex
 /* ------------------------------------------------------------------------
  * Quantised dispatch: the dispatch above with int8 rows and one dynamic
  * scale per row ("aclnnMoeDistributeCombineV4", Example: the paired dispatch
- * call with a quantisation mode takes smooth scales [experts, H] and returns
+ * call with a quantisation mode takes smooth scales [experts + 1, H] and returns
  * int8 expandX and dynamicScales [A]).  Row r of token t routed to expert e
  * holds q = clamp(rint(v / s), -127, 127) with v = float(x[t]) * smooth[e]
  * (or float(x[t]) when smooth_scales is NULL) and s = max|v| / 127, both in
  * fp32 with IEEE rounding; dynamic_scales[r] = s.
- * smooth_scales   fp32 [E, H] or NULL
+ * smooth_scales   fp32 [E, H] or NULL (rows past E, such as the shared
+ *                 expert's row of an [E+1, H] array, are not read)
  * expand_x        int8 [T*K, H]; dynamic_scales fp32 [T*K]; rows >= R untouched
  * Other arguments and the workspace (moe_dispatch_workspace_size) as in
  * moe_dispatch.  H <= 8192.
