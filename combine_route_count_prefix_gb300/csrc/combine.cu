@@ -140,9 +140,12 @@ k_combine(CombineArgs a) {
     __syncthreads();
     pdl_wait();
 
-    // this CTA's tokens: blockIdx.x + G * i for i in [0, ntok)
+    // this CTA's tokens: T - 1 - (blockIdx.x + G * i) for i in [0, ntok).  Tokens are
+    // taken from the last one down: the row copy writes rows in token order, so when
+    // combine follows it the last tokens' rows are the ones most likely still in L2.
     const int64_t G = gridDim.x;
     const int64_t ntok = (a.T - blockIdx.x + G - 1) / G;
+    auto token_of = [&](int64_t i) -> int64_t { return a.T - 1 - (blockIdx.x + G * i); };
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -157,7 +160,7 @@ k_combine(CombineArgs a) {
         // metadata of the batch starting at tb, for token tb + lane, into registers
         auto load_meta = [&](int64_t ib) {
             const bool in = ib + lane < ntok;
-            const int64_t t = blockIdx.x + G * (ib + lane);
+            const int64_t t = token_of(ib + lane);
             const bool tok = in && (a.mask_kind != 1 || a.mask[t] != 0);
 #pragma unroll
             for (int k = 0; k < kMaxTopK; ++k) {
@@ -200,7 +203,7 @@ k_combine(CombineArgs a) {
             if (lane == 0 && ok) {
                 const int64_t ie = min(ib + 32, ntok);
                 for (int64_t ii = ib; ok && ii < ie; ++ii) {
-                    const int64_t tt = blockIdx.x + G * ii;
+                    const int64_t tt = token_of(ii);
                     const int32_t *rows = meta_row + buf * 32 * a.K + (ii - ib) * a.K;
                     const float *ps = meta_p + buf * 32 * a.K + (ii - ib) * a.K;
                     for (int seg = 0; seg < a.nseg; ++seg) {
@@ -270,7 +273,7 @@ k_combine(CombineArgs a) {
         uint32_t phase = 0;
         bool ok = true;
         for (int64_t ii = 0; ok && ii < ntok; ++ii) {
-            const int64_t tt = blockIdx.x + G * ii;
+            const int64_t tt = token_of(ii);
             for (int seg = 0; seg < a.nseg; ++seg) {
                 const bool w = wait_bounded(&full[stage], phase, abort_flag, a.status);
                 if (!__all_sync(kFull, w)) { ok = false; break; }

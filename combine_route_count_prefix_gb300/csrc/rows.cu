@@ -76,18 +76,46 @@ k_dispatch_rows(RouteDev ra, const uint4 *__restrict__ x, int32_t *__restrict__ 
     __shared__ int32_t rows[kMaxTopK];
     const int64_t T = ra.T;
     const int K = (int)ra.K;
+    uint4 v[kVec];
+    auto load_row = [&](int64_t t, int64_t j0) {
+#pragma unroll
+        for (int u = 0; u < kVec; ++u) {
+            int64_t j = j0 + (int64_t)u * kRowThreads;
+            if (j < H8) v[u] = ld_stream(x + t * H8 + j);
+        }
+    };
+    // The first token's row is loaded before waiting on the routing kernel, so that the
+    // read of x overlaps it.  x is not written by anything this grid can overlap: the
+    // routing kernel triggers its dependents only after its own wait has returned, i.e.
+    // after every earlier kernel of the stream has finished.
+    // The mask is an input too, so a token it switches off entirely is not loaded.
+    bool preloaded = false;
+    if ((int64_t)blockIdx.x < T && H8 <= (int64_t)kRowThreads * kVec) {
+        const int64_t t = blockIdx.x;
+        bool on = ra.mask_kind != 1 || ra.mask[t] != 0;
+        if (ra.mask_kind == 2) {
+            on = false;
+            for (int k = 0; k < K; ++k) on = on || ra.mask[t * K + k] != 0;
+        }
+        if (on) {
+            load_row(t, threadIdx.x);
+            preloaded = true;
+        }
+    }
     pdl_wait();
     for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
         __syncthreads();
         if (threadIdx.x < K) rows[threadIdx.x] = resolve_route_row(ra, t, threadIdx.x, route_row, assist);
         __syncthreads();
+        bool any = false;
+        for (int k = 0; k < K; ++k) any = any || rows[k] >= 0;
+        if (!any) {
+            preloaded = false;
+            continue;
+        }
         for (int64_t j0 = threadIdx.x; j0 < H8; j0 += (int64_t)kRowThreads * kVec) {
-            uint4 v[kVec];
-#pragma unroll
-            for (int u = 0; u < kVec; ++u) {
-                int64_t j = j0 + (int64_t)u * kRowThreads;
-                if (j < H8) v[u] = ld_stream(x + t * H8 + j);
-            }
+            if (!preloaded) load_row(t, j0);
+            preloaded = false;
             for (int k = 0; k < K; ++k) {
                 int32_t r = rows[k];
                 if (r < 0) continue;
