@@ -66,6 +66,9 @@ def parse():
     ap.add_argument("--soak", type=float, default=2.0,
                     help="seconds of untimed steps before the timed region (clock samples)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ffn-path", default="auto", choices=["auto", "large", "small"],
+                    help="grouped-GEMM kernels of the layer workloads (auto: small-batch "
+                         "kernels when T*K <= 64*E)")
     return ap.parse_args()
 
 
@@ -374,7 +377,7 @@ class LayerPath:
     """moe_layer: routing, per-token int8 quantisation, grouped GEMM1 + SwiGLU,
     second quantisation, grouped GEMM2 + dequant, combine."""
 
-    def __init__(self, B, w, inp, dev, seed):
+    def __init__(self, B, w, inp, dev, seed, ffn_path="auto"):
         import torch
         self.B, self.w, self.inp = B, w, inp
         T, P, H, E, K, N = (w.num_tokens, w.num_partitions, w.hidden, w.num_experts, w.topk,
@@ -384,7 +387,7 @@ class LayerPath:
         self.probs = torch.from_numpy(inp["probs"]).to(dev)
         self.mask = None if inp["mask"] is None else torch.from_numpy(inp["mask"]).to(dev)
         self.shared = bf16_dev(inp["shared"], dev)
-        self.shape = B.make_shape(T, P, H, E, K, N, w.mask_kind, w.has_shared)
+        self.shape = B.make_shape(T, P, H, E, K, N, w.mask_kind, w.has_shared, ffn_path=ffn_path)
         w1, self.s1, w2, self.s2 = device_weights(w, dev, seed)
         (self.o1, self.w1p), (self.o2, self.w2p) = B.pack_weights(self.shape, w1, w2)
         del w1, w2
@@ -404,17 +407,34 @@ class LayerPath:
     def roofline(self, prof, pk):
         w = self.w
         R = self.rows()
-        fl = {"gemm1_swiglu": 2.0 * R * w.hidden * w.ffn,
-              "gemm2_dequant": 2.0 * R * (w.ffn // 2) * w.hidden}
+        H, N, Nh = w.hidden, w.ffn, w.ffn // 2
+        small = "gemm1_swiglu_small" in prof
+        sfx = "_small" if small else ""
+        g1, g2 = "gemm1_swiglu" + sfx, "gemm2_dequant" + sfx
+        fl = {g1: 2.0 * R * H * N, g2: 2.0 * R * Nh * H}
         dom = max(fl, key=lambda k: prof.get(k, (1, 0.0))[1])
         n, ms = prof[dom]
         us = ms / n * 1e3
-        achieved = fl[dom] / (us * 1e-6) / 1e12
-        other = [k for k in fl if k != dom][0]
-        n2, ms2 = prof[other]
-        extra = {"gemm_tflops": {k: fl[k] / (prof[k][1] / prof[k][0] * 1e-3) / 1e12 for k in fl},
+        extra = {"ffn_path": "small" if small else "large",
+                 "gemm_tflops": {k: fl[k] / (prof[k][1] / prof[k][0] * 1e-3) / 1e12 for k in fl},
                  "status": self.B.read_device_status(self.ws)}
         step_bytes = None
+        if small:
+            # few rows per expert: reading the int8 weights of every expert that
+            # has rows bounds the time.  Algorithmic bytes per launch: those
+            # weights, the int8 operand rows, and the stage's output.
+            counts = self.B.stage_views(self.shape, self.ws)["expert_token_nums"].cpu().numpy()
+            e_act = int((counts > 0).sum())
+            by = {g1: e_act * N * H + R * H + R * Nh * 4, g2: e_act * H * Nh + R * Nh + R * H * 2}
+            extra["gemm_hbm_gbs"] = {k: by[k] / (prof[k][1] / prof[k][0] * 1e-3) / 1e9 for k in by}
+            achieved = by[dom] / (us * 1e-6) / 1e9
+            return dict(bound="hbm", kernel=dom, achieved=achieved, peak=pk["hbm_gbs"], unit="GB/s",
+                        frac=achieved / pk["hbm_gbs"], traffic=recorded_traffic(dom, w.name),
+                        algorithmic_bytes=by[dom],
+                        algorithmic_unit="int8 weights of the experts with rows + int8 rows + "
+                        "stage output (g fp32 / y bf16) bytes per launch",
+                        peak_source=pk["source"] + " hbm_gbs"), step_bytes, extra
+        achieved = fl[dom] / (us * 1e-6) / 1e12
         return dict(bound="tensor", kernel=dom, achieved=achieved,
                     peak=pk["bf16_tflops_sustained"], unit="TFLOP/s",
                     frac=achieved / pk["bf16_tflops_sustained"],
@@ -426,6 +446,37 @@ class LayerPath:
 
     def dtype(self):
         return "int8 GEMMs (exact, on fp16 images), fp32 epilogues, bf16 rows"
+
+
+def run_layer_secondary(args, B, dev, stream, flush, pk):
+    """The full layer workload (16384 tokens, 128 experts, FFN 4096) as a
+    secondary line item: tokens/s and the grouped GEMMs' roofline."""
+    import torch
+    w = wl.WORKLOADS["full_layer"]
+    inp = wl.make_inputs(w, seed=args.seed)
+    path = LayerPath(B, w, inp, dev, args.seed, args.ffn_path)
+    for _ in range(3):
+        path.step()
+    steps = max(3, min(args.steps, 10))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.fill_(1)
+        ev[i][0].record(stream)
+        path.step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    B.profile_enable(True)
+    for i in range(steps):
+        flush.fill_(1)
+        path.step()
+    torch.cuda.synchronize()
+    B.profile_enable(False)
+    roofline, _, extra = path.roofline(B.profile_report(), pk)
+    return {"workload": w.name, "value": whole_job_tokens_per_s(w.num_tokens, 1, ms),
+            "unit": "tokens/s", "ms_per_step": ms, "steps": steps, "roofline": roofline, **extra}
 
 
 def run_ours(args, rank, world, dist):
@@ -440,7 +491,8 @@ def run_ours(args, rank, world, dist):
     w = select_workload(args)
     T, H = w.num_tokens, w.hidden
     inp = wl.make_inputs(w, seed=args.seed + rank)
-    path = IdentityPath(B, w, inp, dev) if w.identity else LayerPath(B, w, inp, dev, args.seed + rank)
+    path = (IdentityPath(B, w, inp, dev) if w.identity
+            else LayerPath(B, w, inp, dev, args.seed + rank, args.ffn_path))
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def barrier():

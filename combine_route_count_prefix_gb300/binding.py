@@ -50,7 +50,13 @@ class MoeShape(ctypes.Structure):
                 ("hidden", ctypes.c_int64), ("num_experts", ctypes.c_int64),
                 ("topk", ctypes.c_int64), ("ffn", ctypes.c_int64),
                 ("mask_kind", ctypes.c_int32), ("has_shared", ctypes.c_int32),
-                ("zero_experts", ctypes.c_int64), ("copy_experts", ctypes.c_int64)]
+                ("zero_experts", ctypes.c_int64), ("copy_experts", ctypes.c_int64),
+                ("ffn_path", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+# moe_shape.ffn_path: which grouped-GEMM kernels the FFN uses (same results)
+FFN_PATH_AUTO, FFN_PATH_LARGE, FFN_PATH_SMALL = 0, 1, 2
+FFN_PATHS = {"auto": FFN_PATH_AUTO, "large": FFN_PATH_LARGE, "small": FFN_PATH_SMALL}
 
 
 class StageViews(ctypes.Structure):
@@ -85,7 +91,7 @@ def lib():
         "moe_layer": [SP, P, P, P, P, P, P, P, P, P, P, P, SZ, P],
         "moe_stage_views_get": [SP, ctypes.c_int, P, SZ, ctypes.POINTER(StageViews)],
         "moe_grouped_gemm_s32_workspace_size": [I64, I64, I64, I64, ctypes.POINTER(SZ)],
-        "moe_grouped_gemm_s32": [I64, I64, I64, I64, P, P, P, P, P, SZ, P],
+        "moe_grouped_gemm_s32": [I64, I64, I64, I64, P, P, P, P, ctypes.c_int, P, SZ, P],
         "moe_read_device_status": [P, P, ctypes.POINTER(ctypes.c_int32)],
         "moe_profile_enable": [ctypes.c_int],
         "moe_profile_report": [ctypes.c_char_p, SZ],
@@ -136,9 +142,10 @@ def _check(t, dtype, shape, name):
 
 
 def make_shape(T, P, H, E, K, N=0, mask_kind=0, has_shared=False, zero_experts=0,
-               copy_experts=0) -> MoeShape:
+               copy_experts=0, ffn_path="auto") -> MoeShape:
     return MoeShape(int(T), int(P), int(H), int(E), int(K), int(N), int(mask_kind),
-                    int(bool(has_shared)), int(zero_experts), int(copy_experts))
+                    int(bool(has_shared)), int(zero_experts), int(copy_experts),
+                    FFN_PATHS[ffn_path], 0)
 
 
 def mask_kind_of(mask, T, K):
@@ -401,8 +408,9 @@ def stage_views(shape: MoeShape, ws, for_layer=True) -> dict:
         s2=view(v.s2, torch.float32, (cap,)), y=view(v.y, torch.bfloat16, (cap, H)))
 
 
-def grouped_gemm_s32(expert_offsets, A, W, ws=None, C=None, stream=None):
-    """C[r] = A[r] @ W[e]^T (int8 x int8 -> int32) for rows of expert e."""
+def grouped_gemm_s32(expert_offsets, A, W, ws=None, C=None, stream=None, path="auto"):
+    """C[r] = A[r] @ W[e]^T (int8 x int8 -> int32) for rows of expert e.
+    path: "auto", "large" or "small" (moe_shape.ffn_path's kernels)."""
     rows, Kd = A.shape
     E, N, _ = W.shape
     _check(A, torch.int8, (rows, Kd), "A")
@@ -415,7 +423,7 @@ def grouped_gemm_s32(expert_offsets, A, W, ws=None, C=None, stream=None):
     if C is None:
         C = torch.empty((rows, N), dtype=torch.int32, device=A.device)
     _call("moe_grouped_gemm_s32", rows, E, N, Kd, _ptr(expert_offsets), _ptr(A), _ptr(W), _ptr(C),
-          _ptr(ws), ctypes.c_size_t(ws.numel()), _stream(stream))
+          FFN_PATHS[path], _ptr(ws), ctypes.c_size_t(ws.numel()), _stream(stream))
     return C, ws
 
 

@@ -87,6 +87,8 @@ moe_status check_shape(const moe_shape *s, bool need_ffn) {
         s->num_experts + s->zero_experts + s->copy_experts > INT32_MAX)
         return MOE_ERR_SHAPE;
     if (s->has_shared != 0 && s->has_shared != 1) return MOE_ERR_PARAM_INVALID;
+    if (s->ffn_path < MOE_FFN_PATH_AUTO || s->ffn_path > MOE_FFN_PATH_SMALL || s->reserved != 0)
+        return MOE_ERR_PARAM_INVALID;
     const int64_t cap = s->num_tokens * s->topk;
     if (cap > INT32_MAX) return MOE_ERR_SHAPE;
     if (need_ffn) {
@@ -331,9 +333,21 @@ moe_status moe_packed_weight_bytes(const moe_shape *shape, size_t *w1_bytes, siz
     MOE_TRY(check_shape(shape, true));
     if (!w1_bytes || !w2_bytes) return MOE_ERR_NULLPTR;
     const moe_shape &s = *shape;
-    *w1_bytes = (size_t)s.num_experts * s.ffn * s.hidden * 2;
-    *w2_bytes = (size_t)s.num_experts * s.hidden * (s.ffn / 2) * 2;
+    *w1_bytes = (size_t)s.num_experts * s.ffn * s.hidden * 3;
+    *w2_bytes = (size_t)s.num_experts * s.hidden * (s.ffn / 2) * 3;
     return MOE_OK;
+}
+
+// The int8 part of a packed buffer follows the fp16 images (E*rows*cols*2 bytes,
+// a multiple of 1024 because N % 256 == 0 and H % 16 == 0).
+static const void *packed_i8(const void *packed, int64_t E, int64_t rows, int64_t cols) {
+    return static_cast<const uint8_t *>(packed) + (size_t)E * rows * cols * 2;
+}
+
+static bool use_small_path(int32_t path, int64_t rows, int64_t E) {
+    if (path == MOE_FFN_PATH_SMALL) return true;
+    if (path == MOE_FFN_PATH_LARGE) return false;
+    return rows <= (int64_t)MOE_FFN_SMALL_ROWS_PER_EXPERT * E;
 }
 
 moe_status moe_pack_weights(const moe_shape *shape, const int8_t *w1, const int8_t *w2,
@@ -344,8 +358,13 @@ moe_status moe_pack_weights(const moe_shape *shape, const int8_t *w1, const int8
     if (!aligned(w1, 16) || !aligned(w2, 16) || !aligned(w1_packed, kAlign) ||
         !aligned(w2_packed, kAlign))
         return MOE_ERR_ALIGNMENT;
-    MOE_TRY(launch_pack_w1(w1, w1_packed, s.num_experts, s.ffn, s.hidden, stream));
-    MOE_TRY(launch_i8_to_f16(w2, w2_packed, s.num_experts * s.hidden * (s.ffn / 2), stream));
+    const int64_t E = s.num_experts, N = s.ffn, H = s.hidden, Nh = s.ffn / 2;
+    MOE_TRY(launch_pack_w1(w1, w1_packed, E, N, H, stream));
+    MOE_TRY(launch_i8_to_f16(w2, w2_packed, E * H * Nh, stream));
+    MOE_TRY(launch_pack_w1_i8(w1, const_cast<void *>(packed_i8(w1_packed, E, N, H)), E, N, H, stream));
+    if (cudaMemcpyAsync(const_cast<void *>(packed_i8(w2_packed, E, H, Nh)), w2, (size_t)E * H * Nh,
+                        cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
     return MOE_OK;
 }
 
@@ -356,10 +375,12 @@ static moe_status run_ffn_core(const moe_shape &s, const Layout &L, void *ws,
                                cudaStream_t stream) {
     const int64_t cap = s.num_tokens * s.topk, Nh = s.ffn / 2;
     int32_t *status = at<int32_t>(ws, L.status);
+    const bool small = use_small_path(s.ffn_path, cap, s.num_experts);
+    auto gemm = small ? launch_grouped_gemm_small : launch_grouped_gemm;
     GemmArgs g1{};
     g1.a_img = at<void>(ws, L.q1);
     g1.cap_rows = cap;
-    g1.b_img = w1p;
+    g1.b_img = small ? packed_i8(w1p, s.num_experts, s.ffn, s.hidden) : w1p;
     g1.E = s.num_experts;
     g1.Nout = s.ffn;
     g1.Kd = s.hidden;
@@ -369,13 +390,13 @@ static moe_status run_ffn_core(const moe_shape &s, const Layout &L, void *ws,
     g1.scale1 = scale1;
     g1.s1 = at<float>(ws, L.s1);
     g1.status = status;
-    MOE_TRY(launch_grouped_gemm(Epi::SwiGLU, g1, stream));
+    MOE_TRY(gemm(Epi::SwiGLU, g1, stream));
     MOE_TRY(launch_quant2(at<float>(ws, L.g), offsets, s.num_experts, at<void>(ws, L.q2),
                           at<float>(ws, L.s2), cap, Nh, stream));
     GemmArgs g2{};
     g2.a_img = at<void>(ws, L.q2);
     g2.cap_rows = cap;
-    g2.b_img = w2p;
+    g2.b_img = small ? packed_i8(w2p, s.num_experts, s.hidden, Nh) : w2p;
     g2.E = s.num_experts;
     g2.Nout = s.hidden;
     g2.Kd = Nh;
@@ -385,7 +406,7 @@ static moe_status run_ffn_core(const moe_shape &s, const Layout &L, void *ws,
     g2.scale2 = scale2;
     g2.s2 = at<float>(ws, L.s2);
     g2.status = status;
-    return launch_grouped_gemm(Epi::DequantBF16, g2, stream);
+    return gemm(Epi::DequantBF16, g2, stream);
 }
 
 moe_status moe_grouped_ffn_workspace_size(const moe_shape *shape, size_t *bytes) {
@@ -546,7 +567,7 @@ moe_status moe_grouped_gemm_s32_workspace_size(int64_t rows, int64_t E, int64_t 
 
 moe_status moe_grouped_gemm_s32(int64_t rows, int64_t E, int64_t N, int64_t Kd,
                                 const int32_t *expert_offsets, const int8_t *A, const int8_t *W,
-                                int32_t *C, void *workspace, size_t workspace_bytes,
+                                int32_t *C, int path, void *workspace, size_t workspace_bytes,
                                 cudaStream_t stream) {
     size_t need = 0;
     MOE_TRY(moe_grouped_gemm_s32_workspace_size(rows, E, N, Kd, &need));
@@ -554,16 +575,19 @@ moe_status moe_grouped_gemm_s32(int64_t rows, int64_t E, int64_t N, int64_t Kd,
     if (!aligned(A, 16) || !aligned(W, 16) || !aligned(C, 16) || !aligned(workspace, kAlign))
         return MOE_ERR_ALIGNMENT;
     if (workspace_bytes < need) return MOE_ERR_WORKSPACE;
+    if (path < MOE_FFN_PATH_AUTO || path > MOE_FFN_PATH_SMALL) return MOE_ERR_PARAM_INVALID;
+    if (path == MOE_FFN_PATH_SMALL && Kd % 16 != 0) return MOE_ERR_SHAPE;
+    const bool small = Kd % 16 == 0 && use_small_path(path, rows, E);
     if (rows == 0) return MOE_OK;
     const Layout L = gemm_layout(rows, E, N, Kd);
     MOE_TRY(launch_sched(expert_offsets, E, at<int32_t>(workspace, L.sched),
                          at<int32_t>(workspace, L.status), stream));
     MOE_TRY(launch_i8_to_f16(A, at<void>(workspace, L.a_img), rows * Kd, stream));
-    MOE_TRY(launch_i8_to_f16(W, at<void>(workspace, L.w_img), E * N * Kd, stream));
+    if (!small) MOE_TRY(launch_i8_to_f16(W, at<void>(workspace, L.w_img), E * N * Kd, stream));
     GemmArgs g{};
     g.a_img = at<void>(workspace, L.a_img);
     g.cap_rows = rows;
-    g.b_img = at<void>(workspace, L.w_img);
+    g.b_img = small ? static_cast<const void *>(W) : at<void>(workspace, L.w_img);
     g.E = E;
     g.Nout = N;
     g.Kd = Kd;
@@ -571,7 +595,8 @@ moe_status moe_grouped_gemm_s32(int64_t rows, int64_t E, int64_t N, int64_t Kd,
     g.sched = at<int32_t>(workspace, L.sched);
     g.c_s32 = C;
     g.status = at<int32_t>(workspace, L.status);
-    return launch_grouped_gemm(Epi::S32, g, stream);
+    return small ? launch_grouped_gemm_small(Epi::S32, g, stream)
+                 : launch_grouped_gemm(Epi::S32, g, stream);
 }
 
 }  // extern "C"

@@ -32,13 +32,15 @@
 // Every wait is bounded: after about two seconds a wait gives up, sets
 // MOE_DEV_TIMEOUT in the status word and the CTA drains and exits.
 #include "common.cuh"
-#include "ptx.cuh"
+#include "tcgen05.cuh"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
 namespace moe {
 namespace {
+
+using namespace tc;
 
 constexpr int BM = kGemmBM;          // 128
 constexpr int BN = kGemmBN;          // 256
@@ -73,94 +75,6 @@ struct GemmDev {
     int32_t *status;
 };
 
-// ---------------------------------------------------------------- PTX wrappers
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
-                                            int x, int y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-        "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y)
-        : "memory");
-}
-__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
-                                            int x, int y, int z) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
-        "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
-        : "memory");
-}
-__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(slot)),
-                 "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.u32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-__device__ __forceinline__ void mma_commit(uint64_t *bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_u32(bar))
-        : "memory");
-}
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31])
-        : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_ld_wait() {
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
-// 128 bytes, 8-row groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);        // start address
-    d |= (uint64_t)1 << 16;                          // leading byte offset (unused here)
-    d |= (uint64_t)(1024 >> 4) << 32;                // stride byte offset: 8 rows x 128 B
-    d |= (uint64_t)1 << 46;                          // descriptor version
-    d |= (uint64_t)2 << 61;                          // swizzle: 128 B
-    return d;
-}
-
-// Instruction descriptor: fp16 A and B (K-major), fp32 accumulator, M x N.
-__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
-    return (1u << 4)                        // D format: f32
-           | (0u << 7) | (0u << 10)         // A, B format: f16
-           | ((uint32_t)(N >> 3) << 17)     // N
-           | ((uint32_t)(M >> 4) << 24);    // M
-}
-
 struct Tile {
     int e, row0, rows, nb;
 };
@@ -181,9 +95,6 @@ __device__ __forceinline__ Tile decode_tile(int64_t tile, int n_blocks, int E, c
     return t;
 }
 
-__device__ __forceinline__ float silu_f32(float v) {
-    return __fdiv_rn(v, __fadd_rn(1.0f, expf(-v)));
-}
 
 // ---------------------------------------------------------------- epilogues
 // acc[i] is the exact int32 sum for row `row` and tile column hf*128 + i.
@@ -410,33 +321,6 @@ k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 }
 
 // ---------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
-    return fn;
-}
-
-bool make_map(CUtensorMap *m, const void *base, int rank, const uint64_t *dims,
-              const uint64_t *strides_bytes, const uint32_t *box) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t d[3], s[2];
-    cuuint32_t b[3], es[3] = {1, 1, 1};
-    for (int i = 0; i < rank; ++i) { d[i] = dims[i]; b[i] = box[i]; }
-    for (int i = 0; i < rank - 1; ++i) s[i] = strides_bytes[i];
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (cuuint32_t)rank, const_cast<void *>(base), d, s,
-                    b, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 template <int EPI>
 moe_status launch_epi(const CUtensorMap &ma, const CUtensorMap &mb, const GemmDev &d,
                       cudaStream_t stream) {
@@ -454,6 +338,29 @@ moe_status launch_epi(const CUtensorMap &ma, const CUtensorMap &mb, const GemmDe
 
 }  // namespace
 
+bool make_tensor_map(CUtensorMap *m, CUtensorMapDataType dtype, CUtensorMapSwizzle swizzle,
+                     const void *base, int rank, const uint64_t *dims,
+                     const uint64_t *strides_bytes, const uint32_t *box) {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    if (!fn) return false;
+    cuuint64_t d[3], s[2];
+    cuuint32_t b[3], es[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) { d[i] = dims[i]; b[i] = box[i]; }
+    for (int i = 0; i < rank - 1; ++i) s[i] = strides_bytes[i];
+    CUresult r = fn(m, dtype, (cuuint32_t)rank, const_cast<void *>(base), d, s, b, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 moe_status launch_grouped_gemm(Epi epi, const GemmArgs &a, cudaStream_t stream) {
     if (a.cap_rows <= 0 || a.E <= 0) return MOE_OK;
     CUtensorMap ma, mb;
@@ -463,8 +370,12 @@ moe_status launch_grouped_gemm(Epi epi, const GemmArgs &a, cudaStream_t stream) 
     const uint64_t bdims[3] = {(uint64_t)a.Kd, (uint64_t)a.Nout, (uint64_t)a.E};
     const uint64_t bstr[2] = {(uint64_t)a.Kd * 2, (uint64_t)a.Kd * a.Nout * 2};
     const uint32_t bbox[3] = {BK, BN, 1};
-    if (!make_map(&ma, a.a_img, 2, adims, astr, abox)) return MOE_ERR_CUDA;
-    if (!make_map(&mb, a.b_img, 3, bdims, bstr, bbox)) return MOE_ERR_CUDA;
+    if (!make_tensor_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, CU_TENSOR_MAP_SWIZZLE_128B, a.a_img, 2,
+                         adims, astr, abox))
+        return MOE_ERR_CUDA;
+    if (!make_tensor_map(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, CU_TENSOR_MAP_SWIZZLE_128B, a.b_img, 3,
+                         bdims, bstr, bbox))
+        return MOE_ERR_CUDA;
     GemmDev d;
     d.offsets = a.offsets;
     d.sched = a.sched;

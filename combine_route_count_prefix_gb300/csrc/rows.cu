@@ -438,6 +438,28 @@ __global__ void k_pack_w1(const int8_t *__restrict__ w1, uint4 *__restrict__ out
     }
 }
 
+// W1 [E, N, H] -> int8 [E, N, H] with rows reordered for the small-batch GEMM:
+// packed row 128b + 32q + l (b = 128-channel block, q = lane quadrant) holds
+//   l <  16: SiLU-half channel         64b + 16q + l
+//   l >= 16: multiplier channel  N/2 + 64b + 16q + (l - 16)
+// so the two halves of a SwiGLU pair sit 16 TMEM lanes apart in one warp.
+__global__ void k_pack_w1_i8(const int8_t *__restrict__ w1, int4 *__restrict__ out, int64_t E,
+                             int64_t N, int64_t H) {
+    pdl_wait();
+    const int64_t H16 = H / 16;
+    const int64_t total = E * N * H16;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t col16 = i % H16;
+        const int64_t prow = (i / H16) % N;
+        const int64_t e = i / (H16 * N);
+        const int64_t b = prow / 128, qq = (prow % 128) / 32, l = prow % 32;
+        const int64_t j = 64 * b + 16 * qq + (l & 15);
+        const int64_t src_row = l < 16 ? j : N / 2 + j;
+        out[i] = *reinterpret_cast<const int4 *>(w1 + (e * N + src_row) * H + col16 * 16);
+    }
+}
+
 int grid_for(int64_t items, int per_sm) {
     int64_t g = (int64_t)num_sms() * per_sm;
     if (items < g) g = items;
@@ -515,6 +537,15 @@ moe_status launch_pack_w1(const int8_t *w1, void *w1p, int64_t E, int64_t N, int
     if (total == 0) return MOE_OK;
     MOE_LAUNCH("pack_w1", k_pack_w1, grid_for((total + 255) / 256, 8), 256, 0, stream, w1,
                (uint4 *)w1p, E, N, H);
+    return MOE_OK;
+}
+
+moe_status launch_pack_w1_i8(const int8_t *w1, void *w1p, int64_t E, int64_t N, int64_t H,
+                             cudaStream_t stream) {
+    int64_t total = E * N * (H / 16);
+    if (total == 0) return MOE_OK;
+    MOE_LAUNCH("pack_w1_i8", k_pack_w1_i8, grid_for((total + 255) / 256, 8), 256, 0, stream, w1,
+               (int4 *)w1p, E, N, H);
     return MOE_OK;
 }
 

@@ -75,6 +75,10 @@ WORKLOADS = {
         description="16x256 = 4096 tokens, H=7168, 128 experts with Zipf(1.2) popularity "
                     "(10 experts unused), top-8, identity expert, shared, per-route mask "
                     "Bernoulli(0.95)"),
+    "small_batch_layer": Workload(
+        "small_batch_layer", 8, 16, 7168, 128, 8, 4096,
+        description="8x16 = 128 tokens, H=7168, 128 experts, top-8, FFN N=4096: the smallest "
+                    "point of the tokens-per-rank sweep (8 rows per expert on average)"),
     "large_prefill": Workload(
         "large_prefill", 8, 4096, 7168, 256, 8, 4096, has_shared=True,
         description="8x4096 = 32768 tokens, H=7168, 256 experts, top-8, FFN N=4096, shared"),

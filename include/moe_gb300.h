@@ -91,7 +91,22 @@ typedef struct moe_shape {
     int32_t has_shared;
     int64_t zero_experts;    /* Z: ids [E, E+Z) are zero experts (output 0) */
     int64_t copy_experts;    /* C: ids [E+Z, E+Z+C) are copy experts (output oriX) */
+    int32_t ffn_path;        /* MOE_FFN_PATH_*: which grouped-GEMM kernels the FFN uses */
+    int32_t reserved;        /* must be 0 */
 } moe_shape;
+
+/* Grouped-GEMM kernels of the expert FFN.  Both give bit-identical results.
+ *   LARGE: 128-row x 256-channel tiles on fp16 images of the weights; for
+ *          many rows per expert, where the tensor cores bound the time.
+ *   SMALL: the expert's rows (up to 128) against 128-channel tiles of int8
+ *          weights widened on chip; for few rows per expert, where reading
+ *          the weights bounds the time ("PTO MegaMoE ...", Supported Cases:
+ *          the M sweep from 16 tokens per rank).
+ *   AUTO:  SMALL when T*K <= MOE_FFN_SMALL_ROWS_PER_EXPERT * E, else LARGE. */
+#define MOE_FFN_PATH_AUTO 0
+#define MOE_FFN_PATH_LARGE 1
+#define MOE_FFN_PATH_SMALL 2
+#define MOE_FFN_SMALL_ROWS_PER_EXPERT 64
 
 /* ------------------------------------------------------------------------
  * Dispatch.
@@ -179,11 +194,11 @@ moe_status moe_combine(const moe_shape *shape, const void *expand_x, const int32
  * packed weights" and fixpipe scales.  The caller's int8 weights are
  *   w1 int8 [E, N, H]   (row n = GMM1 output channel n, H contiguous)
  *   w2 int8 [E, H, N/2] (row c = GMM2 output channel c, N/2 contiguous)
- * Packing, done once per model, turns them into the operand format the tensor
- * cores read: every int8 value becomes the fp16 number of the same value
- * (exact), and W1's rows are reordered so that each 256-row block holds a
- * SwiGLU pair of 64-column groups twice.  Packed sizes: E*N*H*2 and
- * E*H*(N/2)*2 bytes.  The packed buffers are opaque.
+ * Packing, done once per model, writes both kernels' operand formats into
+ * each packed buffer: fp16 images of the int8 values (exact) for the LARGE
+ * path, followed by int8 copies for the SMALL path; W1's rows are reordered
+ * in each so that every GEMM1 tile holds complete SwiGLU pairs.  Packed
+ * sizes: E*N*H*3 and E*H*(N/2)*3 bytes.  The packed buffers are opaque.
  * ------------------------------------------------------------------------ */
 moe_status moe_packed_weight_bytes(const moe_shape *shape, size_t *w1_bytes, size_t *w2_bytes);
 moe_status moe_pack_weights(const moe_shape *shape, const int8_t *w1, const int8_t *w2,
@@ -266,14 +281,16 @@ moe_status moe_stage_views_get(const moe_shape *shape, int for_layer, void *work
  * accumulator, per local expert).  C[r, n] = sum_i A[r, i] * W[e, n, i] for
  * rows r in [offsets[e], offsets[e+1]).
  *   A int8 [rows, Kd]; W int8 [E, N, Kd]; C int32 [rows, N]; rows >= offsets[E].
- *   N % 256 == 0, Kd % 8 == 0.
- * The int8 operands are first converted into fp16 images in the workspace.
+ *   N % 8 == 0, Kd % 8 == 0 (Kd % 16 == 0 for the SMALL kernel).
+ * path: MOE_FFN_PATH_* (AUTO: SMALL when rows <= 64 * E and Kd % 16 == 0).
+ * A is first converted into fp16 images in the workspace, and W too for the
+ * LARGE kernel; the SMALL kernel reads W as it is.
  * ------------------------------------------------------------------------ */
 moe_status moe_grouped_gemm_s32_workspace_size(int64_t rows, int64_t E, int64_t N, int64_t Kd,
                                                size_t *bytes);
 moe_status moe_grouped_gemm_s32(int64_t rows, int64_t E, int64_t N, int64_t Kd,
                                 const int32_t *expert_offsets, const int8_t *A,
-                                const int8_t *W, int32_t *C,
+                                const int8_t *W, int32_t *C, int path,
                                 void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------

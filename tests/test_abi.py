@@ -46,12 +46,16 @@ def test_workspace_sizes_and_shape_checks(B):
     cap = 16384 * 8
     assert n >= cap * 7168 * 2 * 2 + cap * 2048 * 6      # q1 + y + g + q2
     a, b = B.packed_weight_bytes(s)
-    assert a == 128 * 4096 * 7168 * 2 and b == 128 * 7168 * 2048 * 2
+    # fp16 images for the large-tile GEMM + int8 copies for the small-batch GEMM
+    assert a == 128 * 4096 * 7168 * 3 and b == 128 * 7168 * 2048 * 3
     for bad in [B.make_shape(10, 3, 128, 8, 2),      # T % P
                 B.make_shape(16, 2, 100, 8, 2),      # H % 8
                 B.make_shape(16, 2, 128, 2000, 2),   # E too large
                 B.make_shape(16, 2, 128, 8, 17),     # K > 16
-                B.make_shape(16, 2, 128, 8, 2, 300)]:  # N % 256
+                B.make_shape(16, 2, 128, 8, 2, 300),   # N % 256
+                B.make_shape(16, 2, 128, 8, 2, 256, ffn_path="large")]:
+        if bad.ffn_path:
+            bad.ffn_path = 3                           # no such kernel choice
         with pytest.raises(B.MoeError):
             B.layer_workspace_size(bad) if bad.ffn else B.dispatch_workspace_size(bad)
 

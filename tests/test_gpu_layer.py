@@ -7,6 +7,9 @@ Bars (the oracle computes each stage from its own inputs only):
   q2 (second quantisation): within 1 LSB on at most 0.1% of elements;
   y: bit-exact on every row whose q2 and s2 match the oracle's;
   out: max 2 bf16 ulp and rel-L2 <= 1e-3.
+Each check runs on both grouped-GEMM kernels ("large": fp16 weight images in
+128 x 256 tiles; "small": int8 weights widened on chip, an expert's rows on the
+MMA's N side), and the two must agree with each other bit for bit.
 """
 import numpy as np
 import pytest
@@ -29,12 +32,15 @@ def _device_weights(B, shape, W1, W2):
     return B.pack_weights(shape, dev(W1), dev(W2))
 
 
-def _stage_check(B, w, seed, with_stage_views=True):
+PATHS = ["large", "small"]
+
+
+def _stage_check(B, w, seed, path="auto"):
     T, P, H, E, K, N = (w.num_tokens, w.num_partitions, w.hidden, w.num_experts, w.topk, w.ffn)
     inp = wl.make_inputs(w, seed=seed)
     W1, S1, W2, S2 = wl.all_expert_weights(w, seed=seed)
     shape = B.make_shape(T, P, H, E, K, N, B.mask_kind_of(dev(inp["mask"]), T, K),
-                         inp["shared"] is not None)
+                         inp["shared"] is not None, ffn_path=path)
     (o1, w1p), (o2, w2p) = _device_weights(B, shape, W1, W2)
     out, ws = B.layer(shape, dev_bf16(inp["x"]), dev(inp["ids"]), dev(inp["probs"]), w1p,
                       dev(S1), w2p, dev(S2), mask=dev(inp["mask"]), shared=dev_bf16(inp["shared"]))
@@ -81,24 +87,56 @@ def _stage_check(B, w, seed, with_stage_views=True):
     return dict(q2_flips=q2_flips, R=R, ulp=ulp, rel=rel)
 
 
-def test_tiny_layer(B):
-    _stage_check(B, wl.WORKLOADS["tiny_layer"], seed=0)
+@pytest.mark.parametrize("path", PATHS)
+def test_tiny_layer(B, path):
+    _stage_check(B, wl.WORKLOADS["tiny_layer"], seed=0, path=path)
 
 
-def test_medium_layer_ragged_mask_shared(B):
+@pytest.mark.parametrize("path", PATHS)
+def test_medium_layer_ragged_mask_shared(B, path):
     w = wl.custom(P=2, M=160, H=512, E=8, K=4, N=512, mask_kind=1, mask_p=0.8, has_shared=True)
-    _stage_check(B, w, seed=1)
+    _stage_check(B, w, seed=1, path=path)
 
 
-def test_layer_route_mask_empty_experts(B):
+@pytest.mark.parametrize("path", PATHS)
+def test_layer_route_mask_empty_experts(B, path):
     w = wl.custom(P=4, M=72, H=256, E=24, K=6, N=256, mask_kind=2, mask_p=0.7, has_shared=True,
                   routing="zipf", zipf_zero=6)
-    _stage_check(B, w, seed=2)
+    _stage_check(B, w, seed=2, path=path)
 
 
-def test_layer_many_partitions_unfused_routing(B):
+@pytest.mark.parametrize("path", PATHS)
+def test_layer_many_partitions_unfused_routing(B, path):
     w = wl.custom(P=640, M=1, H=128, E=8, K=2, N=256, has_shared=True)
-    _stage_check(B, w, seed=3)
+    _stage_check(B, w, seed=3, path=path)
+
+
+def test_layer_paths_agree_bit_for_bit(B):
+    """Both GEMM kernels give the same g, q2, s2, y and output, bit for bit,
+    with experts holding 0, a few, and more than 128 rows (two row blocks)."""
+    w = wl.custom(P=4, M=96, H=1024, E=16, K=4, N=768, mask_kind=2, mask_p=0.6, has_shared=True,
+                  routing="zipf", zipf_s=2.0, zipf_zero=3)
+    T, P, H, E, K, N = (w.num_tokens, w.num_partitions, w.hidden, w.num_experts, w.topk, w.ffn)
+    inp = wl.make_inputs(w, seed=8)
+    W1, S1, W2, S2 = wl.all_expert_weights(w, seed=8)
+    res = {}
+    for path in PATHS:
+        shape = B.make_shape(T, P, H, E, K, N, 2, True, ffn_path=path)
+        (o1, w1p), (o2, w2p) = _device_weights(B, shape, W1, W2)
+        out, ws = B.layer(shape, dev_bf16(inp["x"]), dev(inp["ids"]), dev(inp["probs"]), w1p,
+                          dev(S1), w2p, dev(S2), mask=dev(inp["mask"]),
+                          shared=dev_bf16(inp["shared"]))
+        torch.cuda.synchronize()
+        assert B.read_device_status(ws) == 0
+        v = B.stage_views(shape, ws, for_layer=True)
+        R = int(v["expert_offsets"][-1].item())
+        res[path] = dict(out=host_bits(out), R=R, counts=v["expert_token_nums"].cpu().numpy(),
+                         **{k: v[k][:R].contiguous().view(torch.uint8).cpu().numpy()
+                            for k in ("g", "q2", "s2", "y")})
+    counts = res["large"]["counts"]
+    assert counts.max() > 128 and (counts == 0).any() and ((counts > 0) & (counts < 16)).any()
+    for k in ("out", "g", "q2", "s2", "y"):
+        np.testing.assert_array_equal(res["large"][k], res["small"][k], err_msg=k)
 
 
 def test_grouped_ffn_entry_on_dispatched_rows(B):
@@ -139,13 +177,13 @@ def test_layer_deterministic(B):
         np.testing.assert_array_equal(outs[0], o)
 
 
-def _sampled_full_size(B, name, n_tokens, seed=0):
+def _sampled_full_size(B, name, n_tokens, seed=0, path="auto"):
     """Full-size layer in the benchmark's launch configuration; the oracle
     computes a sample of tokens one by one."""
     w = wl.WORKLOADS[name]
     T, P, H, E, K, N = (w.num_tokens, w.num_partitions, w.hidden, w.num_experts, w.topk, w.ffn)
     inp = wl.make_inputs(w, seed=seed)
-    shape = B.make_shape(T, P, H, E, K, N, 0, inp["shared"] is not None)
+    shape = B.make_shape(T, P, H, E, K, N, 0, inp["shared"] is not None, ffn_path=path)
     w1 = torch.empty((E, N, H), dtype=torch.int8, device="cuda")
     w2 = torch.empty((E, H, N // 2), dtype=torch.int8, device="cuda")
     s1 = torch.empty((E, N), dtype=torch.float32, device="cuda")
@@ -194,6 +232,13 @@ def test_full_layer_sampled(B):
 
 def test_large_prefill_sampled(B):
     _sampled_full_size(B, "large_prefill", n_tokens=4)
+
+
+@pytest.mark.parametrize("path", ["auto", "large"])
+def test_small_batch_layer_sampled(B, path):
+    """The smallest point of the tokens-per-rank sweep (8 x 16 tokens, 128
+    experts): "auto" takes the small-batch kernels here."""
+    _sampled_full_size(B, "small_batch_layer", n_tokens=8, path=path)
 
 
 def test_quantisation_codes_exact_on_ties_and_many_scales(B):

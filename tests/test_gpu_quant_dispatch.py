@@ -37,12 +37,13 @@ def test_dispatch_quant_parity(B, smooth, mask_kind):
     np.testing.assert_array_equal(d["dynamic_scales"][:R].cpu().numpy(), s)
 
 
-def test_ffn_on_quantised_rows_equals_ffn_on_bf16_rows(B):
+@pytest.mark.parametrize("path", ["large", "small"])
+def test_ffn_on_quantised_rows_equals_ffn_on_bf16_rows(B, path):
     w = wl.custom(P=2, M=96, H=512, E=6, K=3, N=512)
     T, P, H, E, K, N = (w.num_tokens, w.num_partitions, w.hidden, w.num_experts, w.topk, w.ffn)
     inp = wl.make_inputs(w, seed=42)
     W1, S1, W2, S2 = wl.all_expert_weights(w, seed=42)
-    shape = B.make_shape(T, P, H, E, K, N)
+    shape = B.make_shape(T, P, H, E, K, N, ffn_path=path)
     (o1, w1p), (o2, w2p) = B.pack_weights(shape, dev(W1), dev(W2))
     dq = B.dispatch_quant(dev_bf16(inp["x"]), dev(inp["ids"]), E, P)
     yq, _ = B.grouped_ffn_q(shape, dq["expand_x"], dq["dynamic_scales"], dq["expert_offsets"], w1p,
