@@ -362,9 +362,7 @@ moe_status moe_pack_weights(const moe_shape *shape, const int8_t *w1, const int8
     MOE_TRY(launch_pack_w1(w1, w1_packed, E, N, H, stream));
     MOE_TRY(launch_i8_to_f16(w2, w2_packed, E * H * Nh, stream));
     MOE_TRY(launch_pack_w1_i8(w1, const_cast<void *>(packed_i8(w1_packed, E, N, H)), E, N, H, stream));
-    if (cudaMemcpyAsync(const_cast<void *>(packed_i8(w2_packed, E, H, Nh)), w2, (size_t)E * H * Nh,
-                        cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
-        return MOE_ERR_CUDA;
+    MOE_TRY(launch_bias_i8(w2, const_cast<void *>(packed_i8(w2_packed, E, H, Nh)), E * H * Nh, stream));
     return MOE_OK;
 }
 
@@ -583,11 +581,14 @@ moe_status moe_grouped_gemm_s32(int64_t rows, int64_t E, int64_t N, int64_t Kd,
     MOE_TRY(launch_sched(expert_offsets, E, at<int32_t>(workspace, L.sched),
                          at<int32_t>(workspace, L.status), stream));
     MOE_TRY(launch_i8_to_f16(A, at<void>(workspace, L.a_img), rows * Kd, stream));
-    if (!small) MOE_TRY(launch_i8_to_f16(W, at<void>(workspace, L.w_img), E * N * Kd, stream));
+    if (small)
+        MOE_TRY(launch_bias_i8(W, at<void>(workspace, L.w_img), E * N * Kd, stream));
+    else
+        MOE_TRY(launch_i8_to_f16(W, at<void>(workspace, L.w_img), E * N * Kd, stream));
     GemmArgs g{};
     g.a_img = at<void>(workspace, L.a_img);
     g.cap_rows = rows;
-    g.b_img = small ? static_cast<const void *>(W) : at<void>(workspace, L.w_img);
+    g.b_img = at<void>(workspace, L.w_img);
     g.E = E;
     g.Nout = N;
     g.Kd = Kd;

@@ -238,13 +238,14 @@ moe_status launch_pack_w1(const int8_t *w1, void *w1p, int64_t E, int64_t N, int
 moe_status launch_i8_to_f16(const int8_t *src, void *dst, int64_t n, cudaStream_t stream);
 moe_status launch_pack_w1_i8(const int8_t *w1, void *w1p, int64_t E, int64_t N, int64_t H,
                              cudaStream_t stream);
+moe_status launch_bias_i8(const int8_t *src, void *dst, int64_t n, cudaStream_t stream);
 
 // Grouped GEMM on fp16 images of int8 operands (tcgen05, TMEM accumulators).
 enum class Epi { S32 = 0, SwiGLU = 1, DequantBF16 = 2 };
 struct GemmArgs {
     const void *a_img;        // fp16 [cap_rows, Kd]
     int64_t cap_rows;
-    const void *b_img;        // fp16 [E, Nout, Kd]; int8 [E, Nout, Kd] for the small-batch GEMM
+    const void *b_img;        // fp16 [E, Nout, Kd]; biased bytes w + 128 for the int8-weight GEMM
     int64_t E, Nout, Kd;
     const int32_t *offsets;   // [E+1]; rows >= cap_rows are never stored
     const int32_t *sched;     // [E+1]
@@ -259,9 +260,9 @@ struct GemmArgs {
     int32_t *status;
 };
 moe_status launch_grouped_gemm(Epi epi, const GemmArgs &a, cudaStream_t stream);
-// The same GEMM for few rows per expert: int8 weights (b_img), weights on the
-// MMA's M side; Kd % 16 == 0 (and Nout % 128 == 0 for the SwiGLU epilogue,
-// whose weights come from launch_pack_w1_i8).
+// The same GEMM for few rows per expert: the weights stream as biased bytes
+// (b_img, w + 128; W1 in launch_pack_w1_i8's row order) and are widened to
+// fp16 on chip; only the rows present are loaded.  Kd % 16 == 0.
 moe_status launch_grouped_gemm_small(Epi epi, const GemmArgs &a, cudaStream_t stream);
 
 }  // namespace moe

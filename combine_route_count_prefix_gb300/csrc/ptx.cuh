@@ -8,6 +8,7 @@
 namespace moe {
 
 constexpr unsigned long long kTimeoutNs = 2000000000ull;   // bounded waits give up after ~2 s
+constexpr uint32_t kWaitSliceNs = 20000;                    // longest park per try_wait
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -31,6 +32,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// try_wait with a suspend-time hint: a thread whose phase is not complete is
+// parked (it issues nothing) until the phase completes or about `ns`
+// nanoseconds pass, instead of spinning and taking issue slots from the warps
+// that share its scheduler.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
                  "r"(bytes)
@@ -51,22 +67,28 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
 }
 
 // Waits for phase `parity` of `bar`.  Gives up when the CTA's abort flag is set
-// or after kTimeoutNs, setting the abort flag and the status bit.
-static __device__ __noinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          int32_t *status, bool honour_abort = true) {
-    if (mbar_try_wait(bar, parity)) return true;
+// or after kTimeoutNs, setting the abort flag and the status bit.  The first
+// test is inline; the bounded loop is a separate function entered only when
+// the phase is not complete yet, so that a wait which succeeds at once costs
+// one instruction and no call (a call spills the caller's live registers).
+static __device__ __noinline__ bool wait_bounded_loop(uint64_t *bar, uint32_t parity,
+                                                      volatile int *abort_flag, int32_t *status,
+                                                      bool honour_abort) {
     const uint64_t t0 = globaltimer();
-    for (uint32_t n = 1;; ++n) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((n & 255u) == 0) {
-            if (honour_abort && *abort_flag) return false;
-            if (globaltimer() - t0 > kTimeoutNs) {
-                *abort_flag = 1;
-                if (status) atomicOr(status, MOE_DEV_TIMEOUT);
-                return false;
-            }
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, kWaitSliceNs)) return true;
+        if (honour_abort && *abort_flag) return false;
+        if (globaltimer() - t0 > kTimeoutNs) {
+            *abort_flag = 1;
+            if (status) atomicOr(status, MOE_DEV_TIMEOUT);
+            return false;
         }
     }
+}
+__device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                             int32_t *status, bool honour_abort = true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_bounded_loop(bar, parity, abort_flag, status, honour_abort);
 }
 
 }  // namespace moe

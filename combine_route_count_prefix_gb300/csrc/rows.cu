@@ -438,25 +438,35 @@ __global__ void k_pack_w1(const int8_t *__restrict__ w1, uint4 *__restrict__ out
     }
 }
 
-// W1 [E, N, H] -> int8 [E, N, H] with rows reordered for the small-batch GEMM:
-// packed row 128b + 32q + l (b = 128-channel block, q = lane quadrant) holds
-//   l <  16: SiLU-half channel         64b + 16q + l
-//   l >= 16: multiplier channel  N/2 + 64b + 16q + (l - 16)
-// so the two halves of a SwiGLU pair sit 16 TMEM lanes apart in one warp.
-__global__ void k_pack_w1_i8(const int8_t *__restrict__ w1, int4 *__restrict__ out, int64_t E,
+// W1 [E, N, H] -> biased bytes (w + 128) [E, N, H] with k_pack_w1's row order,
+// the weight operand of the int8-weight GEMM.
+__global__ void k_pack_w1_i8(const int8_t *__restrict__ w1, uint4 *__restrict__ out, int64_t E,
                              int64_t N, int64_t H) {
     pdl_wait();
     const int64_t H16 = H / 16;
     const int64_t total = E * N * H16;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t col16 = i % H16;
-        const int64_t prow = (i / H16) % N;
-        const int64_t e = i / (H16 * N);
-        const int64_t b = prow / 128, qq = (prow % 128) / 32, l = prow % 32;
-        const int64_t j = 64 * b + 16 * qq + (l & 15);
-        const int64_t src_row = l < 16 ? j : N / 2 + j;
-        out[i] = *reinterpret_cast<const int4 *>(w1 + (e * N + src_row) * H + col16 * 16);
+        int64_t col16 = i % H16;
+        int64_t prow = (i / H16) % N;
+        int64_t e = i / (H16 * N);
+        int64_t b = prow / 256, within = prow % 256, h = within / 128, ii = within % 128;
+        int64_t src_row = (ii < 64) ? (128 * b + 64 * h + ii) : (N / 2 + 128 * b + 64 * h + (ii - 64));
+        uint4 v = *reinterpret_cast<const uint4 *>(w1 + (e * N + src_row) * H + col16 * 16);
+        out[i] = make_uint4(v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u,
+                            v.w ^ 0x80808080u);
+    }
+}
+
+// int8 -> biased bytes (w + 128): flipping the sign bit of a two's-complement
+// byte adds 128.  n16 = number of 16-byte vectors.
+__global__ void k_bias_i8(const uint4 *__restrict__ src, uint4 *__restrict__ dst, int64_t n16) {
+    pdl_wait();
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const uint4 v = src[i];
+        dst[i] = make_uint4(v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u,
+                            v.w ^ 0x80808080u);
     }
 }
 
@@ -545,7 +555,15 @@ moe_status launch_pack_w1_i8(const int8_t *w1, void *w1p, int64_t E, int64_t N, 
     int64_t total = E * N * (H / 16);
     if (total == 0) return MOE_OK;
     MOE_LAUNCH("pack_w1_i8", k_pack_w1_i8, grid_for((total + 255) / 256, 8), 256, 0, stream, w1,
-               (int4 *)w1p, E, N, H);
+               (uint4 *)w1p, E, N, H);
+    return MOE_OK;
+}
+
+moe_status launch_bias_i8(const int8_t *src, void *dst, int64_t n, cudaStream_t stream) {
+    const int64_t n16 = n / 16;   // callers pass multiples of 16
+    if (n16 == 0) return MOE_OK;
+    MOE_LAUNCH("bias_i8", k_bias_i8, grid_for((n16 + 255) / 256, 8), 256, 0, stream,
+               (const uint4 *)src, (uint4 *)dst, n16);
     return MOE_OK;
 }
 

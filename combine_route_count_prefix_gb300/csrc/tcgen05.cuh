@@ -1,5 +1,5 @@
 // tcgen05.cuh -- inline-PTX wrappers for TMA tensor copies, TMEM allocation,
-// tcgen05.mma (kind::f16, one CTA) and tcgen05.ld, shared by the grouped GEMMs.
+// tcgen05.mma (kind::f16, one CTA) and tcgen05.ld for the grouped GEMMs.
 #pragma once
 #include "ptx.cuh"
 

@@ -98,15 +98,16 @@ typedef struct moe_shape {
 /* Grouped-GEMM kernels of the expert FFN.  Both give bit-identical results.
  *   LARGE: 128-row x 256-channel tiles on fp16 images of the weights; for
  *          many rows per expert, where the tensor cores bound the time.
- *   SMALL: the expert's rows (up to 128) against 128-channel tiles of int8
- *          weights widened on chip; for few rows per expert, where reading
- *          the weights bounds the time ("PTO MegaMoE ...", Supported Cases:
- *          the M sweep from 16 tokens per rank).
+ *   SMALL: the same tiles with the weights read as int8 (half the bytes)
+ *          and widened to fp16 on chip, and only the rows present loaded; for
+ *          few rows per expert, where reading the weights bounds the time
+ *          ("PTO MegaMoE ...", Supported Cases: the M sweep from 16 tokens
+ *          per rank).
  *   AUTO:  SMALL when T*K <= MOE_FFN_SMALL_ROWS_PER_EXPERT * E, else LARGE. */
 #define MOE_FFN_PATH_AUTO 0
 #define MOE_FFN_PATH_LARGE 1
 #define MOE_FFN_PATH_SMALL 2
-#define MOE_FFN_SMALL_ROWS_PER_EXPERT 64
+#define MOE_FFN_SMALL_ROWS_PER_EXPERT 32
 
 /* ------------------------------------------------------------------------
  * Dispatch.
@@ -196,9 +197,9 @@ moe_status moe_combine(const moe_shape *shape, const void *expand_x, const int32
  *   w2 int8 [E, H, N/2] (row c = GMM2 output channel c, N/2 contiguous)
  * Packing, done once per model, writes both kernels' operand formats into
  * each packed buffer: fp16 images of the int8 values (exact) for the LARGE
- * path, followed by int8 copies for the SMALL path; W1's rows are reordered
- * in each so that every GEMM1 tile holds complete SwiGLU pairs.  Packed
- * sizes: E*N*H*3 and E*H*(N/2)*3 bytes.  The packed buffers are opaque.
+ * path, followed by byte copies biased by +128 for the SMALL path; W1's rows
+ * are reordered in both so that every GEMM1 tile holds complete SwiGLU pairs.
+ * Packed sizes: E*N*H*3 and E*H*(N/2)*3 bytes.  The packed buffers are opaque.
  * ------------------------------------------------------------------------ */
 moe_status moe_packed_weight_bytes(const moe_shape *shape, size_t *w1_bytes, size_t *w2_bytes);
 moe_status moe_pack_weights(const moe_shape *shape, const int8_t *w1, const int8_t *w2,
@@ -282,9 +283,9 @@ moe_status moe_stage_views_get(const moe_shape *shape, int for_layer, void *work
  * rows r in [offsets[e], offsets[e+1]).
  *   A int8 [rows, Kd]; W int8 [E, N, Kd]; C int32 [rows, N]; rows >= offsets[E].
  *   N % 8 == 0, Kd % 8 == 0 (Kd % 16 == 0 for the SMALL kernel).
- * path: MOE_FFN_PATH_* (AUTO: SMALL when rows <= 64 * E and Kd % 16 == 0).
- * A is first converted into fp16 images in the workspace, and W too for the
- * LARGE kernel; the SMALL kernel reads W as it is.
+ * path: MOE_FFN_PATH_* (AUTO: SMALL when rows <= 32 * E and Kd % 16 == 0).
+ * A is first converted into fp16 images in the workspace, and W into fp16
+ * images (LARGE) or biased bytes (SMALL).
  * ------------------------------------------------------------------------ */
 moe_status moe_grouped_gemm_s32_workspace_size(int64_t rows, int64_t E, int64_t N, int64_t Kd,
                                                size_t *bytes);
