@@ -66,7 +66,7 @@ def parse():
     ap.add_argument("--soak", type=float, default=2.0,
                     help="seconds of untimed steps before the timed region (clock samples)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ffn-path", default="auto", choices=["auto", "large", "small"],
+    ap.add_argument("--ffn-path", default="auto", choices=["auto", "large", "small", "large_pair"],
                     help="grouped-GEMM kernels of the layer workloads (auto: small-batch "
                          "kernels when T*K <= 32*E)")
     return ap.parse_args()
@@ -409,13 +409,13 @@ class LayerPath:
         R = self.rows()
         H, N, Nh = w.hidden, w.ffn, w.ffn // 2
         small = "gemm1_swiglu_w8" in prof
-        sfx = "_w8" if small else ""
+        sfx = "_w8" if small else ("_pair" if "gemm1_swiglu_pair" in prof else "")
         g1, g2 = "gemm1_swiglu" + sfx, "gemm2_dequant" + sfx
         fl = {g1: 2.0 * R * H * N, g2: 2.0 * R * Nh * H}
         dom = max(fl, key=lambda k: prof.get(k, (1, 0.0))[1])
         n, ms = prof[dom]
         us = ms / n * 1e3
-        extra = {"ffn_path": "small" if small else "large",
+        extra = {"ffn_path": "small" if small else ("large_pair" if sfx else "large"),
                  "gemm_tflops": {k: fl[k] / (prof[k][1] / prof[k][0] * 1e-3) / 1e12 for k in fl},
                  "status": self.B.read_device_status(self.ws)}
         step_bytes = None
@@ -542,6 +542,7 @@ def run_ours(args, rank, world, dist):
     pk = peaks()
     roofline, step_bytes, extra = path.roofline(prof, pk)
     roofline["per_kernel_us"] = {k: round(ms_ / n * 1e3, 3) for k, (n, ms_) in prof.items()}
+    roofline["per_kernel_grid"] = dict(B.LAST_GRIDS)
 
     # ---------------- end to end through the C ABI with pinned host buffers
     def pin(a):

@@ -55,8 +55,9 @@ class MoeShape(ctypes.Structure):
 
 
 # moe_shape.ffn_path: which grouped-GEMM kernels the FFN uses (same results)
-FFN_PATH_AUTO, FFN_PATH_LARGE, FFN_PATH_SMALL = 0, 1, 2
-FFN_PATHS = {"auto": FFN_PATH_AUTO, "large": FFN_PATH_LARGE, "small": FFN_PATH_SMALL}
+FFN_PATH_AUTO, FFN_PATH_LARGE, FFN_PATH_SMALL, FFN_PATH_LARGE_PAIR = 0, 1, 2, 3
+FFN_PATHS = {"auto": FFN_PATH_AUTO, "large": FFN_PATH_LARGE, "small": FFN_PATH_SMALL,
+             "large_pair": FFN_PATH_LARGE_PAIR}
 
 
 class StageViews(ctypes.Structure):
@@ -410,7 +411,7 @@ def stage_views(shape: MoeShape, ws, for_layer=True) -> dict:
 
 def grouped_gemm_s32(expert_offsets, A, W, ws=None, C=None, stream=None, path="auto"):
     """C[r] = A[r] @ W[e]^T (int8 x int8 -> int32) for rows of expert e.
-    path: "auto", "large" or "small" (moe_shape.ffn_path's kernels)."""
+    path: "auto", "large", "small" or "large_pair" (moe_shape.ffn_path's kernels)."""
     rows, Kd = A.shape
     E, N, _ = W.shape
     _check(A, torch.int8, (rows, Kd), "A")
@@ -441,12 +442,18 @@ def profile_enable(on: bool):
     _call("moe_profile_enable", int(bool(on)))
 
 
+LAST_GRIDS = {}   # kernel name -> CTAs of its last launch, from the latest profile_report()
+
+
 def profile_report() -> dict:
-    """{kernel name: (launches, total_ms)} since the last report."""
+    """{kernel name: (launches, total_ms)} since the last report; the grid
+    size of each kernel's launches is left in LAST_GRIDS."""
     buf = ctypes.create_string_buffer(1 << 16)
     _call("moe_profile_report", buf, ctypes.c_size_t(len(buf)))
     out = {}
+    LAST_GRIDS.clear()
     for line in buf.value.decode().splitlines():
-        name, n, ms = line.split()
+        name, n, ms, grid = line.split()
         out[name] = (int(n), float(ms))
+        LAST_GRIDS[name] = int(grid)
     return out

@@ -21,6 +21,7 @@ std::atomic<bool> g_profile{false};
 struct ProfRecord {
     const char *name;
     cudaEvent_t start, stop;
+    unsigned grid;   // CTAs launched
 };
 std::mutex g_prof_mu;
 std::vector<ProfRecord> g_records;
@@ -38,11 +39,11 @@ cudaEvent_t take_event() {
 }
 }  // namespace
 
-int launch_begin(const char *name, cudaStream_t stream) {
+int launch_begin(const char *name, cudaStream_t stream, unsigned grid) {
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (!g_profile.load(std::memory_order_relaxed)) return -1;
     std::lock_guard<std::mutex> lk(g_prof_mu);
-    ProfRecord r{name, take_event(), take_event()};
+    ProfRecord r{name, take_event(), take_event(), grid};
     cudaEventRecord(r.start, stream);
     g_records.push_back(r);
     return (int)g_records.size() - 1;
@@ -87,7 +88,7 @@ moe_status check_shape(const moe_shape *s, bool need_ffn) {
         s->num_experts + s->zero_experts + s->copy_experts > INT32_MAX)
         return MOE_ERR_SHAPE;
     if (s->has_shared != 0 && s->has_shared != 1) return MOE_ERR_PARAM_INVALID;
-    if (s->ffn_path < MOE_FFN_PATH_AUTO || s->ffn_path > MOE_FFN_PATH_SMALL || s->reserved != 0)
+    if (s->ffn_path < MOE_FFN_PATH_AUTO || s->ffn_path > MOE_FFN_PATH_LARGE_PAIR || s->reserved != 0)
         return MOE_ERR_PARAM_INVALID;
     const int64_t cap = s->num_tokens * s->topk;
     if (cap > INT32_MAX) return MOE_ERR_SHAPE;
@@ -199,6 +200,7 @@ moe_status moe_profile_report(char *buf, size_t bytes) {
     if (!buf || bytes == 0) return MOE_ERR_NULLPTR;
     std::lock_guard<std::mutex> lk(g_prof_mu);
     std::map<std::string, std::pair<int, double>> agg;
+    std::map<std::string, unsigned> grid;
     std::vector<std::string> order;
     for (auto &r : g_records) {
         float ms = 0.0f;
@@ -211,6 +213,7 @@ moe_status moe_profile_report(char *buf, size_t bytes) {
             it->second.first += 1;
             it->second.second += ms;
         }
+        grid[r.name] = r.grid;
         g_event_pool.push_back(r.start);
         g_event_pool.push_back(r.stop);
     }
@@ -219,7 +222,7 @@ moe_status moe_profile_report(char *buf, size_t bytes) {
     std::string out;
     char line[256];
     for (auto &n : order) {
-        snprintf(line, sizeof line, "%s %d %.6f\n", n.c_str(), agg[n].first, agg[n].second);
+        snprintf(line, sizeof line, "%s %d %.6f %u\n", n.c_str(), agg[n].first, agg[n].second, grid[n]);
         out += line;
     }
     if (out.size() + 1 > bytes) return MOE_ERR_PARAM_INVALID;
@@ -346,8 +349,13 @@ static const void *packed_i8(const void *packed, int64_t E, int64_t rows, int64_
 
 static bool use_small_path(int32_t path, int64_t rows, int64_t E) {
     if (path == MOE_FFN_PATH_SMALL) return true;
-    if (path == MOE_FFN_PATH_LARGE) return false;
+    if (path == MOE_FFN_PATH_LARGE || path == MOE_FFN_PATH_LARGE_PAIR) return false;
     return rows <= (int64_t)MOE_FFN_SMALL_ROWS_PER_EXPERT * E;
+}
+
+static moe_status run_gemm(bool small, int32_t path, Epi epi, const GemmArgs &g, cudaStream_t stream) {
+    if (small) return launch_grouped_gemm_small(epi, g, stream);
+    return launch_grouped_gemm(epi, g, stream, path == MOE_FFN_PATH_LARGE_PAIR);
 }
 
 moe_status moe_pack_weights(const moe_shape *shape, const int8_t *w1, const int8_t *w2,
@@ -374,7 +382,6 @@ static moe_status run_ffn_core(const moe_shape &s, const Layout &L, void *ws,
     const int64_t cap = s.num_tokens * s.topk, Nh = s.ffn / 2;
     int32_t *status = at<int32_t>(ws, L.status);
     const bool small = use_small_path(s.ffn_path, cap, s.num_experts);
-    auto gemm = small ? launch_grouped_gemm_small : launch_grouped_gemm;
     GemmArgs g1{};
     g1.a_img = at<void>(ws, L.q1);
     g1.cap_rows = cap;
@@ -388,7 +395,7 @@ static moe_status run_ffn_core(const moe_shape &s, const Layout &L, void *ws,
     g1.scale1 = scale1;
     g1.s1 = at<float>(ws, L.s1);
     g1.status = status;
-    MOE_TRY(gemm(Epi::SwiGLU, g1, stream));
+    MOE_TRY(run_gemm(small, s.ffn_path, Epi::SwiGLU, g1, stream));
     MOE_TRY(launch_quant2(at<float>(ws, L.g), offsets, s.num_experts, at<void>(ws, L.q2),
                           at<float>(ws, L.s2), cap, Nh, stream));
     GemmArgs g2{};
@@ -404,7 +411,7 @@ static moe_status run_ffn_core(const moe_shape &s, const Layout &L, void *ws,
     g2.scale2 = scale2;
     g2.s2 = at<float>(ws, L.s2);
     g2.status = status;
-    return gemm(Epi::DequantBF16, g2, stream);
+    return run_gemm(small, s.ffn_path, Epi::DequantBF16, g2, stream);
 }
 
 moe_status moe_grouped_ffn_workspace_size(const moe_shape *shape, size_t *bytes) {
@@ -573,7 +580,7 @@ moe_status moe_grouped_gemm_s32(int64_t rows, int64_t E, int64_t N, int64_t Kd,
     if (!aligned(A, 16) || !aligned(W, 16) || !aligned(C, 16) || !aligned(workspace, kAlign))
         return MOE_ERR_ALIGNMENT;
     if (workspace_bytes < need) return MOE_ERR_WORKSPACE;
-    if (path < MOE_FFN_PATH_AUTO || path > MOE_FFN_PATH_SMALL) return MOE_ERR_PARAM_INVALID;
+    if (path < MOE_FFN_PATH_AUTO || path > MOE_FFN_PATH_LARGE_PAIR) return MOE_ERR_PARAM_INVALID;
     if (path == MOE_FFN_PATH_SMALL && Kd % 16 != 0) return MOE_ERR_SHAPE;
     const bool small = Kd % 16 == 0 && use_small_path(path, rows, E);
     if (rows == 0) return MOE_OK;
@@ -596,8 +603,7 @@ moe_status moe_grouped_gemm_s32(int64_t rows, int64_t E, int64_t N, int64_t Kd,
     g.sched = at<int32_t>(workspace, L.sched);
     g.c_s32 = C;
     g.status = at<int32_t>(workspace, L.status);
-    return small ? launch_grouped_gemm_small(Epi::S32, g, stream)
-                 : launch_grouped_gemm(Epi::S32, g, stream);
+    return run_gemm(small, path, Epi::S32, g, stream);
 }
 
 }  // extern "C"

@@ -27,7 +27,7 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // Every kernel launch goes through launch_begin/launch_end: they count launches
 // and, when profiling is on, bracket the launch with a CUDA event pair recorded
 // on the launching stream.
-int launch_begin(const char *name, cudaStream_t stream);
+int launch_begin(const char *name, cudaStream_t stream, unsigned grid);
 void launch_end(int token, cudaStream_t stream);
 int num_sms();
 
@@ -55,9 +55,30 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// The same with a cluster of `cluster_x` CTAs along x (grid.x a multiple of it).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                               cudaStream_t stream, unsigned cluster_x, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster_x;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1 + MOE_PDL_ATTRS;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 #define MOE_LAUNCH(name, kernel, grid, block, smem, stream, ...)                          \
     do {                                                                                  \
-        int _tok = ::moe::launch_begin(name, stream);                                     \
+        int _tok = ::moe::launch_begin(name, stream, dim3(grid).x);                       \
         cudaError_t _err = ::moe::launch_pdl(kernel, dim3(grid), dim3(block), (smem),     \
                                              (stream), __VA_ARGS__);                      \
         if (_err == cudaSuccess) _err = cudaGetLastError();                               \
@@ -73,6 +94,17 @@ __device__ __forceinline__ void pdl_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+
+#define MOE_LAUNCH_CLUSTER(name, kernel, grid, block, smem, stream, cluster_x, ...)      \
+    do {                                                                                  \
+        int _tok = ::moe::launch_begin(name, stream, dim3(grid).x);                       \
+        cudaError_t _err = ::moe::launch_pdl_cluster(kernel, dim3(grid), dim3(block),     \
+                                                     (smem), (stream), (cluster_x),       \
+                                                     __VA_ARGS__);                        \
+        if (_err == cudaSuccess) _err = cudaGetLastError();                               \
+        ::moe::launch_end(_tok, stream);                                                  \
+        if (_err != cudaSuccess) return MOE_ERR_CUDA;                                     \
+    } while (0)
 
 #define MOE_TRY(expr)                                                         \
     do {                                                                      \
@@ -259,7 +291,10 @@ struct GemmArgs {
     const float *s2;          // [cap_rows]
     int32_t *status;
 };
-moe_status launch_grouped_gemm(Epi epi, const GemmArgs &a, cudaStream_t stream);
+// pair: 256-row tiles on clusters of two CTAs (falls back to one-SM tiles when
+// no cluster of that kernel fits).
+moe_status launch_grouped_gemm(Epi epi, const GemmArgs &a, cudaStream_t stream,
+                               bool pair = false);
 // The same GEMM for few rows per expert: the weights stream as biased bytes
 // (b_img, w + 128; W1 in launch_pack_w1_i8's row order) and are widened to
 // fp16 on chip; only the rows present are loaded.  Kd % 16 == 0.

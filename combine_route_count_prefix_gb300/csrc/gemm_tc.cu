@@ -57,6 +57,18 @@ constexpr size_t kBarrierBytes = 256;
 constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + 1024 + kBarrierBytes +
                               2 * (kMaxExperts + 1) * sizeof(int32_t);
 
+// The CTA-pair variant: a 256 x 256 tile per cluster of two CTAs; each CTA
+// stages its 128 rows of A and its 128 of the 256 weight rows (16 + 16 KB)
+// per k-block, so six stages fit.
+constexpr int P_STAGES = 6;
+constexpr int P_B_BYTES = (BN / 2) * BK * 2;
+constexpr int P_STAGE_BYTES = A_BYTES + P_B_BYTES;
+constexpr size_t P_RING_BYTES = (size_t)P_STAGES * P_STAGE_BYTES;
+constexpr size_t P_SMEM_BYTES = P_RING_BYTES + 1024 + kBarrierBytes +
+                                2 * (kMaxExperts + 1) * sizeof(int32_t);
+static_assert(P_SMEM_BYTES <= 232448, "shared memory budget");
+static_assert((3 * P_STAGES + 5) * 8 + 16 <= (int)kBarrierBytes, "barriers");
+
 // The int8-weight variant (few rows per expert): weights stream as int8 into
 // their own ring and two converter warps widen each 256 x 64 tile to the fp16
 // B operand; the tile's rows come as 16-row boxes, only as many as it has.
@@ -337,6 +349,251 @@ k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// ---------------------------------------------------------------- CTA-pair variant
+struct PairTile {
+    int e, row0, rows, nb;   // row0/rows: this CTA's 128-row half (rows may be <= 0)
+};
+
+__device__ __forceinline__ PairTile decode_pair_tile(int64_t tile, int n_blocks, int E,
+                                                     const int32_t *s_psched, const int32_t *s_off,
+                                                     uint32_t rank) {
+    PairTile t;
+    const int pb = (int)(tile / n_blocks);
+    t.nb = (int)(tile % n_blocks);
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {   // last expert whose first 256-row block is <= pb
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_psched[mid] <= pb) lo = mid; else hi = mid - 1;
+    }
+    t.e = lo;
+    t.row0 = s_off[lo] + (pb - s_psched[lo]) * (2 * BM) + (int)rank * BM;
+    t.rows = min(BM, s_off[lo + 1] - t.row0);
+    return t;
+}
+
+// Clusters of two CTAs (ranks 0 and 1, on two SMs).  Per 256-row x 256-column
+// tile, CTA r loads rows [128 r, 128 r + 128) of the tile's A and weight rows
+// [128 r, 128 r + 128) of its B; one thread of CTA 0 issues M = 256, N = 256
+// MMAs over both CTAs' halves, and each CTA's TMEM receives its own 128 rows of
+// the accumulator, which its own epilogue warps drain as in k_grouped_gemm.
+//   warp 0      TMA producer (each CTA, its own halves) into a 6-stage ring
+//   warp 1      TMEM (pair allocation); CTA 0: MMA issuer; CTA 1: relays the
+//               landing of its halves to CTA 0's barrier (cluster-scope arrive)
+//   warps 2..9  epilogue; their accumulator-free signal goes to CTA 0
+// Commits arrive on both CTAs' barriers (multicast).  Every wait is bounded;
+// both CTAs meet at a cluster barrier before either frees TMEM or exits.
+template <int EPI>
+__global__ void __launch_bounds__(THREADS, 1)
+k_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    GemmDev p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + P_RING_BYTES);
+    uint64_t *peer_full = full + P_STAGES;
+    uint64_t *empty = peer_full + P_STAGES;
+    uint64_t *acc_full = empty + P_STAGES;
+    uint64_t *acc_empty = acc_full + 2;
+    uint64_t *drain = acc_empty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int32_t *s_off = reinterpret_cast<int32_t *>(smem + P_RING_BYTES + kBarrierBytes);
+    int32_t *s_psched = s_off + (kMaxExperts + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P_STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&peer_full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 2 * EPI_WARPS);   // both CTAs' epilogue warps
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB) : "memory");
+    }
+    pdl_wait();   // everything below may read what earlier kernels wrote
+    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s_off[i] = p.offsets[i];
+    __syncthreads();
+    if (warp == 0) {
+        // s_psched[e] = 256-row blocks of the experts before e (warp scan)
+        int carry = 0;
+        for (int base = 0; base < p.E; base += 32) {
+            const int e = base + lane;
+            const int c = e < p.E ? (s_off[e + 1] - s_off[e] + 2 * BM - 1) / (2 * BM) : 0;
+            int x = c;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, d);
+                if (lane >= d) x += y;
+            }
+            if (e < p.E) s_psched[e] = carry + x - c;
+            carry += __shfl_sync(0xffffffffu, x, 31);
+        }
+        if (lane == 0) s_psched[p.E] = carry;
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();   // both CTAs' barriers and TMEM exist before any cross-CTA use
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int64_t total_tiles = (int64_t)s_psched[p.E] * p.n_blocks;
+    const int num_chunks = (p.num_kb + CHUNK_KB - 1) / CHUNK_KB;
+    const int64_t first = blockIdx.x >> 1, step = gridDim.x >> 1;   // cluster index and count
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer (both CTAs)
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued_phase[P_STAGES];
+#pragma unroll
+            for (int s = 0; s < P_STAGES; ++s) issued_phase[s] = -1;
+            bool ok = true;
+            for (int64_t tile = first; ok && tile < total_tiles; tile += step) {
+                const PairTile t = decode_pair_tile(tile, p.n_blocks, p.E, s_psched, s_off, rank);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    // freed by CTA 0's commit once the MMAs have read both halves
+                    if (!wait_bounded_cluster(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                    uint8_t *sa = smem + (size_t)stage * P_STAGE_BYTES;
+                    mbar_arrive_expect_tx(&full[stage], P_STAGE_BYTES);
+                    // rows past this CTA's half (or past the buffer) only reach
+                    // accumulator rows that are never stored
+                    tma_load_2d(sa, &tmA, &full[stage], kb * BK, t.row0);
+                    tma_load_3d(sa + A_BYTES, &tmB, &full[stage], kb * BK,
+                                t.nb * BN + (int)rank * (BN / 2), t.e);
+                    issued_phase[stage] = (int)phase;
+                    if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            for (int s = 0; s < P_STAGES; ++s)
+                if (issued_phase[s] >= 0)
+                    wait_bounded(&full[s], (uint32_t)issued_phase[s], abort_flag, p.status, false);
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && !leader) {
+            // ------------------------------------------------ relay (CTA 1)
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int64_t tile = first; ok && tile < total_tiles; tile += step) {
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bounded(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+                    mbar_arrive_cluster(&peer_full[stage], 0);
+                    if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+        } else if (lane == 0) {
+            // ------------------------------------------------ MMA issuer (CTA 0)
+            constexpr uint32_t idesc = idesc_f16(2 * BM, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int accb = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int64_t tile = first; ok && tile < total_tiles; tile += step) {
+                for (int kb0 = 0; ok && kb0 < p.num_kb; kb0 += CHUNK_KB) {
+                    if (!wait_bounded_cluster(&acc_empty[accb], acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + (uint32_t)(accb * BN);
+                    const int kb1 = min(kb0 + CHUNK_KB, p.num_kb);
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!wait_bounded(&full[stage], phase, abort_flag, p.status) ||
+                            !wait_bounded_cluster(&peer_full[stage], phase, abort_flag, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a_addr = smem_u32(smem + (size_t)stage * P_STAGE_BYTES);
+                        const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+                        for (int k = 0; k < BK / 16; ++k)
+                            mma_f16_pair(d_tmem, desc_sw128(a_addr + 32 * k), desc_sw128(b_addr + 32 * k),
+                                         idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                        mma_commit_pair(&empty[stage], 0x3);
+                        if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
+                    }
+                    if (!ok) break;
+                    mma_commit_pair(&acc_full[accb], 0x3);
+                    if (++accb == 2) { accb = 0; acc_phase ^= 1u; }
+                }
+            }
+            // no MMA may still be running when either CTA frees TMEM or exits
+            mma_commit_pair(drain, 0x1);
+            wait_bounded(drain, 0, abort_flag, p.status, false);
+        }
+    } else {
+        // ---------------------------------------------------- epilogue warps (both CTAs)
+        const int q = warp & 3;
+        const int hf = (warp - 2) >> 2;
+        const int rloc = q * 32 + lane;
+        int accb = 0;
+        uint32_t acc_phase = 0;
+        for (int64_t tile = first; tile < total_tiles; tile += step) {
+            const PairTile t = decode_pair_tile(tile, p.n_blocks, p.E, s_psched, s_off, rank);
+            const bool rows_here = q * 32 < t.rows;   // warp-uniform
+            int32_t acc[128];
+            bool ok = true;
+            for (int c = 0; c < num_chunks; ++c) {
+                const bool w = wait_bounded_cluster(&acc_full[accb], acc_phase, abort_flag, p.status);
+                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+                tc_fence_after();
+                if (rows_here) {
+                    const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) +
+                                           (uint32_t)(accb * BN + hf * 128);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t r[32];
+                        tmem_ld32(taddr + 32 * j, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int v = __float2int_rn(__uint_as_float(r[i]));
+                            acc[32 * j + i] = (c == 0) ? v : acc[32 * j + i] + v;
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (leader) mbar_arrive(&acc_empty[accb]);
+                    else mbar_arrive_cluster(&acc_empty[accb], 0);
+                }
+                if (++accb == 2) { accb = 0; acc_phase ^= 1u; }
+            }
+            if (!ok) break;
+            if (rows_here && rloc < t.rows && (int64_t)t.row0 + rloc < p.cap_rows) {
+                Tile et;
+                et.e = t.e;
+                et.row0 = t.row0;
+                et.rows = t.rows;
+                et.nb = t.nb;
+                epilogue_store<EPI>(p, et, t.row0 + rloc, hf, acc);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
 
 // ---------------------------------------------------------------- int8-weight variant
@@ -651,6 +908,49 @@ moe_status launch_epi_w8(const CUtensorMap &ma, const CUtensorMap &mw, const Gem
     return MOE_OK;
 }
 
+// Clusters of the pair kernel that fit on the GPU at once (0 if it cannot run);
+// the persistent grid is twice that.
+template <int EPI>
+int pair_clusters() {
+    static int cached = -1;
+    if (cached < 0) {
+        cached = 0;
+        if (cudaFuncSetAttribute(k_grouped_gemm_pair<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)P_SMEM_BYTES) != cudaSuccess) {
+            cudaGetLastError();
+            return cached;
+        }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(num_sms() & ~1));
+        cfg.blockDim = dim3(THREADS);
+        cfg.dynamicSmemBytes = P_SMEM_BYTES;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, (const void *)k_grouped_gemm_pair<EPI>, &cfg) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+        cached = n;
+    }
+    return cached;
+}
+
+template <int EPI>
+moe_status launch_epi_pair(const CUtensorMap &ma, const CUtensorMap &mb, const GemmDev &d,
+                           int clusters, cudaStream_t stream) {
+    const char *names[3] = {"gemm_s32_pair", "gemm1_swiglu_pair", "gemm2_dequant_pair"};
+    MOE_LAUNCH_CLUSTER(names[EPI], k_grouped_gemm_pair<EPI>, 2 * clusters, THREADS, P_SMEM_BYTES,
+                       stream, 2u, ma, mb, d);
+    return MOE_OK;
+}
+
 GemmDev gemm_dev(const GemmArgs &a) {
     GemmDev d;
     d.offsets = a.offsets;
@@ -696,15 +996,16 @@ bool make_tensor_map(CUtensorMap *m, CUtensorMapDataType dtype, CUtensorMapSwizz
     return r == CUDA_SUCCESS;
 }
 
-moe_status launch_grouped_gemm(Epi epi, const GemmArgs &a, cudaStream_t stream) {
-    if (a.cap_rows <= 0 || a.E <= 0) return MOE_OK;
+template <int EPI>
+moe_status launch_pair_or_single(const GemmArgs &a, cudaStream_t stream, bool pair) {
     CUtensorMap ma, mb;
+    const int clusters = pair ? pair_clusters<EPI>() : 0;
     const uint64_t adims[2] = {(uint64_t)a.Kd, (uint64_t)a.cap_rows};
     const uint64_t astr[1] = {(uint64_t)a.Kd * 2};
     const uint32_t abox[2] = {BK, BM};
     const uint64_t bdims[3] = {(uint64_t)a.Kd, (uint64_t)a.Nout, (uint64_t)a.E};
     const uint64_t bstr[2] = {(uint64_t)a.Kd * 2, (uint64_t)a.Kd * a.Nout * 2};
-    const uint32_t bbox[3] = {BK, BN, 1};
+    const uint32_t bbox[3] = {BK, clusters > 0 ? (uint32_t)(BN / 2) : (uint32_t)BN, 1};
     if (!make_tensor_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, CU_TENSOR_MAP_SWIZZLE_128B, a.a_img, 2,
                          adims, astr, abox))
         return MOE_ERR_CUDA;
@@ -712,10 +1013,16 @@ moe_status launch_grouped_gemm(Epi epi, const GemmArgs &a, cudaStream_t stream) 
                          bdims, bstr, bbox))
         return MOE_ERR_CUDA;
     const GemmDev d = gemm_dev(a);
+    if (clusters > 0) return launch_epi_pair<EPI>(ma, mb, d, clusters, stream);
+    return launch_epi<EPI>(ma, mb, d, stream);
+}
+
+moe_status launch_grouped_gemm(Epi epi, const GemmArgs &a, cudaStream_t stream, bool pair) {
+    if (a.cap_rows <= 0 || a.E <= 0) return MOE_OK;
     switch (epi) {
-        case Epi::S32: return launch_epi<(int)Epi::S32>(ma, mb, d, stream);
-        case Epi::SwiGLU: return launch_epi<(int)Epi::SwiGLU>(ma, mb, d, stream);
-        case Epi::DequantBF16: return launch_epi<(int)Epi::DequantBF16>(ma, mb, d, stream);
+        case Epi::S32: return launch_pair_or_single<(int)Epi::S32>(a, stream, pair);
+        case Epi::SwiGLU: return launch_pair_or_single<(int)Epi::SwiGLU>(a, stream, pair);
+        case Epi::DequantBF16: return launch_pair_or_single<(int)Epi::DequantBF16>(a, stream, pair);
     }
     return MOE_ERR_PARAM_INVALID;
 }

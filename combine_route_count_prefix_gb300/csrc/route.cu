@@ -547,7 +547,7 @@ moe_status launch_route_fused(RouteDev &r, int64_t chunks, int64_t *counts, int3
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         r.rows_final = 1;
-        const int tok = launch_begin("route_fused", stream);
+        const int tok = launch_begin("route_fused", stream, (unsigned)chunks);
         cudaError_t err = cudaLaunchKernelEx(&cfg, k_route_fused, r, chunks, counts, offsets,
                                              recv_cum, sched, route_row, assist);
         if (err == cudaSuccess) err = cudaGetLastError();

@@ -96,8 +96,12 @@ typedef struct moe_shape {
 } moe_shape;
 
 /* Grouped-GEMM kernels of the expert FFN.  Both give bit-identical results.
- *   LARGE: 128-row x 256-channel tiles on fp16 images of the weights; for
- *          many rows per expert, where the tensor cores bound the time.
+ *   LARGE: 128-row x 256-channel tiles on fp16 images of the weights, one
+ *          SM each; for many rows per expert, where the tensor cores bound
+ *          the time.
+ *   LARGE_PAIR: 256-row tiles, each computed by a pair of SMs (a cluster of
+ *          two CTAs sharing one 256-row MMA, B split between them).  Same
+ *          results; measured slower than LARGE on GB300, kept as an option.
  *   SMALL: the same tiles with the weights read as int8 (half the bytes)
  *          and widened to fp16 on chip, and only the rows present loaded; for
  *          few rows per expert, where reading the weights bounds the time
@@ -107,6 +111,7 @@ typedef struct moe_shape {
 #define MOE_FFN_PATH_AUTO 0
 #define MOE_FFN_PATH_LARGE 1
 #define MOE_FFN_PATH_SMALL 2
+#define MOE_FFN_PATH_LARGE_PAIR 3
 #define MOE_FFN_SMALL_ROWS_PER_EXPERT 32
 
 /* ------------------------------------------------------------------------
@@ -283,7 +288,7 @@ moe_status moe_stage_views_get(const moe_shape *shape, int for_layer, void *work
  * rows r in [offsets[e], offsets[e+1]).
  *   A int8 [rows, Kd]; W int8 [E, N, Kd]; C int32 [rows, N]; rows >= offsets[E].
  *   N % 8 == 0, Kd % 8 == 0 (Kd % 16 == 0 for the SMALL kernel).
- * path: MOE_FFN_PATH_* (AUTO: SMALL when rows <= 32 * E and Kd % 16 == 0).
+ * path: MOE_FFN_PATH_* (AUTO: SMALL when rows <= 32 * E and Kd % 16 == 0, else LARGE).
  * A is first converted into fp16 images in the workspace, and W into fp16
  * images (LARGE) or biased bytes (SMALL).
  * ------------------------------------------------------------------------ */

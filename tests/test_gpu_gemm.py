@@ -3,9 +3,10 @@ oracle ("PTO MegaMoE Dispatch + Combine Fusion Example", GMM1/GMM2: int8 x
 int8 -> int32 accumulator per local expert).  The tcgen05 path multiplies fp16
 images of the int8 values with fp32 accumulation and drains every 1024-deep K
 chunk to int32; the adversarial cases below reach the largest sums that
-chunking must keep exact.  Both kernels are checked: "large" (128-row x
-256-channel tiles on fp16 weight images) and "small" (an expert's rows against
-128-channel tiles of int8 weights widened on chip)."""
+chunking must keep exact.  All kernels are checked: "large" (128-row x
+256-channel tiles on fp16 weight images, one SM each), "large_pair" (256-row
+tiles on pairs of SMs) and "small" (int8 weights widened on chip, only the
+rows present loaded)."""
 import numpy as np
 import pytest
 import torch
@@ -25,7 +26,7 @@ def _offsets(counts):
     return np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
 
 
-PATHS = ["large", "small"]
+PATHS = ["large", "large_pair", "small"]
 
 
 @pytest.mark.parametrize("path", PATHS)

@@ -7,9 +7,9 @@ Bars (the oracle computes each stage from its own inputs only):
   q2 (second quantisation): within 1 LSB on at most 0.1% of elements;
   y: bit-exact on every row whose q2 and s2 match the oracle's;
   out: max 2 bf16 ulp and rel-L2 <= 1e-3.
-Each check runs on both grouped-GEMM kernels ("large": fp16 weight images in
-128 x 256 tiles; "small": int8 weights widened on chip, an expert's rows on the
-MMA's N side), and the two must agree with each other bit for bit.
+Each check runs on every grouped-GEMM kernel ("large": fp16 weight images in
+128 x 256 tiles, one SM each; "large_pair": 256 x 256 tiles on SM pairs;
+"small": int8 weights widened on chip), and they must agree bit for bit.
 """
 import numpy as np
 import pytest
@@ -32,7 +32,7 @@ def _device_weights(B, shape, W1, W2):
     return B.pack_weights(shape, dev(W1), dev(W2))
 
 
-PATHS = ["large", "small"]
+PATHS = ["large", "large_pair", "small"]
 
 
 def _stage_check(B, w, seed, path="auto"):
@@ -135,8 +135,9 @@ def test_layer_paths_agree_bit_for_bit(B):
                             for k in ("g", "q2", "s2", "y")})
     counts = res["large"]["counts"]
     assert counts.max() > 128 and (counts == 0).any() and ((counts > 0) & (counts < 16)).any()
-    for k in ("out", "g", "q2", "s2", "y"):
-        np.testing.assert_array_equal(res["large"][k], res["small"][k], err_msg=k)
+    for other in PATHS[1:]:
+        for k in ("out", "g", "q2", "s2", "y"):
+            np.testing.assert_array_equal(res["large"][k], res[other][k], err_msg=f"{other} {k}")
 
 
 def test_grouped_ffn_entry_on_dispatched_rows(B):
