@@ -14,23 +14,27 @@
 // CTA owns a contiguous block of tokens.  Warp 0 produces: its lanes load the
 // route rows, mask bits and probabilities of 32 tokens into registers (all
 // loads issued together, and the next batch's loads in flight while the
-// current batch is issued), and lane 0 walks the items: wait for a free stage,
-// write the item header (active slot count and their probabilities), arm the
-// stage's mbarrier with the byte count, and issue one bulk copy per active row
-// segment and one for the shared-expert segment.  Warps 1..8 consume a stage:
-// each thread owns up to two 16-byte vectors of the segment, accumulates the
-// rows from shared memory in slot order and stores the bf16 result.  Several
-// segments of ~7 KB per row are in flight per SM; the copies bypass the SM's
-// load-tracking limits and keep DRAM reads long and contiguous.  CTA b takes
-// tokens b, b + G, b + 2G, ... (G CTAs), so the tokens in flight at any time
-// are close together and so are their rows inside each expert's block.
+// current batch is issued); per item, lane 0 waits for a free stage, writes
+// the item header (active slot count and their probabilities) and arms the
+// stage's mbarrier with the byte count, and the lanes issue the item's bulk
+// copies in parallel, one active row segment each plus the shared-expert
+// segment.  Warps 1..15 consume a stage: each thread owns up to two 16-byte
+// vectors of the segment, loads the rows' vectors from shared memory, adds
+// them in slot order and stores the bf16 result.  Three stages of ~64 KB are
+// in flight per SM; the copies bypass the SM's load-tracking limits and keep
+// DRAM reads long and contiguous.  Measured on the decode workload: smaller
+// stages (more of them) and whole-row stages (one copy per row) are both
+// slower, so the time is set by the bytes in flight per SM against DRAM
+// latency under load.  CTA b takes tokens from the last one down in steps of
+// G (G CTAs), so the tokens in flight at any time are close together and so
+// are their rows inside each expert's block.
 #include "common.cuh"
 #include "ptx.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 15;   // with the producer, 16 warps: four per scheduler
 constexpr int kThreads = 32 * (1 + kConsumerWarps);
 constexpr int kVecsPerThread = 2;
 constexpr int kMaxSegVecs = kConsumerWarps * 32 * kVecsPerThread;   // 512 vectors = 8 KB
@@ -200,58 +204,66 @@ k_combine(CombineArgs a) {
         for (int64_t ib = 0; ib < ntok; ib += 32) {
             const bool more = ib + 32 < ntok;
             if (more) load_meta(ib + 32);          // in flight while this batch is issued
-            if (lane == 0 && ok) {
-                const int64_t ie = min(ib + 32, ntok);
-                for (int64_t ii = ib; ok && ii < ie; ++ii) {
-                    const int64_t tt = token_of(ii);
-                    const int32_t *rows = meta_row + buf * 32 * a.K + (ii - ib) * a.K;
-                    const float *ps = meta_p + buf * 32 * a.K + (ii - ib) * a.K;
-                    for (int seg = 0; seg < a.nseg; ++seg) {
-                        if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, a.status)) {
-                            ok = false;
-                            break;
-                        }
-                        const int64_t v0 = (int64_t)seg * a.seg_vecs;
-                        const uint32_t bytes = (uint32_t)(min((int64_t)a.seg_vecs, a.H8 - v0) * 16);
-                        ItemHdr *h = hdrs + stage;
-                        uint8_t *dst = bufs + stage * sbytes;
-                        int n = 0, nrow = 0;
-                        bool need_ori = false;
+            // Lane 0 waits for the stage and writes its header; the copies are
+            // issued by the lanes in parallel (a bulk copy costs its issuing
+            // thread a few hundred cycles): lane k < K the row of slot k if it
+            // has one, lane K the shared-expert row, lane K + 1 the token's
+            // own row when a copy expert needs it.
+            const int64_t ie = min(ib + 32, ntok);
+            for (int64_t ii = ib; ok && ii < ie; ++ii) {
+                const int64_t tt = token_of(ii);
+                const int32_t *rows = meta_row + buf * 32 * a.K + (ii - ib) * a.K;
+                const float *ps = meta_p + buf * 32 * a.K + (ii - ib) * a.K;
+                const int32_t my_code = lane < a.K ? rows[lane] : -1;
+                const uint32_t row_mask = __ballot_sync(kFull, my_code >= 0);
+                const int my_slot = __popc(row_mask & ((1u << lane) - 1u));
+                const int nrow = __popc(row_mask);
+                const bool need_ori = kSpecial && __any_sync(kFull, my_code == -3);
+                for (int seg = 0; seg < a.nseg; ++seg) {
+                    bool w = true;
+                    if (lane == 0) w = wait_bounded(&empty[stage], phase ^ 1u, abort_flag, a.status);
+                    if (!__shfl_sync(kFull, w, 0)) {
+                        ok = false;
+                        break;
+                    }
+                    const int64_t v0 = (int64_t)seg * a.seg_vecs;
+                    const uint32_t bytes = (uint32_t)(min((int64_t)a.seg_vecs, a.H8 - v0) * 16);
+                    ItemHdr *h = hdrs + stage;
+                    uint8_t *dst = bufs + stage * sbytes;
+                    if (lane == 0) {
+                        int n = 0;
                         if (kSpecial) {
+                            int nr = 0;
                             for (int k = 0; k < a.K; ++k) {
                                 const int32_t code = rows[k];
                                 if (code == -1) continue;
                                 h->p[n] = ps[k];
-                                if (code >= 0) h->src[n] = nrow++;
+                                if (code >= 0) h->src[n] = nr++;
                                 else if (code == -2) h->src[n] = -1;
-                                else { h->src[n] = a.K + 1; need_ori = true; }
+                                else h->src[n] = a.K + 1;
                                 ++n;
                             }
                         } else {
                             for (int k = 0; k < a.K; ++k)
                                 if (rows[k] >= 0) h->p[n++] = ps[k];
-                            nrow = n;
                         }
                         h->n = n;
                         const uint32_t loads =
                             (uint32_t)(nrow + (a.shared ? 1 : 0) + (need_ori ? 1 : 0));
                         mbar_arrive_expect_tx(&full[stage], loads * bytes);
-                        int jj = 0;
-                        for (int k = 0; k < a.K; ++k) {
-                            if (rows[k] < 0) continue;
-                            bulk_load(dst + (size_t)jj * a.seg_vecs * 16,
-                                      a.y + (int64_t)rows[k] * a.H8 + v0, bytes, &full[stage]);
-                            ++jj;
-                        }
-                        if (a.shared)
-                            bulk_load(dst + (size_t)a.K * a.seg_vecs * 16, a.shared + tt * a.H8 + v0,
-                                      bytes, &full[stage]);
-                        if (need_ori)
-                            bulk_load(dst + (size_t)(a.K + 1) * a.seg_vecs * 16,
-                                      a.ori_x + tt * a.H8 + v0, bytes, &full[stage]);
                         issued_phase[stage] = (int)phase;
-                        if (++stage == a.stages) { stage = 0; phase ^= 1u; }
                     }
+                    __syncwarp();
+                    if (my_code >= 0)
+                        bulk_load(dst + (size_t)my_slot * a.seg_vecs * 16,
+                                  a.y + (int64_t)my_code * a.H8 + v0, bytes, &full[stage]);
+                    else if (lane == a.K && a.shared)
+                        bulk_load(dst + (size_t)a.K * a.seg_vecs * 16, a.shared + tt * a.H8 + v0,
+                                  bytes, &full[stage]);
+                    else if (lane == a.K + 1 && need_ori)
+                        bulk_load(dst + (size_t)(a.K + 1) * a.seg_vecs * 16,
+                                  a.ori_x + tt * a.H8 + v0, bytes, &full[stage]);
+                    if (++stage == a.stages) { stage = 0; phase ^= 1u; }
                 }
             }
             ok = __shfl_sync(kFull, ok, 0);
@@ -298,15 +310,27 @@ k_combine(CombineArgs a) {
                         float acc[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+                        // up to 8 terms' vectors are loaded before any is used, so the
+                        // shared-memory latency is paid once per 8 terms
 #pragma unroll
-                        for (int j = 0; j < kMaxTopK; ++j) {
-                            if (j >= n) break;
-                            const bool zero = sl[j] < 0;
-                            float f[8];
-                            unpack8(lds128(src + ((size_t)(zero ? 0 : sl[j]) * a.seg_vecs + v) * 16), f);
+                        for (int j0 = 0; j0 < kMaxTopK; j0 += 8) {
+                            if (j0 >= n) break;
+                            uint4 raw[8];
 #pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                acc[i] = __fadd_rn(acc[i], __fmul_rn(pr[j], zero ? 0.0f : f[i]));
+                            for (int j = 0; j < 8; ++j)
+                                if (j0 + j < n)
+                                    raw[j] = lds128(src + ((size_t)(sl[j0 + j] < 0 ? 0 : sl[j0 + j]) *
+                                                               a.seg_vecs + v) * 16);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                if (j0 + j >= n) break;
+                                const bool zero = sl[j0 + j] < 0;
+                                float f[8];
+                                unpack8(raw[j], f);
+#pragma unroll
+                                for (int i = 0; i < 8; ++i)
+                                    acc[i] = __fadd_rn(acc[i], __fmul_rn(pr[j0 + j], zero ? 0.0f : f[i]));
+                            }
                         }
                         store_result(a, src, v, tt * a.H8 + v0 + v, acc);
                     }
@@ -318,12 +342,26 @@ k_combine(CombineArgs a) {
                         float acc[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-                        for (int jj = 0; jj < n; ++jj) {
-                            float f[8];
-                            unpack8(lds128(src + ((size_t)jj * a.seg_vecs + v) * 16), f);
-                            const float p = h->p[jj];
+                        for (int j0 = 0; j0 < n; j0 += 8) {
+                            // up to 8 rows' vectors loaded before any is used
+                            uint4 raw[8];
+                            float pj[8];
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(p, f[i]));
+                            for (int j = 0; j < 8; ++j) {
+                                if (j0 + j < n) {
+                                    raw[j] = lds128(src + ((size_t)(j0 + j) * a.seg_vecs + v) * 16);
+                                    pj[j] = h->p[j0 + j];
+                                }
+                            }
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                if (j0 + j >= n) break;
+                                float f[8];
+                                unpack8(raw[j], f);
+#pragma unroll
+                                for (int i = 0; i < 8; ++i)
+                                    acc[i] = __fadd_rn(acc[i], __fmul_rn(pj[j], f[i]));
+                            }
                         }
                         store_result(a, src, v, tt * a.H8 + v0 + v, acc);
                     }
@@ -343,6 +381,7 @@ moe_status launch_combine(const void *y, const int32_t *route_row, const float *
                           const void *ori_x, bool special, void *out, int64_t T, int64_t K,
                           int64_t H, int64_t cap_rows, int32_t *status, cudaStream_t stream) {
     if (T == 0) return MOE_OK;
+    const int64_t grid = T < num_sms() ? T : (int64_t)num_sms();
     CombineArgs a;
     a.y = static_cast<const uint4 *>(y);
     a.route_row = route_row;
@@ -368,7 +407,6 @@ moe_status launch_combine(const void *y, const int32_t *route_row, const float *
     a.stages = (int)(kSmemBudget / stage_bytes(a.slots, a.seg_vecs));
     if (a.stages > kMaxStages) a.stages = kMaxStages;
     if (a.stages < 2) a.stages = 2;
-    const int64_t grid = T < num_sms() ? T : (int64_t)num_sms();
     a.tokens_per_cta = 0;
     a.status = status;
     const size_t smem = smem_bytes(a.K, a.slots, a.stages, a.seg_vecs);
