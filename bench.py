@@ -68,7 +68,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ffn-path", default="auto", choices=["auto", "large", "small", "large_pair"],
                     help="grouped-GEMM kernels of the layer workloads (auto: small-batch "
-                         "kernels when T*K <= 32*E)")
+                         "kernels when T*K <= 64*E)")
     return ap.parse_args()
 
 
@@ -408,8 +408,8 @@ class LayerPath:
         w = self.w
         R = self.rows()
         H, N, Nh = w.hidden, w.ffn, w.ffn // 2
-        small = "gemm1_swiglu_w8" in prof
-        sfx = "_w8" if small else ("_pair" if "gemm1_swiglu_pair" in prof else "")
+        small = "gemm1_swiglu_small" in prof
+        sfx = "_small" if small else ("_pair" if "gemm1_swiglu_pair" in prof else "")
         g1, g2 = "gemm1_swiglu" + sfx, "gemm2_dequant" + sfx
         fl = {g1: 2.0 * R * H * N, g2: 2.0 * R * Nh * H}
         dom = max(fl, key=lambda k: prof.get(k, (1, 0.0))[1])

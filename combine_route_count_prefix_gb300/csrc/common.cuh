@@ -296,8 +296,10 @@ struct GemmArgs {
 moe_status launch_grouped_gemm(Epi epi, const GemmArgs &a, cudaStream_t stream,
                                bool pair = false);
 // The same GEMM for few rows per expert: the weights stream as biased bytes
-// (b_img, w + 128; W1 in launch_pack_w1_i8's row order) and are widened to
-// fp16 on chip; only the rows present are loaded.  Kd % 16 == 0.
+// (b_img, w + 128; W1 in launch_pack_w1_i8's row order), are widened on chip
+// into tensor memory and are the MMA's M side; the expert's rows are its N
+// side, only as many as present.  Kd % 16 == 0 (and Nout % 128 == 0 for the
+// SwiGLU epilogue).
 moe_status launch_grouped_gemm_small(Epi epi, const GemmArgs &a, cudaStream_t stream);
 
 }  // namespace moe

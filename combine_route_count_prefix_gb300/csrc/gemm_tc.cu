@@ -69,25 +69,6 @@ constexpr size_t P_SMEM_BYTES = P_RING_BYTES + 1024 + kBarrierBytes +
 static_assert(P_SMEM_BYTES <= 232448, "shared memory budget");
 static_assert((3 * P_STAGES + 5) * 8 + 16 <= (int)kBarrierBytes, "barriers");
 
-// The int8-weight variant (few rows per expert): weights stream as int8 into
-// their own ring and two converter warps widen each 256 x 64 tile to the fp16
-// B operand; the tile's rows come as 16-row boxes, only as many as it has.
-constexpr int W8_STAGES = 4;
-constexpr int W8_AB_STAGES = 3;
-constexpr int W8_BYTES = BN * BK;    // 16 KB int8 weight tile
-constexpr int BOX_ROWS = 16;
-constexpr int BOX_BYTES = BOX_ROWS * BK * 2;
-constexpr int CONV_WARPS = 2;
-constexpr int W8_CONV_WARP0 = 2;     // warps: loads, MMA, converters, epilogue
-constexpr int W8_EPI_WARP0 = W8_CONV_WARP0 + CONV_WARPS;
-constexpr int W8_THREADS = 32 * (W8_EPI_WARP0 + EPI_WARPS);
-constexpr int CONV_PIECES = W8_BYTES / 16 / (32 * CONV_WARPS);   // 16-byte pieces per thread
-constexpr size_t W8_RING_BYTES = (size_t)W8_AB_STAGES * STAGE_BYTES + (size_t)W8_STAGES * W8_BYTES;
-constexpr size_t W8_SMEM_BYTES = W8_RING_BYTES + 1024 + kBarrierBytes +
-                                 2 * (kMaxExperts + 1) * sizeof(int32_t);
-static_assert(W8_SMEM_BYTES <= 232448, "shared memory budget");
-static_assert((2 * W8_STAGES + 3 * W8_AB_STAGES + 5) * 8 + 16 <= (int)kBarrierBytes, "barriers");
-
 struct GemmDev {
     const int32_t *offsets;
     const int32_t *sched;
@@ -596,286 +577,6 @@ k_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
 
-// ---------------------------------------------------------------- int8-weight variant
-// 16 weights stored biased (w + 128, as bytes) -> 16 fp16 values w.  Byte u
-// goes into the low mantissa bits of the fp16 number 1024 (exponent 10, unit
-// spacing), giving 1024 + u exactly; subtracting 1152 leaves u - 128 = w, also
-// exactly.
-__device__ __forceinline__ uint32_t widen_biased_x2(uint32_t pair) {
-    uint32_t d;
-    // pair holds two halves 1024 + u; subtract 1152 = 0x6480 from each (exact)
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(pair), "r"(0x64806480u));
-    return d;
-}
-__device__ __forceinline__ void widen_biased_x16(const uint4 &in, uint4 &lo, uint4 &hi) {
-    // bytes 0, 1 of a word -> two halves (selector 0x4140), bytes 2, 3 -> 0x4342
-    lo.x = widen_biased_x2(__byte_perm(in.x, 0x64646464u, 0x4140));
-    lo.y = widen_biased_x2(__byte_perm(in.x, 0x64646464u, 0x4342));
-    lo.z = widen_biased_x2(__byte_perm(in.y, 0x64646464u, 0x4140));
-    lo.w = widen_biased_x2(__byte_perm(in.y, 0x64646464u, 0x4342));
-    hi.x = widen_biased_x2(__byte_perm(in.z, 0x64646464u, 0x4140));
-    hi.y = widen_biased_x2(__byte_perm(in.z, 0x64646464u, 0x4342));
-    hi.z = widen_biased_x2(__byte_perm(in.w, 0x64646464u, 0x4140));
-    hi.w = widen_biased_x2(__byte_perm(in.w, 0x64646464u, 0x4342));
-}
-
-// Warps (384 threads, one persistent CTA per SM; a multiple of four warps, so
-// that every scheduler holds three and the epilogue keeps 168 registers):
-//   warp 0      loads: one biased-int8 TMA weight tile (256 rows x 64) per
-//               k-block into a 4-stage ring, running 4 k-blocks ahead of the
-//               tile's rows (16-row TMA boxes, only as many as the tile has),
-//               which go into the operand stage once it is free
-//   warp 1      TMEM owner and MMA issuer, as in k_grouped_gemm
-//   warps 2..3  converters: widen the int8 tile into the stage's fp16 B operand
-//               (128-byte swizzle); each thread loads all its pieces first, so
-//               the shared-memory latency is paid once per k-block
-//   warps 4..11 epilogue, as in k_grouped_gemm
-template <int EPI>
-__global__ void __launch_bounds__(W8_THREADS, 1)
-k_grouped_gemm_w8(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
-                  GemmDev p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint8_t *ring8 = smem + (size_t)W8_AB_STAGES * STAGE_BYTES;
-    uint64_t *w8_full = reinterpret_cast<uint64_t *>(smem + W8_RING_BYTES);
-    uint64_t *w8_empty = w8_full + W8_STAGES;
-    uint64_t *a_full = w8_empty + W8_STAGES;
-    uint64_t *b_full = a_full + W8_AB_STAGES;
-    uint64_t *ab_empty = b_full + W8_AB_STAGES;
-    uint64_t *acc_full = ab_empty + W8_AB_STAGES;
-    uint64_t *acc_empty = acc_full + 2;
-    uint64_t *drain = acc_empty + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    int32_t *s_sched = reinterpret_cast<int32_t *>(smem + W8_RING_BYTES + kBarrierBytes);
-    int32_t *s_off = s_sched + (kMaxExperts + 1);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < W8_STAGES; ++s) {
-            mbar_init(&w8_full[s], 1);
-            mbar_init(&w8_empty[s], CONV_WARPS);
-        }
-        for (int s = 0; s < W8_AB_STAGES; ++s) {
-            mbar_init(&a_full[s], 1);
-            mbar_init(&b_full[s], CONV_WARPS);
-            mbar_init(&ab_empty[s], 1);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], EPI_WARPS);
-        }
-        mbar_init(drain, 1);
-        *abort_flag = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    if (warp == 0 && lane == 0) {
-        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmW) : "memory");
-    }
-    pdl_wait();   // everything below may read what earlier kernels wrote
-    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
-        s_sched[i] = p.sched[i];
-        s_off[i] = p.offsets[i];
-    }
-    if (warp == 1) {
-        tmem_alloc(tmem_slot, TMEM_COLS);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
-    const int64_t total_tiles = (int64_t)s_sched[p.E] * p.n_blocks;
-    const int num_chunks = (p.num_kb + CHUNK_KB - 1) / CHUNK_KB;
-
-    if (warp == 0) {
-        if (lane == 0) {
-            // ------------------------------------------------ loads
-            // weight tiles: position (wtile, wkb), W8_STAGES k-blocks ahead of the rows
-            int s8 = 0;
-            uint32_t ph8 = 0;
-            int w8_issued[W8_STAGES];
-#pragma unroll
-            for (int s = 0; s < W8_STAGES; ++s) w8_issued[s] = -1;
-            int64_t wtile = blockIdx.x;
-            int wkb = 0;
-            Tile wt = decode_tile(wtile, p.n_blocks, p.E, s_sched, s_off);
-            bool ok = true;
-            auto issue_w8 = [&]() {
-                if (!ok || wtile >= total_tiles) return;
-                if (!wait_bounded(&w8_empty[s8], ph8 ^ 1u, abort_flag, p.status)) { ok = false; return; }
-                mbar_arrive_expect_tx(&w8_full[s8], W8_BYTES);
-                tma_load_3d(ring8 + (size_t)s8 * W8_BYTES, &tmW, &w8_full[s8], wkb * BK, wt.nb * BN,
-                            wt.e);
-                w8_issued[s8] = (int)ph8;
-                if (++s8 == W8_STAGES) { s8 = 0; ph8 ^= 1u; }
-                if (++wkb == p.num_kb) {
-                    wkb = 0;
-                    wtile += gridDim.x;
-                    if (wtile < total_tiles) wt = decode_tile(wtile, p.n_blocks, p.E, s_sched, s_off);
-                }
-            };
-            for (int i = 0; i < W8_STAGES; ++i) issue_w8();
-            int sa = 0;
-            uint32_t pha = 0;
-            int a_issued[W8_AB_STAGES];
-#pragma unroll
-            for (int s = 0; s < W8_AB_STAGES; ++s) a_issued[s] = -1;
-            for (int64_t tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-                const Tile t = decode_tile(tile, p.n_blocks, p.E, s_sched, s_off);
-                const int nbox = (t.rows + BOX_ROWS - 1) / BOX_ROWS;
-                for (int kb = 0; ok && kb < p.num_kb; ++kb) {
-                    if (!wait_bounded(&ab_empty[sa], pha ^ 1u, abort_flag, p.status)) { ok = false; break; }
-                    // the rows present; rows past them in the stage are stale and
-                    // only reach accumulator lanes that are never stored
-                    uint8_t *dst = smem + (size_t)sa * STAGE_BYTES;
-                    mbar_arrive_expect_tx(&a_full[sa], (uint32_t)(nbox * BOX_BYTES));
-                    for (int i = 0; i < nbox; ++i)
-                        tma_load_2d(dst + i * BOX_BYTES, &tmA, &a_full[sa], kb * BK,
-                                    t.row0 + i * BOX_ROWS);
-                    a_issued[sa] = (int)pha;
-                    if (++sa == W8_AB_STAGES) { sa = 0; pha ^= 1u; }
-                    issue_w8();
-                }
-            }
-            // every load issued must have landed before the CTA may exit
-            for (int s = 0; s < W8_STAGES; ++s)
-                if (w8_issued[s] >= 0)
-                    wait_bounded(&w8_full[s], (uint32_t)w8_issued[s], abort_flag, p.status, false);
-            for (int s = 0; s < W8_AB_STAGES; ++s)
-                if (a_issued[s] >= 0)
-                    wait_bounded(&a_full[s], (uint32_t)a_issued[s], abort_flag, p.status, false);
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------ MMA issuer
-            constexpr uint32_t idesc = idesc_f16(BM, BN);
-            int stage = 0;
-            uint32_t phase = 0;
-            int accb = 0;
-            uint32_t acc_phase = 0;
-            bool ok = true;
-            for (int64_t tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-                for (int kb0 = 0; ok && kb0 < p.num_kb; kb0 += CHUNK_KB) {
-                    if (!wait_bounded(&acc_empty[accb], acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + (uint32_t)(accb * BN);
-                    const int kb1 = min(kb0 + CHUNK_KB, p.num_kb);
-                    for (int kb = kb0; kb < kb1; ++kb) {
-                        if (!wait_bounded(&b_full[stage], phase, abort_flag, p.status) ||
-                            !wait_bounded(&a_full[stage], phase, abort_flag, p.status)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t a_addr = smem_u32(smem + (size_t)stage * STAGE_BYTES);
-                        const uint32_t b_addr = a_addr + A_BYTES;
-#pragma unroll
-                        for (int k = 0; k < BK / 16; ++k)
-                            mma_f16(d_tmem, desc_sw128(a_addr + 32 * k), desc_sw128(b_addr + 32 * k),
-                                    idesc, (kb > kb0 || k > 0) ? 1u : 0u);
-                        mma_commit(&ab_empty[stage]);
-                        if (++stage == W8_AB_STAGES) { stage = 0; phase ^= 1u; }
-                    }
-                    if (!ok) break;
-                    mma_commit(&acc_full[accb]);
-                    if (++accb == 2) { accb = 0; acc_phase ^= 1u; }
-                }
-            }
-            mma_commit(drain);
-            wait_bounded(drain, 0, abort_flag, p.status, false);
-        }
-    } else if (warp < W8_EPI_WARP0) {
-        // ---------------------------------------------------- converters
-        const int ct = threadIdx.x - 32 * W8_CONV_WARP0;   // 0..63
-        // piece i of this thread: int8 row (ct >> 2) + 16 i, 16-byte column ct & 3;
-        // in the fp16 tile its two 16-byte units land at (2 col, 2 col + 1) ^ (row % 8),
-        // and row % 8 = (ct >> 2) % 8 for every i
-        const int r0 = ct >> 2, col = ct & 3;
-        const int src_off = r0 * 64 + col * 16;
-        const int dst_off = r0 * 128;
-        const int u_lo = ((2 * col) ^ (r0 & 7)) << 4, u_hi = ((2 * col + 1) ^ (r0 & 7)) << 4;
-        int s8 = 0, sa = 0;
-        uint32_t ph8 = 0, pha = 0;
-        bool ok = true;
-        for (int64_t tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-            for (int kb = 0; kb < p.num_kb; ++kb) {
-                const bool w = wait_bounded(&w8_full[s8], ph8, abort_flag, p.status) &&
-                               wait_bounded(&ab_empty[sa], pha ^ 1u, abort_flag, p.status);
-                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-                const uint8_t *src = ring8 + (size_t)s8 * W8_BYTES + src_off;
-                uint8_t *dst = smem + (size_t)sa * STAGE_BYTES + A_BYTES + dst_off;
-                uint4 v[CONV_PIECES];
-#pragma unroll
-                for (int i = 0; i < CONV_PIECES; ++i)
-                    v[i] = *reinterpret_cast<const uint4 *>(src + i * 16 * 64);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&w8_empty[s8]);   // the int8 tile has been read
-#pragma unroll
-                for (int i = 0; i < CONV_PIECES; ++i) {
-                    uint4 lo, hi;
-                    widen_biased_x16(v[i], lo, hi);
-                    *reinterpret_cast<uint4 *>(dst + i * 16 * 128 + u_lo) = lo;
-                    *reinterpret_cast<uint4 *>(dst + i * 16 * 128 + u_hi) = hi;
-                }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // for the MMA's reads
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&b_full[sa]);
-                if (++s8 == W8_STAGES) { s8 = 0; ph8 ^= 1u; }
-                if (++sa == W8_AB_STAGES) { sa = 0; pha ^= 1u; }
-            }
-        }
-    } else {
-        // ---------------------------------------------------- epilogue warps
-        const int q = warp & 3;                       // TMEM lane quadrant this warp may read
-        const int hf = (warp - W8_EPI_WARP0) >> 2;    // column half of the tile
-        const int rloc = q * 32 + lane;
-        int accb = 0;
-        uint32_t acc_phase = 0;
-        for (int64_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-            const Tile t = decode_tile(tile, p.n_blocks, p.E, s_sched, s_off);
-            int32_t acc[128];
-            bool ok = true;
-            const bool rows_here = q * 32 < t.rows;   // warp-uniform: this quadrant holds rows
-            for (int c = 0; c < num_chunks; ++c) {
-                bool w = wait_bounded(&acc_full[accb], acc_phase, abort_flag, p.status);
-                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-                tc_fence_after();
-                if (rows_here) {
-                    const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) +
-                                           (uint32_t)(accb * BN + hf * 128);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        uint32_t r[32];
-                        tmem_ld32(taddr + 32 * j, r);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const int v = __float2int_rn(__uint_as_float(r[i]));
-                            acc[32 * j + i] = (c == 0) ? v : acc[32 * j + i] + v;
-                        }
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&acc_empty[accb]);
-                if (++accb == 2) { accb = 0; acc_phase ^= 1u; }
-            }
-            if (!ok) break;
-            if (rows_here && rloc < t.rows && (int64_t)t.row0 + rloc < p.cap_rows)
-                epilogue_store<EPI>(p, t, t.row0 + rloc, hf, acc);
-        }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
-}
-
 // ---------------------------------------------------------------- host side
 template <int EPI>
 moe_status launch_epi(const CUtensorMap &ma, const CUtensorMap &mb, const GemmDev &d,
@@ -889,22 +590,6 @@ moe_status launch_epi(const CUtensorMap &ma, const CUtensorMap &mb, const GemmDe
     }
     const char *names[3] = {"gemm_s32", "gemm1_swiglu", "gemm2_dequant"};
     MOE_LAUNCH(names[EPI], k_grouped_gemm<EPI>, num_sms(), THREADS, SMEM_BYTES, stream, ma, mb, d);
-    return MOE_OK;
-}
-
-template <int EPI>
-moe_status launch_epi_w8(const CUtensorMap &ma, const CUtensorMap &mw, const GemmDev &d,
-                         cudaStream_t stream) {
-    static bool configured = false;
-    if (!configured) {
-        if (cudaFuncSetAttribute(k_grouped_gemm_w8<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)W8_SMEM_BYTES) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        configured = true;
-    }
-    const char *names[3] = {"gemm_s32_w8", "gemm1_swiglu_w8", "gemm2_dequant_w8"};
-    MOE_LAUNCH(names[EPI], k_grouped_gemm_w8<EPI>, num_sms(), W8_THREADS, W8_SMEM_BYTES, stream, ma,
-               mw, d);
     return MOE_OK;
 }
 
@@ -1023,31 +708,6 @@ moe_status launch_grouped_gemm(Epi epi, const GemmArgs &a, cudaStream_t stream, 
         case Epi::S32: return launch_pair_or_single<(int)Epi::S32>(a, stream, pair);
         case Epi::SwiGLU: return launch_pair_or_single<(int)Epi::SwiGLU>(a, stream, pair);
         case Epi::DequantBF16: return launch_pair_or_single<(int)Epi::DequantBF16>(a, stream, pair);
-    }
-    return MOE_ERR_PARAM_INVALID;
-}
-
-moe_status launch_grouped_gemm_small(Epi epi, const GemmArgs &a, cudaStream_t stream) {
-    if (a.cap_rows <= 0 || a.E <= 0) return MOE_OK;
-    if (a.Kd % 16 != 0) return MOE_ERR_SHAPE;   // int8 rows must be 16-byte strided for TMA
-    CUtensorMap ma, mw;
-    const uint64_t adims[2] = {(uint64_t)a.Kd, (uint64_t)a.cap_rows};
-    const uint64_t astr[1] = {(uint64_t)a.Kd * 2};
-    const uint32_t abox[2] = {BK, BOX_ROWS};
-    const uint64_t wdims[3] = {(uint64_t)a.Kd, (uint64_t)a.Nout, (uint64_t)a.E};
-    const uint64_t wstr[2] = {(uint64_t)a.Kd, (uint64_t)a.Kd * a.Nout};
-    const uint32_t wbox[3] = {BK, BN, 1};
-    if (!make_tensor_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, CU_TENSOR_MAP_SWIZZLE_128B, a.a_img, 2,
-                         adims, astr, abox))
-        return MOE_ERR_CUDA;
-    if (!make_tensor_map(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_SWIZZLE_NONE, a.b_img, 3,
-                         wdims, wstr, wbox))
-        return MOE_ERR_CUDA;
-    const GemmDev d = gemm_dev(a);
-    switch (epi) {
-        case Epi::S32: return launch_epi_w8<(int)Epi::S32>(ma, mw, d, stream);
-        case Epi::SwiGLU: return launch_epi_w8<(int)Epi::SwiGLU>(ma, mw, d, stream);
-        case Epi::DequantBF16: return launch_epi_w8<(int)Epi::DequantBF16>(ma, mw, d, stream);
     }
     return MOE_ERR_PARAM_INVALID;
 }

@@ -438,8 +438,12 @@ __global__ void k_pack_w1(const int8_t *__restrict__ w1, uint4 *__restrict__ out
     }
 }
 
-// W1 [E, N, H] -> biased bytes (w + 128) [E, N, H] with k_pack_w1's row order,
-// the weight operand of the int8-weight GEMM.
+// W1 [E, N, H] -> biased bytes (w + 128) [E, N, H] with rows reordered for the
+// small-batch GEMM: packed row 128b + 32q + l (b = 128-channel block, q = TMEM
+// lane quadrant) holds
+//   l <  16: SiLU-half channel         64b + 16q + l
+//   l >= 16: multiplier channel  N/2 + 64b + 16q + (l - 16)
+// so the two halves of a SwiGLU pair sit 16 TMEM lanes apart in one warp.
 __global__ void k_pack_w1_i8(const int8_t *__restrict__ w1, uint4 *__restrict__ out, int64_t E,
                              int64_t N, int64_t H) {
     pdl_wait();
@@ -447,12 +451,13 @@ __global__ void k_pack_w1_i8(const int8_t *__restrict__ w1, uint4 *__restrict__ 
     const int64_t total = E * N * H16;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
-        int64_t col16 = i % H16;
-        int64_t prow = (i / H16) % N;
-        int64_t e = i / (H16 * N);
-        int64_t b = prow / 256, within = prow % 256, h = within / 128, ii = within % 128;
-        int64_t src_row = (ii < 64) ? (128 * b + 64 * h + ii) : (N / 2 + 128 * b + 64 * h + (ii - 64));
-        uint4 v = *reinterpret_cast<const uint4 *>(w1 + (e * N + src_row) * H + col16 * 16);
+        const int64_t col16 = i % H16;
+        const int64_t prow = (i / H16) % N;
+        const int64_t e = i / (H16 * N);
+        const int64_t b = prow / 128, qq = (prow % 128) / 32, l = prow % 32;
+        const int64_t j = 64 * b + 16 * qq + (l & 15);
+        const int64_t src_row = l < 16 ? j : N / 2 + j;
+        const uint4 v = *reinterpret_cast<const uint4 *>(w1 + (e * N + src_row) * H + col16 * 16);
         out[i] = make_uint4(v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u,
                             v.w ^ 0x80808080u);
     }

@@ -102,17 +102,17 @@ typedef struct moe_shape {
  *   LARGE_PAIR: 256-row tiles, each computed by a pair of SMs (a cluster of
  *          two CTAs sharing one 256-row MMA, B split between them).  Same
  *          results; measured slower than LARGE on GB300, kept as an option.
- *   SMALL: the same tiles with the weights read as int8 (half the bytes)
- *          and widened to fp16 on chip, and only the rows present loaded; for
- *          few rows per expert, where reading the weights bounds the time
- *          ("PTO MegaMoE ...", Supported Cases: the M sweep from 16 tokens
- *          per rank).
+ *   SMALL: the weights read as int8 (half the bytes), widened on chip into
+ *          tensor memory as the MMA's 128-row side, against the expert's rows
+ *          (only those present); for few rows per expert, where reading the
+ *          weights bounds the time ("PTO MegaMoE ...", Supported Cases: the M
+ *          sweep from 16 tokens per rank).
  *   AUTO:  SMALL when T*K <= MOE_FFN_SMALL_ROWS_PER_EXPERT * E, else LARGE. */
 #define MOE_FFN_PATH_AUTO 0
 #define MOE_FFN_PATH_LARGE 1
 #define MOE_FFN_PATH_SMALL 2
 #define MOE_FFN_PATH_LARGE_PAIR 3
-#define MOE_FFN_SMALL_ROWS_PER_EXPERT 32
+#define MOE_FFN_SMALL_ROWS_PER_EXPERT 64
 
 /* ------------------------------------------------------------------------
  * Dispatch.
@@ -203,7 +203,8 @@ moe_status moe_combine(const moe_shape *shape, const void *expand_x, const int32
  * Packing, done once per model, writes both kernels' operand formats into
  * each packed buffer: fp16 images of the int8 values (exact) for the LARGE
  * path, followed by byte copies biased by +128 for the SMALL path; W1's rows
- * are reordered in both so that every GEMM1 tile holds complete SwiGLU pairs.
+ * are reordered in each (differently) so that every GEMM1 tile holds complete
+ * SwiGLU pairs.
  * Packed sizes: E*N*H*3 and E*H*(N/2)*3 bytes.  The packed buffers are opaque.
  * ------------------------------------------------------------------------ */
 moe_status moe_packed_weight_bytes(const moe_shape *shape, size_t *w1_bytes, size_t *w2_bytes);
@@ -288,7 +289,7 @@ moe_status moe_stage_views_get(const moe_shape *shape, int for_layer, void *work
  * rows r in [offsets[e], offsets[e+1]).
  *   A int8 [rows, Kd]; W int8 [E, N, Kd]; C int32 [rows, N]; rows >= offsets[E].
  *   N % 8 == 0, Kd % 8 == 0 (Kd % 16 == 0 for the SMALL kernel).
- * path: MOE_FFN_PATH_* (AUTO: SMALL when rows <= 32 * E and Kd % 16 == 0, else LARGE).
+ * path: MOE_FFN_PATH_* (AUTO: SMALL when rows <= 64 * E and Kd % 16 == 0, else LARGE).
  * A is first converted into fp16 images in the workspace, and W into fp16
  * images (LARGE) or biased bytes (SMALL).
  * ------------------------------------------------------------------------ */
