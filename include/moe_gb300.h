@@ -102,6 +102,10 @@ typedef struct moe_shape {
  *   LARGE_PAIR: 256-row tiles, each computed by a pair of SMs (a cluster of
  *          two CTAs sharing one 256-row MMA, B split between them).  Same
  *          results; measured slower than LARGE on GB300, kept as an option.
+ *   FUSED: LARGE's tiles with GMM1, the second quantisation and GMM2 in one
+ *          persistent kernel; GMM2 starts on an m-block as soon as its rows
+ *          are quantised ("PTO MegaMoE ...", the quantisation overlapping GMM2).
+ *          Same results; measured slower than LARGE, kept as an option.
  *   SMALL: the weights read as int8 (half the bytes), widened on chip into
  *          tensor memory as the MMA's 128-row side, against the expert's rows
  *          (only those present); for few rows per expert, where reading the
@@ -112,6 +116,7 @@ typedef struct moe_shape {
 #define MOE_FFN_PATH_LARGE 1
 #define MOE_FFN_PATH_SMALL 2
 #define MOE_FFN_PATH_LARGE_PAIR 3
+#define MOE_FFN_PATH_FUSED 4
 #define MOE_FFN_SMALL_ROWS_PER_EXPERT 64
 
 /* ------------------------------------------------------------------------

@@ -55,7 +55,7 @@ def test_workspace_sizes_and_shape_checks(B):
                 B.make_shape(16, 2, 128, 8, 2, 300),   # N % 256
                 B.make_shape(16, 2, 128, 8, 2, 256, ffn_path="large")]:
         if bad.ffn_path:
-            bad.ffn_path = 4                           # no such kernel choice
+            bad.ffn_path = 5                           # no such kernel choice
         with pytest.raises(B.MoeError):
             B.layer_workspace_size(bad) if bad.ffn else B.dispatch_workspace_size(bad)
 

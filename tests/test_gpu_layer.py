@@ -9,7 +9,8 @@ Bars (the oracle computes each stage from its own inputs only):
   out: max 2 bf16 ulp and rel-L2 <= 1e-3.
 Each check runs on every grouped-GEMM kernel ("large": fp16 weight images in
 128 x 256 tiles, one SM each; "large_pair": 256 x 256 tiles on SM pairs;
-"small": int8 weights widened on chip), and they must agree bit for bit.
+"small": int8 weights widened on chip; "fused": large tiles with GMM1, the
+second quantisation and GMM2 in one kernel), and they must agree bit for bit.
 """
 import numpy as np
 import pytest
@@ -32,7 +33,7 @@ def _device_weights(B, shape, W1, W2):
     return B.pack_weights(shape, dev(W1), dev(W2))
 
 
-PATHS = ["large", "large_pair", "small"]
+PATHS = ["large", "large_pair", "small", "fused"]
 
 
 def _stage_check(B, w, seed, path="auto"):
