@@ -68,7 +68,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ffn-path", default="auto", choices=["auto", "large", "small", "large_pair", "fused"],
                     help="grouped-GEMM kernels of the layer workloads (auto: small-batch "
-                         "kernels when T*K <= 64*E)")
+                         "kernels when T*K <= 32*E)")
     return ap.parse_args()
 
 

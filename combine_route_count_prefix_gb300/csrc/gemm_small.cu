@@ -18,10 +18,13 @@
 // Kernel shape (one persistent CTA per SM, 16 warps):
 //   warp 0       weight producer: one biased-int8 TMA tile (128 rows x 128,
 //                128-byte swizzle) per k-block into a 4-stage ring
-//   warp 1       TMEM owner (512 columns: two 128-column accumulators and four
-//                64-column A stages) and MMA issuer (8 MMAs of K = 16 per
-//                k-block: one issuing thread spends ~90 cycles per MMA, so a
-//                128-deep k-block halves the barrier work per weight byte)
+//   warps 1, 3   MMA issuers: one thread spends ~130 cycles issuing each
+//                tcgen05.mma whatever its N, and two threads issue at twice
+//                the rate, so the 8 MMAs (K = 16) of a 128-deep k-block are
+//                split: issuer i takes K [64 i, 64 i + 64) into its own pair of
+//                64-column accumulators (the sums are exact integers, so how
+//                they are split and added does not matter); warp 1 also owns
+//                TMEM (512 columns: 4 accumulators and four 64-column A stages)
 //   warp 2       row producer: the tile's rows (fp16 images, 128-byte swizzle)
 //                as 16-row TMA boxes, two 64-wide halves per k-block, into a
 //                4-stage ring
@@ -29,9 +32,10 @@
 //                tile (128 values) and writes it to its own TMEM lane (64
 //                columns, two fp16 values each)
 //   warps 8..15  epilogue: warp % 4 selects the TMEM lane quadrant (32 output
-//                channels), (warp - 8) / 4 the half of the tile's rows
-// Tiles are (expert, 128-row block of its rows, 128-channel block), channel
-// block fastest.  Every wait is bounded (about two seconds) and sets
+//                channels), (warp - 8) / 4 the half of the tile's rows; adds
+//                the two issuers' accumulators
+// Tiles are (expert, 64-row block of its rows, 128-channel block), channel
+// block fastest; the 64-row block schedule is computed here from the offsets.  Every wait is bounded (about two seconds) and sets
 // MOE_DEV_TIMEOUT.
 #include "common.cuh"
 #include "tcgen05.cuh"
@@ -44,13 +48,13 @@ namespace {
 using namespace tc;
 
 constexpr int BW = 128;                  // weight rows (output channels) per tile = MMA M
-constexpr int TB = kGemmBM;              // token rows per tile (the m-block schedule's block)
+constexpr int TB = 64;                   // token rows per tile
 constexpr int BK = 128;                  // k-block
 constexpr int BKH = 64;                  // one 128-byte swizzle atom of fp16 rows
 constexpr int S8 = 4;                    // int8 weight ring stages
 constexpr int SA = 4;                    // operand stages: TMEM A + shared-memory rows
 constexpr int W8_BYTES = BW * BK;        // 16 KB
-constexpr int B_HALF_BYTES = TB * BKH * 2;   // 16 KB: one 64-wide half of the rows
+constexpr int B_HALF_BYTES = TB * BKH * 2;   // 8 KB: one 64-wide half of the rows
 constexpr int B_BYTES = 2 * B_HALF_BYTES;
 constexpr int BOX_ROWS = 16;
 constexpr int BOX_BYTES = BOX_ROWS * BKH * 2;
@@ -61,12 +65,16 @@ constexpr int EPI_WARPS = 8;
 constexpr int EPI_COLS = TB / 2;         // tile rows per epilogue warp
 constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t A_COL0 = 2 * TB;      // after the two accumulators
+constexpr int ISSUERS = 2;
+constexpr uint32_t ACC_COLS = 128;         // per issuer: two accumulators of TB columns
+constexpr uint32_t A_COL0 = ISSUERS * ACC_COLS;
 constexpr uint32_t A_STAGE_COLS = BK / 2;
 constexpr size_t kBarrierBytes = 512;
 constexpr size_t RING_BYTES = (size_t)SA * B_BYTES + (size_t)S8 * W8_BYTES;
 constexpr size_t SMEM_BYTES = RING_BYTES + 1024 + kBarrierBytes + 2 * (kMaxExperts + 1) * sizeof(int32_t);
 static_assert(A_COL0 + SA * A_STAGE_COLS <= TMEM_COLS, "TMEM budget");
+static_assert(2 * TB <= (int)ACC_COLS, "accumulators");
+static_assert(BK / 16 == 4 * ISSUERS, "k-steps split between the issuers");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert((2 * S8 + 3 * SA + 5) * 8 + 16 <= (int)kBarrierBytes, "barrier area");
 
@@ -195,13 +203,13 @@ k_gemm_small(const __grid_constant__ CUtensorMap tmRows, const __grid_constant__
         for (int s = 0; s < SA; ++s) {
             mbar_init(&a_full[s], 4);
             mbar_init(&b_full[s], 1);
-            mbar_init(&ab_empty[s], 1);
+            mbar_init(&ab_empty[s], ISSUERS);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_full[b], ISSUERS);
             mbar_init(&acc_empty[b], EPI_WARPS);
         }
-        mbar_init(drain, 1);
+        mbar_init(drain, ISSUERS);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -210,9 +218,24 @@ k_gemm_small(const __grid_constant__ CUtensorMap tmRows, const __grid_constant__
         asm volatile("prefetch.tensormap [%0];" ::"l"(&tmW) : "memory");
     }
     pdl_wait();   // everything below may read what earlier kernels wrote
-    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
-        s_sched[i] = p.sched[i];
-        s_off[i] = p.offsets[i];
+    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s_off[i] = p.offsets[i];
+    __syncthreads();
+    if (warp == 0) {
+        // s_sched[e] = TB-row blocks of the experts before e (warp scan)
+        int carry = 0;
+        for (int base = 0; base < p.E; base += 32) {
+            const int e = base + lane;
+            const int c = e < p.E ? (s_off[e + 1] - s_off[e] + TB - 1) / TB : 0;
+            int x = c;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, d);
+                if (lane >= d) x += y;
+            }
+            if (e < p.E) s_sched[e] = carry + x - c;
+            carry += __shfl_sync(0xffffffffu, x, 31);
+        }
+        if (lane == 0) s_sched[p.E] = carry;
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, TMEM_COLS);
@@ -323,9 +346,10 @@ k_gemm_small(const __grid_constant__ CUtensorMap tmRows, const __grid_constant__
                 if (++sa == SA) { sa = 0; pha ^= 1u; }
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == 3) {
         if (lane == 0) {
-            // ------------------------------------------------ MMA issuer
+            // ------------------------------------------------ MMA issuers
+            const int is = warp >> 1;   // 0 or 1: K [64 is, 64 is + 64) of every k-block
             int stage = 0;
             uint32_t phase = 0;
             int accb = 0;
@@ -338,7 +362,7 @@ k_gemm_small(const __grid_constant__ CUtensorMap tmRows, const __grid_constant__
                 for (int kb0 = 0; ok && kb0 < p.num_kb; kb0 += CHUNK_KB) {
                     if (!wait_bounded(&acc_empty[accb], acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + (uint32_t)(accb * TB);
+                    const uint32_t d_tmem = tmem_base + (uint32_t)(is * ACC_COLS + accb * TB);
                     const int kb1 = min(kb0 + CHUNK_KB, p.num_kb);
                     for (int kb = kb0; kb < kb1; ++kb) {
                         if (!wait_bounded(&a_full[stage], phase, abort_flag, p.status) ||
@@ -350,9 +374,9 @@ k_gemm_small(const __grid_constant__ CUtensorMap tmRows, const __grid_constant__
                         const uint32_t a_tmem = tmem_base + A_COL0 + (uint32_t)stage * A_STAGE_COLS;
                         const uint32_t b_addr = smem_u32(ringB + (size_t)stage * B_BYTES);
 #pragma unroll
-                        for (int k = 0; k < BK / 16; ++k)   // K = 16: 8 TMEM columns, 32 bytes of a row
-                            mma_f16_ta(d_tmem, a_tmem + 8 * k,
-                                       desc_sw128(b_addr + (k / 4) * B_HALF_BYTES + 32 * (k % 4)), idesc,
+                        for (int k = 0; k < 4; ++k)   // K = 16: 8 TMEM columns, 32 bytes of a row
+                            mma_f16_ta(d_tmem, a_tmem + 32 * is + 8 * k,
+                                       desc_sw128(b_addr + is * B_HALF_BYTES + 32 * k), idesc,
                                        (kb > kb0 || k > 0) ? 1u : 0u);
                         mma_commit(&ab_empty[stage]);
                         if (++stage == SA) { stage = 0; phase ^= 1u; }
@@ -387,12 +411,15 @@ k_gemm_small(const __grid_constant__ CUtensorMap tmRows, const __grid_constant__
 #pragma unroll
                 for (int j = 0; j < EPI_COLS / 32; ++j) {
                     if (j < nj) {
-                        uint32_t r[32];
-                        tmem_ld32(taddr + 32 * j, r);
-                        tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            acc[32 * j + i] += __float2int_rn(__uint_as_float(r[i]));
+                        for (int is = 0; is < ISSUERS; ++is) {
+                            uint32_t r[32];
+                            tmem_ld32(taddr + is * ACC_COLS + 32 * j, r);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                acc[32 * j + i] += __float2int_rn(__uint_as_float(r[i]));
+                        }
                     }
                 }
                 tc_fence_before();

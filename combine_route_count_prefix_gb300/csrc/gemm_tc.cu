@@ -45,23 +45,30 @@ using namespace tc;
 
 constexpr int BM = kGemmBM;          // 128
 constexpr int BN = kGemmBN;          // 256
-constexpr int BK = 64;               // fp16 elements per k-block = one 128-byte swizzle row
-constexpr int STAGES = 4;
+#ifndef MOE_GEMM_BK
+#define MOE_GEMM_BK 64
+#endif
+// k-block depth: 64 fp16 (128-byte rows, 128-byte swizzle, 4 stages of 48 KB)
+// or 32 fp16 (64-byte rows, 64-byte swizzle, 9 stages of 24 KB)
+constexpr int BK = MOE_GEMM_BK;
+static_assert(BK == 64 || BK == 32, "k-block depth");
+constexpr int STAGES = BK == 64 ? 4 : 9;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int CHUNK_KB = 16;         // 16 x 64 = 1024-deep exact chunk
+constexpr int CHUNK_KB = 1024 / BK;  // 1024-deep exact chunk
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr size_t kBarrierBytes = 256;
+constexpr size_t kBarrierBytes = 512;
 constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + 1024 + kBarrierBytes +
                               2 * (kMaxExperts + 1) * sizeof(int32_t);
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // The CTA-pair variant: a 256 x 256 tile per cluster of two CTAs; each CTA
 // stages its 128 rows of A and its 128 of the 256 weight rows (16 + 16 KB)
 // per k-block, so six stages fit.
-constexpr int P_STAGES = 6;
+constexpr int P_STAGES = BK == 64 ? 6 : 12;
 constexpr int P_B_BYTES = (BN / 2) * BK * 2;
 constexpr int P_STAGE_BYTES = A_BYTES + P_B_BYTES;
 constexpr size_t P_RING_BYTES = (size_t)P_STAGES * P_STAGE_BYTES;
@@ -69,6 +76,22 @@ constexpr size_t P_SMEM_BYTES = P_RING_BYTES + 1024 + kBarrierBytes +
                                 2 * (kMaxExperts + 1) * sizeof(int32_t);
 static_assert(P_SMEM_BYTES <= 232448, "shared memory budget");
 static_assert((3 * P_STAGES + 5) * 8 + 16 <= (int)kBarrierBytes, "barriers");
+
+// Shared-memory descriptor of a K-major tile with BK-element rows: 128-byte
+// rows with the 128-byte swizzle, or 64-byte rows with the 64-byte swizzle
+// (8-row groups 1024 or 512 bytes apart).
+__device__ __forceinline__ uint64_t desc_k(uint32_t saddr) {
+    if (BK == 64) return desc_sw128(saddr);
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);        // start address
+    d |= (uint64_t)1 << 16;                          // leading byte offset (unused here)
+    d |= (uint64_t)(512 >> 4) << 32;                 // stride byte offset: 8 rows x 64 B
+    d |= (uint64_t)1 << 46;                          // descriptor version
+    d |= (uint64_t)4 << 61;                          // swizzle: 64 B
+    return d;
+}
+constexpr CUtensorMapSwizzle kTileSwizzle =
+    BK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
 
 struct GemmDev {
     const int32_t *offsets;
@@ -273,7 +296,7 @@ k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         const uint32_t b_addr = a_addr + A_BYTES;
 #pragma unroll
                         for (int k = 0; k < BK / 16; ++k) {
-                            mma_f16(d_tmem, desc_sw128(a_addr + 32 * k), desc_sw128(b_addr + 32 * k),
+                            mma_f16(d_tmem, desc_k(a_addr + 32 * k), desc_k(b_addr + 32 * k),
                                     idesc, (kb > kb0 || k > 0) ? 1u : 0u);
                         }
                         mma_commit(&empty[stage]);
@@ -540,7 +563,7 @@ k_ffn_fused(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CU
                         const uint32_t b_addr = a_addr + A_BYTES;
 #pragma unroll
                         for (int k = 0; k < BK / 16; ++k)
-                            mma_f16(d_tmem, desc_sw128(a_addr + 32 * k), desc_sw128(b_addr + 32 * k),
+                            mma_f16(d_tmem, desc_k(a_addr + 32 * k), desc_k(b_addr + 32 * k),
                                     idesc, (kb > kb0 || k > 0) ? 1u : 0u);
                         mma_commit(&empty[stage]);
                         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -801,7 +824,7 @@ k_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         const uint32_t b_addr = a_addr + A_BYTES;
 #pragma unroll
                         for (int k = 0; k < BK / 16; ++k)
-                            mma_f16_pair(d_tmem, desc_sw128(a_addr + 32 * k), desc_sw128(b_addr + 32 * k),
+                            mma_f16_pair(d_tmem, desc_k(a_addr + 32 * k), desc_k(b_addr + 32 * k),
                                          idesc, (kb > kb0 || k > 0) ? 1u : 0u);
                         mma_commit_pair(&empty[stage], 0x3);
                         if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
@@ -987,11 +1010,11 @@ moe_status launch_pair_or_single(const GemmArgs &a, cudaStream_t stream, bool pa
     const uint64_t bdims[3] = {(uint64_t)a.Kd, (uint64_t)a.Nout, (uint64_t)a.E};
     const uint64_t bstr[2] = {(uint64_t)a.Kd * 2, (uint64_t)a.Kd * a.Nout * 2};
     const uint32_t bbox[3] = {BK, clusters > 0 ? (uint32_t)(BN / 2) : (uint32_t)BN, 1};
-    if (!make_tensor_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, CU_TENSOR_MAP_SWIZZLE_128B, a.a_img, 2,
-                         adims, astr, abox))
+    if (!make_tensor_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, kTileSwizzle, a.a_img, 2, adims,
+                         astr, abox))
         return MOE_ERR_CUDA;
-    if (!make_tensor_map(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, CU_TENSOR_MAP_SWIZZLE_128B, a.b_img, 3,
-                         bdims, bstr, bbox))
+    if (!make_tensor_map(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, kTileSwizzle, a.b_img, 3, bdims,
+                         bstr, bbox))
         return MOE_ERR_CUDA;
     const GemmDev d = gemm_dev(a);
     if (clusters > 0) return launch_epi_pair<EPI>(ma, mb, d, clusters, stream);
@@ -1013,7 +1036,7 @@ moe_status launch_ffn_fused(const GemmArgs &g1, const GemmArgs &g2, void *q2, fl
     const uint64_t b2dims[3] = {(uint64_t)g2.Kd, (uint64_t)g2.Nout, (uint64_t)g2.E};
     const uint64_t b2str[2] = {(uint64_t)g2.Kd * 2, (uint64_t)g2.Kd * g2.Nout * 2};
     const auto f16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    const auto sw = kTileSwizzle;
     if (!make_tensor_map(&ma1, f16, sw, g1.a_img, 2, a1dims, a1str, abox) ||
         !make_tensor_map(&mb1, f16, sw, g1.b_img, 3, b1dims, b1str, bbox) ||
         !make_tensor_map(&ma2, f16, sw, g2.a_img, 2, a2dims, a2str, abox) ||

@@ -117,7 +117,7 @@ typedef struct moe_shape {
 #define MOE_FFN_PATH_SMALL 2
 #define MOE_FFN_PATH_LARGE_PAIR 3
 #define MOE_FFN_PATH_FUSED 4
-#define MOE_FFN_SMALL_ROWS_PER_EXPERT 64
+#define MOE_FFN_SMALL_ROWS_PER_EXPERT 32
 
 /* ------------------------------------------------------------------------
  * Dispatch.
@@ -294,7 +294,7 @@ moe_status moe_stage_views_get(const moe_shape *shape, int for_layer, void *work
  * rows r in [offsets[e], offsets[e+1]).
  *   A int8 [rows, Kd]; W int8 [E, N, Kd]; C int32 [rows, N]; rows >= offsets[E].
  *   N % 8 == 0, Kd % 8 == 0 (Kd % 16 == 0 for the SMALL kernel).
- * path: MOE_FFN_PATH_* (AUTO: SMALL when rows <= 64 * E and Kd % 16 == 0, else LARGE).
+ * path: MOE_FFN_PATH_* (AUTO: SMALL when rows <= 32 * E and Kd % 16 == 0, else LARGE).
  * A is first converted into fp16 images in the workspace, and W into fp16
  * images (LARGE) or biased bytes (SMALL).
  * ------------------------------------------------------------------------ */
