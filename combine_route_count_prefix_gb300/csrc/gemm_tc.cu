@@ -361,10 +361,10 @@ k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 // kernel ("PTO MegaMoE ...", Overall Architecture: the SwiGLU / dynamic
 // quantisation segments overlap GMM2).  The tile list is every GMM1 tile
 // followed by every GMM2 tile, both m-block-major; CTA b takes tiles b, b + G,
-// ... as in k_grouped_gemm.  When a GMM1 tile's epilogue has stored its g
-// columns it counts the tile in done1[m-block]; the CTA whose count completes
-// the m-block quantises its rows (q2, s2, exactly as k_quant2) with its
-// epilogue warps and then sets ready2[m-block].  A GMM2 tile's loads wait for
+// ... as in k_grouped_gemm.  Each epilogue warp that has stored its part of
+// a GMM1 tile's g columns counts itself in done1[m-block]; two extra warps per
+// CTA quantise the m-blocks m = b, b + G, ... of CTA b once their count is
+// complete (q2, s2, exactly as k_quant2) and then set ready2[m-block].  A GMM2 tile's loads wait for
 // that flag, so GMM2 starts on the first m-blocks while GMM1's last tiles and
 // their quantisation are still running, and no kernel boundary separates the
 // stages.  Every CTA's GMM1 tiles precede its GMM2 tiles, so every flag is
@@ -397,33 +397,59 @@ __device__ __forceinline__ bool wait_flag(const int32_t *flag, volatile int *abo
     }
 }
 
-__device__ __forceinline__ void epi_bar() {   // the 8 epilogue warps only
-    asm volatile("bar.sync 1, %0;" ::"n"(32 * EPI_WARPS) : "memory");
-}
-// The same barrier, returning whether `ok` holds in every epilogue thread.
-__device__ __forceinline__ bool epi_bar_and(bool ok) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 1, %2, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)ok), "n"(32 * EPI_WARPS)
-        : "memory");
-    return r != 0;
+constexpr int Q2_WARPS = 2;                       // quantisation service warps per CTA
+constexpr int FUSED_THREADS = THREADS + 32 * Q2_WARPS;
+
+__device__ __forceinline__ bool wait_count(const int32_t *ctr, int target, volatile int *abort_flag,
+                                           int32_t *status) {
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+        if (v >= target) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > kTimeoutNs) {
+            *abort_flag = 1;
+            atomicOr(status, MOE_DEV_TIMEOUT);
+            return false;
+        }
+        __nanosleep(512);
+    }
 }
 
-// Rows [row0, row0 + rows) of g -> q2 codes and s2 (one warp per row, the
-// arithmetic of k_quant2).  g was written by other CTAs: read through L2.
-__device__ __forceinline__ void quant2_rows(const FusedDev &p, int row0, int rows, int ew, int lane) {
-    // two passes over the row (the second from L2), so that the epilogue's
-    // registers are not needed for it
-    for (int r = row0 + ew; r < row0 + rows; r += EPI_WARPS) {
-        const float4 *src = reinterpret_cast<const float4 *>(p.g1.g) + (int64_t)r * p.Nh4;
-        uint2 *dst = p.q2 + (int64_t)r * p.Nh4;
-        float amax = 0.0f;
-#pragma unroll 4
+// Row r of g -> its q2 codes and s2 (one warp, the arithmetic of k_quant2).
+// g was written by other CTAs: read through L2.
+__device__ __forceinline__ void quant2_row(const FusedDev &p, int64_t r, int lane) {
+    constexpr int kV = 16;
+    const float4 *src = reinterpret_cast<const float4 *>(p.g1.g) + r * p.Nh4;
+    uint2 *dst = p.q2 + r * p.Nh4;
+    float amax = 0.0f;
+    if (p.Nh4 <= 32 * kV) {
+        float4 v[kV];
+#pragma unroll
+        for (int u = 0; u < kV; ++u) {
+            const int j = lane + 32 * u;
+            v[u] = (j < p.Nh4) ? __ldcg(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kV; ++u)
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w))));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float s = __fdiv_rn(amax, 127.0f);
+        const float rs = __frcp_rn(s);
+#pragma unroll
+        for (int u = 0; u < kV; ++u) {
+            const int j = lane + 32 * u;
+            if (j < p.Nh4) {
+                uint2 o;
+                o.x = pack_half2(quant_code(v[u].x, s, rs), quant_code(v[u].y, s, rs));
+                o.y = pack_half2(quant_code(v[u].z, s, rs), quant_code(v[u].w, s, rs));
+                dst[j] = o;
+            }
+        }
+        if (lane == 0) p.s2[r] = s;
+    } else {
         for (int j = lane; j < p.Nh4; j += 32) {
             const float4 v = __ldcg(src + j);
             amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
@@ -432,7 +458,6 @@ __device__ __forceinline__ void quant2_rows(const FusedDev &p, int row0, int row
         for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         const float s = __fdiv_rn(amax, 127.0f);
         const float rs = __frcp_rn(s);
-#pragma unroll 4
         for (int j = lane; j < p.Nh4; j += 32) {
             const float4 v = __ldcg(src + j);
             uint2 o;
@@ -444,7 +469,7 @@ __device__ __forceinline__ void quant2_rows(const FusedDev &p, int row0, int row
     }
 }
 
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(FUSED_THREADS, 1)
 k_ffn_fused(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
             const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
             FusedDev p) {
@@ -458,7 +483,6 @@ k_ffn_fused(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CU
     uint64_t *drain = acc_empty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    int *last_flag = const_cast<int *>(abort_flag) + 1;
     int32_t *s_sched = reinterpret_cast<int32_t *>(smem + (size_t)STAGES * STAGE_BYTES + kBarrierBytes);
     int32_t *s_off = s_sched + (kMaxExperts + 1);
 
@@ -576,12 +600,11 @@ k_ffn_fused(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CU
             mma_commit(drain);
             wait_bounded(drain, 0, abort_flag, q1.status, false);
         }
-    } else {
+    } else if (warp < 2 + EPI_WARPS) {
         // ---------------------------------------------------- epilogue warps
         const int q = warp & 3;
         const int hf = (warp - 2) >> 2;
         const int rloc = q * 32 + lane;
-        const int ew = warp - 2;          // 0..7
         int accb = 0;
         uint32_t acc_phase = 0;
         for (int64_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
@@ -612,36 +635,34 @@ k_ffn_fused(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CU
                 if (lane == 0) mbar_arrive(&acc_empty[accb]);
                 if (++accb == 2) { accb = 0; acc_phase ^= 1u; }
             }
-            // every epilogue warp leaves together when any of them gave up, so that
-            // no warp is left at one of the barriers below
-            if (!epi_bar_and(ok)) break;
+            if (!ok) break;
             const bool mine = rloc < t.rows && (int64_t)t.row0 + rloc < q1.cap_rows;
             if (second) {
                 if (mine) epilogue_store<(int)Epi::DequantBF16>(p.g2, t, t.row0 + rloc, hf, acc);
                 continue;
             }
             if (mine) epilogue_store<(int)Epi::SwiGLU>(q1, t, t.row0 + rloc, hf, acc);
-            // count the tile in its m-block; the CTA that completes the m-block quantises it
+            // count this warp's part of the tile in its m-block
             __threadfence();   // this thread's g columns, before the count
-            epi_bar();
-            if (ew == 0 && lane == 0) {
-                __threadfence();
-                const int old = atomicAdd(p.done1 + tile / q1.n_blocks, 1);
-                *last_flag = old == q1.n_blocks - 1;
-            }
-            epi_bar();
-            if (*last_flag) {
-                __threadfence();
-                quant2_rows(p, t.row0, t.rows, ew, lane);
-                __threadfence();   // this thread's q2 / s2, before the flag
-                epi_bar();
-                if (ew == 0 && lane == 0) {
-                    __threadfence();
-                    asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p.ready2 + tile / q1.n_blocks),
-                                 "r"(1)
-                                 : "memory");
-                }
-            }
+            __syncwarp();
+            if (lane == 0) atomicAdd(p.done1 + tile / q1.n_blocks, 1);
+        }
+    } else {
+        // ---------------------------------------------------- quantisation service
+        const int sw = warp - 2 - EPI_WARPS;   // 0 .. Q2_WARPS - 1
+        for (int64_t mb = blockIdx.x; mb < mblocks; mb += gridDim.x) {
+            // the m-block's GMM1 tiles, each counted by its 8 epilogue warps
+            bool w = true;
+            if (lane == 0) w = wait_count(p.done1 + mb, EPI_WARPS * q1.n_blocks, abort_flag, q1.status);
+            if (!__shfl_sync(0xffffffffu, w, 0)) break;
+            __threadfence();
+            const Tile t = decode_tile(mb * q1.n_blocks, q1.n_blocks, q1.E, s_sched, s_off);
+            for (int r = sw; r < t.rows; r += Q2_WARPS)
+                if ((int64_t)t.row0 + r < q1.cap_rows) quant2_row(p, (int64_t)t.row0 + r, lane);
+            __threadfence();   // this thread's q2 / s2, before the flag
+            asm volatile("bar.sync 2, %0;" ::"n"(32 * Q2_WARPS) : "memory");
+            if (sw == 0 && lane == 0)
+                asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p.ready2 + mb), "r"(1) : "memory");
         }
     }
 
@@ -1064,7 +1085,7 @@ moe_status launch_ffn_fused(const GemmArgs &g1, const GemmArgs &g2, void *q2, fl
     // other CTAs set
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)num_sms());
-    cfg.blockDim = dim3(THREADS);
+    cfg.blockDim = dim3(FUSED_THREADS);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

@@ -105,7 +105,8 @@ typedef struct moe_shape {
  *   FUSED: LARGE's tiles with GMM1, the second quantisation and GMM2 in one
  *          persistent kernel; GMM2 starts on an m-block as soon as its rows
  *          are quantised ("PTO MegaMoE ...", the quantisation overlapping GMM2).
- *          Same results; measured slower than LARGE, kept as an option.
+ *          Same results; measured slightly slower than LARGE, kept as an
+ *          option.
  *   SMALL: the weights read as int8 (half the bytes), widened on chip into
  *          tensor memory as the MMA's 128-row side, against the expert's rows
  *          (only those present); for few rows per expert, where reading the
