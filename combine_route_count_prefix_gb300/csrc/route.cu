@@ -388,8 +388,9 @@ k_route_fused(RouteDev a, int64_t chunks, int64_t *counts, int32_t *offsets, int
     int32_t *below_s = hw + a.E;         // [E], later the chunk bases
     const bool lead = blockIdx.x == 0;
     const int cpp = (int)a.chunks_per_partition;
+    int32_t *own_s = hw + 2 * a.E;       // [E] this chunk's own counts
     for (int64_t e = tid; e < a.E; e += blockDim.x) {
-        int tot = 0, below = 0;
+        int tot = 0, below = 0, own = 0;
         for (int64_t cb = 0; cb < chunks; cb += kFusedLoads) {
             int v[kFusedLoads];
 #pragma unroll
@@ -399,10 +400,12 @@ k_route_fused(RouteDev a, int64_t chunks, int64_t *counts, int32_t *offsets, int
             for (int u = 0; u < kFusedLoads; ++u) {
                 tot += v[u];
                 if (cb + u < c) below += v[u];
+                if (cb + u == c) own = v[u];
             }
         }
         tot_s[e] = tot;
         below_s[e] = below;
+        own_s[e] = own;
     }
     __syncthreads();
     // exclusive scan over experts of (total, m-blocks), packed in 64 bits
@@ -433,31 +436,19 @@ k_route_fused(RouteDev a, int64_t chunks, int64_t *counts, int32_t *offsets, int
     int bad_all = 0;
     if (lead)
         for (int64_t cc = tid; cc < chunks; cc += blockDim.x) bad_all |= a.bad[cc];
+    // the last chunk of a partition writes that partition's receive counts:
+    // its own base plus its own count is the running sum through the partition
+    const bool part_end = (c + 1) % cpp == 0;
+    const int64_t pc = c / cpp;
     for (int64_t e = e0; e < e1; ++e) {
         const int off = (int)(ex & 0xffffffffll);
         const int tv = tot_s[e];
         below_s[e] += off;   // this chunk's base of expert e
+        if (part_end) recv_cum[e * a.P + pc] = below_s[e] + own_s[e];
         if (lead) {
             counts[e] = tv;
             offsets[e] = off;
             if (sched) sched[e] = (int)(ex >> 32);
-            // receive counts: running sum over the chunks, written at partition ends
-            int run = off, q = 0, pidx = 0;
-            int32_t *rc = recv_cum + e * a.P;
-            const int nch = (int)chunks;
-            const int32_t *hcol = a.hist + e;
-            for (int cb = 0; cb < nch; cb += 16) {
-                int v[16];
-#pragma unroll
-                for (int u = 0; u < 16; ++u) v[u] = (cb + u < nch) ? hcol[(int64_t)(cb + u) * a.E] : 0;
-#pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    if (cb + u < nch) {
-                        run += v[u];
-                        if (++q == cpp) { rc[pidx++] = run; q = 0; }
-                    }
-                }
-            }
         }
         ex += (long long)tv | ((long long)((tv + kGemmBM - 1) / kGemmBM) << 32);
     }
@@ -481,6 +472,150 @@ k_route_fused(RouteDev a, int64_t chunks, int64_t *counts, int32_t *offsets, int
             assist[3 * (int64_t)row + 0] = (int32_t)cr.p;
             assist[3 * (int64_t)row + 1] = t32 - (int32_t)(cr.p * a.M);
             assist[3 * (int64_t)row + 2] = (int32_t)(i - (int64_t)t32 * K32);
+        }
+        route_row[i] = row;
+    }
+}
+
+// ---------------------------------------------------------------- one-CTA routing
+// Tiny batches (at most kSingleMaxRoutes routes): one CTA of 32 warps does
+// everything, so no grid barrier and no global round trip between the count
+// and the final rows.  Larger batches go to the per-chunk kernels: ranking
+// is issue-bound (two warp matches per 32 routes), and one SM ranking 16384
+// routes was measured 4x slower than 32 CTAs with a grid barrier.  Each warp takes a contiguous slice of the route array
+// (route order is row order within an expert), ranks it with __match_any_sync
+// as in k_route_local, and also counts its routes per (partition, expert) for
+// the receive counts.  Per-warp counts are scanned across warps (stable
+// ranks), their totals across experts (offsets, m-block starts), and the
+// partition counts across partitions (recv_cum).
+constexpr int kSingleThreads = 1024;
+constexpr int kSingleWarps = kSingleThreads / 32;
+constexpr int kSingleWindows = 2;   // 32-route windows per warp
+constexpr int64_t kSingleMaxRoutes = (int64_t)kSingleWarps * kSingleWindows * 32;   // 2048
+constexpr size_t kSingleSmemMax = 200 * 1024;
+
+size_t route_single_smem(int64_t E, int64_t P) {
+    return (size_t)(kSingleWarps + P + 1) * (size_t)E * sizeof(int32_t);
+}
+
+__global__ void __launch_bounds__(kSingleThreads)
+k_route_single(RouteDev a, int64_t *counts, int32_t *offsets, int32_t *recv_cum, int32_t *sched,
+               int32_t *route_row, int32_t *assist) {
+    extern __shared__ int32_t sm[];
+    __shared__ long long scratch64[33];
+    const int E = (int)a.E, P = (int)a.P;
+    int32_t *hw = sm;                       // [32][E] warp counts, then warp bases
+    int32_t *hp = sm + kSingleWarps * E;    // [P][E] routes per (partition, expert)
+    int32_t *off_s = hp + P * E;            // [E]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < (kSingleWarps + P) * E; i += kSingleThreads) sm[i] = 0;
+    pdl_wait();
+
+    // T * K <= kSingleMaxRoutes, so every index below fits in 32 bits
+    const int n = (int)(a.T * a.K), K32 = (int)a.K, M32 = (int)a.M;
+    const int per = ((n + kSingleWarps - 1) / kSingleWarps + 31) / 32 * 32;
+    const int w0 = min(warp * per, n), w1 = min(w0 + per, n);
+    const int nwin = (w1 - w0 + 31) / 32;   // warp-uniform, <= kSingleWindows
+    int e_reg[kSingleWindows];
+    int m_reg[kSingleWindows];
+#pragma unroll
+    for (int j = 0; j < kSingleWindows; ++j) {
+        if (j >= nwin) break;
+        const int i = w0 + 32 * j + lane;
+        e_reg[j] = -1;
+        m_reg[j] = 1;
+        if (i < w1) {
+            e_reg[j] = __ldg(a.ids + i);
+            if (a.mask_kind == 1) m_reg[j] = __ldg(a.mask + i / K32);
+            else if (a.mask_kind == 2) m_reg[j] = __ldg(a.mask + i);
+        }
+    }
+    bool bad = false;
+#pragma unroll
+    for (int j = 0; j < kSingleWindows; ++j) {
+        if (j >= nwin) break;
+        int e = -1;
+        if (w0 + 32 * j + lane < w1 && m_reg[j] != 0) {
+            e = route_code(e_reg[j], a);
+            if (e == -4) { bad = true; e = -1; }
+        }
+        e_reg[j] = e;
+    }
+    __syncthreads();   // counters cleared
+
+    int32_t *mine = hw + warp * E;
+    int rl[kSingleWindows];
+#pragma unroll
+    for (int j = 0; j < kSingleWindows; ++j) {
+        if (j >= nwin) break;
+        const int i = w0 + 32 * j + lane;
+        const int e = e_reg[j];
+        const int p = (e >= 0) ? (i / K32) / M32 : 0;
+        const uint32_t grp = __match_any_sync(kFull, e);
+        const uint32_t grp_p = __match_any_sync(kFull, e >= 0 ? p * E + e : -1);
+        rl[j] = (e >= 0) ? mine[e] + __popc(grp & lanemask_lt()) : -1;
+        __syncwarp();
+        if (e >= 0 && lane == __ffs(grp) - 1) mine[e] += __popc(grp);
+        // hp is shared by all warps: one atomic per (partition, expert) group
+        if (e >= 0 && lane == __ffs(grp_p) - 1) atomicAdd(&hp[p * E + e], (int)__popc(grp_p));
+        __syncwarp();
+    }
+    __syncthreads();
+
+    // per expert: warp counts -> exclusive warp bases, partition counts ->
+    // inclusive running sums, and the total
+    int tv = 0;
+    if (tid < E) {
+        int run = 0;
+#pragma unroll 8
+        for (int w = 0; w < kSingleWarps; ++w) {
+            const int v = hw[w * E + tid];
+            hw[w * E + tid] = run;
+            run += v;
+        }
+        tv = run;
+        int pr = 0;
+        for (int p = 0; p < P; ++p) {
+            pr += hp[p * E + tid];
+            hp[p * E + tid] = pr;
+        }
+    }
+    // offsets (low half) and m-block starts (high half) in one 64-bit scan
+    const long long packed = (long long)tv | ((long long)((tv + kGemmBM - 1) / kGemmBM) << 32);
+    long long ptotal;
+    const long long pscan = block_exclusive_scan64_1024(packed, scratch64, &ptotal);
+    if (tid < E) {
+        const int off = (int)(pscan & 0xffffffffll);
+        off_s[tid] = off;
+        counts[tid] = tv;
+        offsets[tid] = off;
+        if (sched) sched[tid] = (int)(pscan >> 32);
+    }
+    const int bad_all = __syncthreads_or(bad);   // also publishes off_s and hp
+    if (tid == 0) {
+        offsets[E] = (int)(ptotal & 0xffffffffll);
+        if (sched) sched[E] = (int)(ptotal >> 32);
+        *a.status = bad_all ? MOE_DEV_BAD_EXPERT_ID : 0;
+    }
+    // receive counts, coalesced: entry (e, p) at e * P + p
+    for (int q = tid; q < E * P; q += kSingleThreads) {
+        const int e = q / P, p = q - e * P;
+        recv_cum[q] = off_s[e] + hp[p * E + e];
+    }
+    // final rows and triplets
+#pragma unroll
+    for (int j = 0; j < kSingleWindows; ++j) {
+        if (j >= nwin) break;
+        const int i = w0 + 32 * j + lane;
+        if (i >= w1) continue;
+        int32_t row = e_reg[j];   // -1 inactive, -2 / -3 special expert
+        if (e_reg[j] >= 0) {
+            row = off_s[e_reg[j]] + mine[e_reg[j]] + rl[j];
+            const int t = i / K32;
+            const int p = t / M32;
+            assist[3 * row + 0] = p;
+            assist[3 * row + 1] = t - p * M32;
+            assist[3 * row + 2] = i - t * K32;
         }
         route_row[i] = row;
     }
@@ -530,6 +665,20 @@ moe_status launch_route(const RouteDev &r, int64_t chunks, int64_t *counts, int3
 moe_status launch_route_fused(RouteDev &r, int64_t chunks, int64_t *counts, int32_t *offsets,
                               int32_t *recv_cum, int32_t *sched, int32_t *route_row,
                               int32_t *assist, cudaStream_t stream) {
+    const size_t ssm = route_single_smem(r.E, r.P);
+    if (r.T * r.K <= kSingleMaxRoutes && ssm <= kSingleSmemMax) {
+        static size_t configured = 0;
+        if (ssm > configured) {
+            if (cudaFuncSetAttribute(k_route_single, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)ssm) != cudaSuccess)
+                return MOE_ERR_CUDA;
+            configured = ssm;
+        }
+        r.rows_final = 1;
+        MOE_LAUNCH("route_single", k_route_single, 1, kSingleThreads, ssm, stream, r, counts,
+                   offsets, recv_cum, sched, route_row, assist);
+        return MOE_OK;
+    }
     const size_t smem = (size_t)kRouteWarps * r.E * sizeof(int32_t);
     int per_sm = 0;
     if (chunks > 0 &&
