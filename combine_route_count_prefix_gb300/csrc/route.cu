@@ -39,7 +39,9 @@
 // when no rows are copied), which also writes the triplet of the row.
 // No global atomics decide a position, so the result is deterministic.
 #include "common.cuh"
+#include "ptx.cuh"
 
+#include <algorithm>
 #include <cooperative_groups.h>
 
 namespace moe {
@@ -621,6 +623,192 @@ k_route_single(RouteDev a, int64_t *counts, int32_t *offsets, int32_t *recv_cum,
     }
 }
 
+// ---------------------------------------------------------------- one-cluster routing
+// Mid-size batches: one thread-block cluster of up to 16 CTAs.  CTA j of the
+// cluster takes the j-th contiguous range of the route array and counts and
+// ranks it as k_route_single does (per warp, __match_any_sync), keeping its
+// per-expert totals and per-(partition, expert) counts in shared memory.  One
+// hardware cluster barrier replaces the grid barrier, and each CTA reads the
+// other CTAs' totals straight from their shared memory (distributed shared
+// memory) instead of a global round trip.  Every CTA then scans the totals
+// over experts itself, writes the final rows and triplets of its range and the
+// receive counts of the partitions that end inside it.
+constexpr int kClThreads = 1024;
+constexpr int kClWarps = kClThreads / 32;
+constexpr int kClWindows = 4;      // 32-route windows per warp
+constexpr int kClMaxParts = 8;     // partitions one CTA's range may touch
+constexpr int kClMaxCtas = 16;
+constexpr int64_t kClMaxRoutesPerCta = (int64_t)kClWarps * kClWindows * 32;   // 4096
+
+size_t route_cluster_smem(int64_t E) {
+    return (size_t)(kClWarps + kClMaxParts + 2) * (size_t)E * sizeof(int32_t);
+}
+
+__device__ __forceinline__ int ld_peer_s32(const int32_t *local, uint32_t rank) {
+    uint32_t remote;
+    int v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+__global__ void __launch_bounds__(kClThreads)
+k_route_cluster(RouteDev a, int64_t per_cta, int64_t *counts, int32_t *offsets, int32_t *recv_cum,
+                int32_t *sched, int32_t *route_row, int32_t *assist) {
+    extern __shared__ int32_t sm[];
+    __shared__ long long scratch64[33];
+    __shared__ int32_t bad_s;
+    const int E = (int)a.E, P = (int)a.P;
+    int32_t *hw = sm;                       // [32][E] warp counts, then warp bases
+    int32_t *hp = hw + kClWarps * E;        // [kClMaxParts][E] per (partition in range, expert)
+    int32_t *tot_s = hp + kClMaxParts * E;  // [E] this CTA's totals (read by the peers)
+    int32_t *base_s = tot_s + E;            // [E] this CTA's base of each expert
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t rank = cluster_ctarank();
+    const int C = (int)gridDim.x;           // the grid is one cluster
+    for (int i = tid; i < (kClWarps + kClMaxParts) * E; i += kClThreads) sm[i] = 0;
+    if (tid == 0) bad_s = 0;
+    pdl_wait();
+
+    // T * K <= kClMaxCtas * kClMaxRoutesPerCta, so indices fit in 32 bits
+    const int n = (int)(a.T * a.K), K32 = (int)a.K, M32 = (int)a.M;
+    const int r0 = min((int)(rank * per_cta), n), r1 = min(r0 + (int)per_cta, n);
+    const int pfirst = (r0 < r1) ? (r0 / K32) / M32 : 0;
+    const int per = ((r1 - r0 + kClWarps - 1) / kClWarps + 31) / 32 * 32;
+    const int w0 = min(r0 + warp * per, r1), w1 = min(w0 + per, r1);
+    const int nwin = (w1 - w0 + 31) / 32;   // warp-uniform, <= kClWindows
+    int e_reg[kClWindows];
+    int m_reg[kClWindows];
+#pragma unroll
+    for (int j = 0; j < kClWindows; ++j) {
+        if (j >= nwin) break;
+        const int i = w0 + 32 * j + lane;
+        e_reg[j] = -1;
+        m_reg[j] = 1;
+        if (i < w1) {
+            e_reg[j] = __ldg(a.ids + i);
+            if (a.mask_kind == 1) m_reg[j] = __ldg(a.mask + i / K32);
+            else if (a.mask_kind == 2) m_reg[j] = __ldg(a.mask + i);
+        }
+    }
+    bool bad = false;
+#pragma unroll
+    for (int j = 0; j < kClWindows; ++j) {
+        if (j >= nwin) break;
+        int e = -1;
+        if (w0 + 32 * j + lane < w1 && m_reg[j] != 0) {
+            e = route_code(e_reg[j], a);
+            if (e == -4) { bad = true; e = -1; }
+        }
+        e_reg[j] = e;
+    }
+    __syncthreads();   // counters cleared
+
+    int32_t *mine = hw + warp * E;
+    int rl[kClWindows];
+#pragma unroll
+    for (int j = 0; j < kClWindows; ++j) {
+        if (j >= nwin) break;
+        const int i = w0 + 32 * j + lane;
+        const int e = e_reg[j];
+        const int q = (e >= 0) ? (i / K32) / M32 - pfirst : 0;   // partition within the range
+        const uint32_t grp = __match_any_sync(kFull, e);
+        rl[j] = (e >= 0) ? mine[e] + __popc(grp & lanemask_lt()) : -1;
+        __syncwarp();
+        if (e >= 0 && lane == __ffs(grp) - 1) mine[e] += __popc(grp);
+        // partition counts (shared by all warps, hence atomic): one add per
+        // expert group when the window lies in one partition (the common
+        // case), else one per route
+        const int i_last = min(w0 + 32 * j + 31, w1 - 1);
+        const bool one_part = (w0 + 32 * j) / K32 / M32 == i_last / K32 / M32;
+        if (one_part) {
+            if (e >= 0 && lane == __ffs(grp) - 1) atomicAdd(&hp[q * E + e], (int)__popc(grp));
+        } else if (e >= 0) {
+            atomicAdd(&hp[q * E + e], 1);
+        }
+        __syncwarp();
+    }
+    if (__any_sync(kFull, bad) && lane == 0) bad_s = 1;
+    __syncthreads();
+    // per expert: warp counts -> exclusive warp bases, partition counts ->
+    // inclusive running sums within the range, and the CTA total
+    if (tid < E) {
+        int run = 0;
+        for (int w = 0; w < kClWarps; ++w) {
+            const int v = hw[w * E + tid];
+            hw[w * E + tid] = run;
+            run += v;
+        }
+        tot_s[tid] = run;
+        int pr = 0;
+        for (int q = 0; q < kClMaxParts; ++q) {
+            pr += hp[q * E + tid];
+            hp[q * E + tid] = pr;
+        }
+    }
+    cluster_sync();   // every CTA's totals are complete and visible to the cluster
+
+    // totals over the cluster and this CTA's share below it
+    int tv = 0, below = 0;
+    if (tid < E) {
+        for (int j = 0; j < C; ++j) {
+            const int v = ld_peer_s32(tot_s + tid, (uint32_t)j);
+            tv += v;
+            if (j < (int)rank) below += v;
+        }
+    }
+    int bad_all = 0;
+    if (rank == 0 && tid < C) bad_all = ld_peer_s32(&bad_s, (uint32_t)tid);
+    const long long packed = (long long)tv | ((long long)((tv + kGemmBM - 1) / kGemmBM) << 32);
+    long long ptotal;
+    const long long pscan = block_exclusive_scan64_1024(packed, scratch64, &ptotal);
+    if (tid < E) {
+        const int off = (int)(pscan & 0xffffffffll);
+        base_s[tid] = off + below;
+        if (rank == 0) {
+            counts[tid] = tv;
+            offsets[tid] = off;
+            if (sched) sched[tid] = (int)(pscan >> 32);
+        }
+    }
+    bad_all = __syncthreads_or(bad_all);   // also publishes base_s
+    if (rank == 0 && tid == 0) {
+        offsets[E] = (int)(ptotal & 0xffffffffll);
+        if (sched) sched[E] = (int)(ptotal >> 32);
+        *a.status = bad_all ? MOE_DEV_BAD_EXPERT_ID : 0;
+    }
+    // receive counts of the partitions whose last route lies in this range
+    if (r0 < r1) {
+        const int MK = M32 * K32;
+        const int plast = (r1 - 1) / MK;
+        for (int q = 0; q <= plast - pfirst; ++q) {
+            const int p = pfirst + q;
+            const int pend = (p + 1) * MK - 1;
+            if (pend < r0 || pend >= r1) continue;
+            for (int e = tid; e < E; e += kClThreads)
+                recv_cum[(int64_t)e * P + p] = base_s[e] + hp[q * E + e];
+        }
+    }
+    // final rows and triplets
+#pragma unroll
+    for (int j = 0; j < kClWindows; ++j) {
+        if (j >= nwin) break;
+        const int i = w0 + 32 * j + lane;
+        if (i >= w1) continue;
+        int32_t row = e_reg[j];   // -1 inactive, -2 / -3 special expert
+        if (e_reg[j] >= 0) {
+            row = base_s[e_reg[j]] + mine[e_reg[j]] + rl[j];
+            const int t = i / K32;
+            const int p = t / M32;
+            assist[3 * row + 0] = p;
+            assist[3 * row + 1] = t - p * M32;
+            assist[3 * row + 2] = i - t * K32;
+        }
+        route_row[i] = row;
+    }
+    cluster_sync();   // the peers have finished reading this CTA's shared memory
+}
+
 __global__ void k_route_resolve(RouteDev a, int32_t *route_row, int32_t *assist) {
     pdl_wait();
     const int64_t n = a.T * a.K;
@@ -662,6 +850,39 @@ moe_status launch_route(const RouteDev &r, int64_t chunks, int64_t *counts, int3
     return MOE_OK;
 }
 
+// Whether a cluster of C CTAs of k_route_cluster with `smem` bytes each can be
+// scheduled (16 CTAs need the non-portable cluster size).
+bool cluster_fits(int64_t C, size_t smem) {
+    static size_t configured = 0;
+    if (smem > configured) {
+        if (cudaFuncSetAttribute(k_route_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess ||
+            cudaFuncSetAttribute(k_route_cluster, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                 1) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        configured = smem;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)C);
+    cfg.blockDim = dim3(kClThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, k_route_cluster, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return clusters >= 1;
+}
+
 moe_status launch_route_fused(RouteDev &r, int64_t chunks, int64_t *counts, int32_t *offsets,
                               int32_t *recv_cum, int32_t *sched, int32_t *route_row,
                               int32_t *assist, cudaStream_t stream) {
@@ -678,6 +899,23 @@ moe_status launch_route_fused(RouteDev &r, int64_t chunks, int64_t *counts, int3
         MOE_LAUNCH("route_single", k_route_single, 1, kSingleThreads, ssm, stream, r, counts,
                    offsets, recv_cum, sched, route_row, assist);
         return MOE_OK;
+    }
+    // one cluster: ranges of at most 4096 routes, each touching at most
+    // kClMaxParts partitions
+    const int64_t n = r.T * r.K;
+    if (n <= (int64_t)kClMaxCtas * kClMaxRoutesPerCta) {
+        const int64_t C = std::min<int64_t>(kClMaxCtas, std::max<int64_t>(2, (n + 1023) / 1024));
+        const int64_t per_cta = ((n + C - 1) / C + 31) / 32 * 32;
+        const int64_t parts = per_cta / (r.M * r.K) + 2;
+        const size_t csm = route_cluster_smem(r.E);
+        if (per_cta <= kClMaxRoutesPerCta && parts <= kClMaxParts && csm <= kSingleSmemMax &&
+            cluster_fits(C, csm)) {
+            r.rows_final = 1;
+            MOE_LAUNCH_CLUSTER("route_cluster", k_route_cluster, (unsigned)C, kClThreads, csm, stream,
+                               (unsigned)C, r, per_cta, counts, offsets, recv_cum, sched, route_row,
+                               assist);
+            return MOE_OK;
+        }
     }
     const size_t smem = (size_t)kRouteWarps * r.E * sizeof(int32_t);
     int per_sm = 0;

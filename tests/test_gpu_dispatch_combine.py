@@ -30,9 +30,11 @@ CASES = {
     "max_e_k": wl.custom(P=5, M=113, H=64, E=1024, K=16, has_shared=True),
     "zipf_skew": wl.custom(P=4, M=256, H=256, E=128, K=8, mask_kind=2, mask_p=0.95,
                            has_shared=True, routing="zipf", zipf_zero=10),
-    # above 2048 routes routing runs on one CTA per chunk with a grid barrier
-    "chunks_fused": wl.custom(P=4, M=600, H=64, E=64, K=8, mask_kind=2, mask_p=0.9,
-                              has_shared=True),
+    # 2048 < routes <= 65536: routing in one thread-block cluster
+    "cluster": wl.custom(P=4, M=600, H=64, E=64, K=8, mask_kind=2, mask_p=0.9,
+                         has_shared=True),
+    # above 65536 routes: one CTA per chunk with a grid barrier
+    "chunks_fused": wl.custom(P=2, M=8200, H=64, E=64, K=4, mask_kind=2, mask_p=0.9),
     # more routing chunks than can be resident at once: the count/scan kernels
     # and row resolution in the row kernel are used instead of the fused kernel
     "many_partitions": wl.custom(P=640, M=8, H=64, E=16, K=4, mask_kind=1, mask_p=0.8,
@@ -41,7 +43,8 @@ CASES = {
     "single_limit": wl.custom(P=8, M=16, H=64, E=200, K=16, mask_kind=2, mask_p=0.7),
     "single_limit_plus": wl.custom(P=1, M=129, H=64, E=200, K=16, mask_kind=1, mask_p=0.7),
     # few routes, but (partition x expert) counters too large for one CTA's
-    # shared memory: the per-chunk kernel with the grid barrier
+    # shared memory and too many partitions per cluster CTA: the per-chunk
+    # kernel with the grid barrier
     "wide_partitions": wl.custom(P=64, M=4, H=64, E=1024, K=8, mask_kind=1, mask_p=0.9),
 }
 
