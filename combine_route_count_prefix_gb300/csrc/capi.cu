@@ -281,7 +281,7 @@ moe_status moe_dispatch(const moe_shape *shape, const void *x, const int32_t *ex
     if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
     RouteDev r = route_dev(s, expert_ids, x_active_mask, workspace, L);
     MOE_TRY(launch_route_fused(r, route_chunks(s), expert_token_nums, expert_offsets,
-                               ep_recv_counts, nullptr, route_row, assist, stream));
+                               ep_recv_counts, nullptr, route_row, stream));
     if (expand_x) return launch_dispatch_rows(r, x, route_row, assist, expand_x, s.hidden, stream);
     return launch_route_resolve(r, route_row, assist, stream);
 }
@@ -308,7 +308,7 @@ moe_status moe_dispatch_quant(const moe_shape *shape, const void *x, const int32
     if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
     RouteDev r = route_dev(s, expert_ids, x_active_mask, workspace, L);
     MOE_TRY(launch_route_fused(r, route_chunks(s), expert_token_nums, expert_offsets,
-                               ep_recv_counts, nullptr, route_row, assist, stream));
+                               ep_recv_counts, nullptr, route_row, stream));
     return launch_dispatch_quant(r, x, smooth_scales, route_row, assist, expand_x, dynamic_scales,
                                  s.hidden, stream);
 }
@@ -523,7 +523,7 @@ moe_status moe_layer(const moe_shape *shape, const void *x, const int32_t *exper
     int32_t *offsets = at<int32_t>(workspace, L.offsets);
     MOE_TRY(launch_route_fused(r, route_chunks(s), at<int64_t>(workspace, L.counts), offsets,
                                at<int32_t>(workspace, L.recv_cum), at<int32_t>(workspace, L.sched),
-                               route_row, at<int32_t>(workspace, L.assist), stream));
+                               route_row, stream));
     if (s.num_tokens == 0) return MOE_OK;
     MOE_TRY(launch_quant_scatter(r, x, route_row, at<int32_t>(workspace, L.assist),
                                  at<void>(workspace, L.q1), at<float>(workspace, L.s1), s.hidden,

@@ -191,23 +191,28 @@ __device__ __forceinline__ int route_code(int e, const RouteDev &a) {
 
 // Final row of route (t, k): route_row holds the route's rank inside its
 // routing chunk (or -1) after launch_route; the chunk base of its expert is
-// in r.hist after the scan.  Replaces route_row[t*K+k] by the row, writes
-// the row's triplet (partition, token in partition, slot) and returns the
-// row (-1 if inactive).  Called exactly once per route per call.
+// in r.hist after the scan.  Replaces route_row[t*K+k] by the row (unless
+// the routing kernel already wrote final rows), writes the row's triplet
+// (partition, token in partition, slot) and returns the row (-1 if
+// inactive).  Called exactly once per route per call, by a kernel that
+// spreads the routes over the whole GPU, so the triplets' scattered stores
+// never sit on the routing kernel's few CTAs.
 __device__ __forceinline__ int32_t resolve_route_row(const RouteDev &a, int64_t t, int k,
                                                      int32_t *route_row, int32_t *assist) {
     const int64_t i = t * a.K + k;
     const int32_t lr = route_row[i];
     if (lr < 0) return lr;   // inactive (-1) or a special expert (-2, -3): no row
-    if (a.rows_final) return lr;
-    const int e = a.ids[i];
     // T * K < 2^31, so token, partition and chunk indices fit in 32 bits
     const int32_t t32 = (int32_t)t, M32 = (int32_t)a.M;
     const int32_t p = t32 / M32;
     const int32_t tl = t32 - p * M32;
-    const int32_t c = p * (int32_t)a.chunks_per_partition + tl / (int32_t)a.chunk_tokens;
-    const int32_t row = a.hist[(int64_t)c * a.E + e] + lr;
-    route_row[i] = row;
+    int32_t row = lr;
+    if (!a.rows_final) {
+        const int e = a.ids[i];
+        const int32_t c = p * (int32_t)a.chunks_per_partition + tl / (int32_t)a.chunk_tokens;
+        row = a.hist[(int64_t)c * a.E + e] + lr;
+        route_row[i] = row;
+    }
     if (assist) {
         assist[3 * (int64_t)row + 0] = p;
         assist[3 * (int64_t)row + 1] = tl;
@@ -221,12 +226,14 @@ __device__ __forceinline__ int32_t resolve_route_row(const RouteDev &a, int64_t 
 moe_status launch_route(const RouteDev &r, int64_t chunks, int64_t *counts, int32_t *offsets,
                         int32_t *recv_cum, int32_t *sched, int32_t *route_row,
                         cudaStream_t stream);
-// Single-kernel routing (count, rank, grid barrier, prefix, final rows and
-// triplets) when all chunks fit on the GPU at once; otherwise launch_route.
-// Sets r.rows_final accordingly.
+// Single-kernel routing (count, rank, prefix and final rows in one launch: one
+// CTA for tiny batches, one thread-block cluster for mid-size ones, one CTA
+// per chunk with a grid barrier when all chunks fit on the GPU at once);
+// otherwise launch_route.  Sets r.rows_final accordingly.  The triplets are
+// written by the kernel that next reads route_row (resolve_route_row).
 moe_status launch_route_fused(RouteDev &r, int64_t chunks, int64_t *counts, int32_t *offsets,
                               int32_t *recv_cum, int32_t *sched, int32_t *route_row,
-                              int32_t *assist, cudaStream_t stream);
+                              cudaStream_t stream);
 // Resolution alone, when no kernel copies or quantises the rows.
 moe_status launch_route_resolve(const RouteDev &r, int32_t *route_row, int32_t *assist,
                                 cudaStream_t stream);

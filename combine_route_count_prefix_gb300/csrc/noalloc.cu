@@ -109,7 +109,7 @@ moe_status moe_dispatch_noalloc(const moe_shape *shape, const void *x, const int
     r.bad = r.hist + chunks * s.num_experts;
     r.rows_final = 0;
     MOE_TRY(launch_route_fused(r, chunks, expert_token_nums, expert_offsets, ep_recv_counts,
-                               nullptr, route_row, assist, stream));
+                               nullptr, route_row, stream));
     if (expand_x) return launch_dispatch_rows(r, x, route_row, assist, expand_x, s.hidden, stream);
     return launch_route_resolve(r, route_row, assist, stream);
 }

@@ -21,7 +21,7 @@
 // partition boundary.
 //   k_route_local  one CTA per chunk.  Each warp loads a contiguous slice of
 //                  the chunk (all its loads issued at once), then walks it in
-//                  order with __match_any_sync: one shared-memory add per
+//                  order with warp_match: one shared-memory add per
 //                  distinct expert per 32 routes gives every route its rank
 //                  among same-expert routes of the warp.  Warp counts are
 //                  then scanned across warps, giving each route its rank
@@ -36,7 +36,9 @@
 //                  call's status word.
 // The final row, base[chunk][e] + rank in chunk, is resolved by the kernel
 // that next touches each token (row copy, quantisation, or k_route_resolve
-// when no rows are copied), which also writes the triplet of the row.
+// when no rows are copied), which also writes the triplet of the row.  The
+// single-kernel forms below write final rows themselves; the triplets are
+// still written by that next kernel.
 // No global atomics decide a position, so the result is deterministic.
 #include "common.cuh"
 #include "ptx.cuh"
@@ -49,6 +51,24 @@ namespace {
 
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kMaxWindows = (kRouteChunkTokensMax * kMaxTopK / kRouteWarps + 31) / 32;   // 16
+
+// Lanes of the warp holding the same value as this lane, for values in
+// [-4, 2^nbits): one ballot for the sign and one per bit.  The same mask as
+// __match_any_sync for the non-negative values (negative values may share a
+// group; callers use the mask only for experts), but built from votes, which
+// pipeline across warps, where the match instruction was measured at about
+// a hundred cycles a call, one call at a time per SM.
+__device__ __forceinline__ uint32_t warp_match(int v, int nbits) {
+    const uint32_t neg = __ballot_sync(kFull, v < 0);
+    uint32_t m = (v < 0) ? neg : ~neg;
+    for (int b = 0; b < nbits; ++b) {
+        const bool bit = (v >> b) & 1;
+        const uint32_t bb = __ballot_sync(kFull, bit);
+        m &= bit ? bb : ~bb;
+    }
+    return m;
+}
+__device__ __forceinline__ int expert_bits(int64_t E) { return 32 - __clz((int)E - 1); }
 
 struct ChunkRange {
     int64_t r0, r1;   // route range [r0, r1) (flat index t*K + k)
@@ -114,13 +134,14 @@ k_route_local(RouteDev a, int32_t *local_rank) {
     __syncthreads();   // hw cleared
 
     int32_t *mine = hw + warp * a.E;
+    const int nbits = expert_bits(a.E);
     int rl[kMaxWindows];
 #pragma unroll
     for (int j = 0; j < kMaxWindows; ++j) {
         if (j >= nwin) break;
         rl[j] = -1;
         const int e = e_reg[j];
-        const uint32_t grp = __match_any_sync(kFull, e);
+        const uint32_t grp = warp_match(e, nbits);
         if (e >= 0) rl[j] = mine[e] + __popc(grp & lanemask_lt());
         __syncwarp();
         if (e >= 0 && lane == __ffs(grp) - 1) mine[e] += __popc(grp);
@@ -305,7 +326,7 @@ constexpr int kFusedLoads = 32;   // chunk counts loaded at once per expert
 
 __global__ void __launch_bounds__(kRouteThreads)
 k_route_fused(RouteDev a, int64_t chunks, int64_t *counts, int32_t *offsets, int32_t *recv_cum,
-              int32_t *sched, int32_t *route_row, int32_t *assist) {
+              int32_t *sched, int32_t *route_row) {
     extern __shared__ int32_t hw[];   // [kRouteWarps][E]; reused after the barrier
     __shared__ int any_bad;
     __shared__ long long scratch64[kRouteWarps + 1];
@@ -351,13 +372,14 @@ k_route_fused(RouteDev a, int64_t chunks, int64_t *counts, int32_t *offsets, int
     }
     __syncthreads();
     int32_t *mine = hw + warp * a.E;
+    const int nbits = expert_bits(a.E);
     int rl[kMaxWindows];
 #pragma unroll
     for (int j = 0; j < kMaxWindows; ++j) {
         if (j >= nwin) break;
         rl[j] = -1;
         const int e = e_reg[j];
-        const uint32_t grp = __match_any_sync(kFull, e);
+        const uint32_t grp = warp_match(e, nbits);
         if (e >= 0) rl[j] = mine[e] + __popc(grp & lanemask_lt());
         __syncwarp();
         if (e >= 0 && lane == __ffs(grp) - 1) mine[e] += __popc(grp);
@@ -461,21 +483,14 @@ k_route_fused(RouteDev a, int64_t chunks, int64_t *counts, int32_t *offsets, int
         if (sched) sched[a.E] = (int)(tot_all >> 32);
         *a.status = bad_all ? MOE_DEV_BAD_EXPERT_ID : 0;
     }
-    // ---------------- final rows and triplets of this chunk's routes
+    // ---------------- final rows of this chunk's routes
 #pragma unroll
     for (int j = 0; j < kMaxWindows; ++j) {
         if (j >= nwin) break;
         const int64_t i = w0 + 32 * j + lane;
         if (i >= w1) continue;
-        int32_t row = e_reg[j];   // -1 inactive, -2 / -3 special expert
-        if (e_reg[j] >= 0) {
-            row = below_s[e_reg[j]] + rl[j];
-            const int32_t t32 = (int32_t)(i / K32);
-            assist[3 * (int64_t)row + 0] = (int32_t)cr.p;
-            assist[3 * (int64_t)row + 1] = t32 - (int32_t)(cr.p * a.M);
-            assist[3 * (int64_t)row + 2] = (int32_t)(i - (int64_t)t32 * K32);
-        }
-        route_row[i] = row;
+        // -1 inactive, -2 / -3 special expert; triplets are written by the next kernel
+        route_row[i] = (e_reg[j] >= 0) ? below_s[e_reg[j]] + rl[j] : e_reg[j];
     }
 }
 
@@ -485,7 +500,7 @@ k_route_fused(RouteDev a, int64_t chunks, int64_t *counts, int32_t *offsets, int
 // and the final rows.  Larger batches go to the per-chunk kernels: ranking
 // is issue-bound (two warp matches per 32 routes), and one SM ranking 16384
 // routes was measured 4x slower than 32 CTAs with a grid barrier.  Each warp takes a contiguous slice of the route array
-// (route order is row order within an expert), ranks it with __match_any_sync
+// (route order is row order within an expert), ranks it with warp_match
 // as in k_route_local, and also counts its routes per (partition, expert) for
 // the receive counts.  Per-warp counts are scanned across warps (stable
 // ranks), their totals across experts (offsets, m-block starts), and the
@@ -502,7 +517,7 @@ size_t route_single_smem(int64_t E, int64_t P) {
 
 __global__ void __launch_bounds__(kSingleThreads)
 k_route_single(RouteDev a, int64_t *counts, int32_t *offsets, int32_t *recv_cum, int32_t *sched,
-               int32_t *route_row, int32_t *assist) {
+               int32_t *route_row) {
     extern __shared__ int32_t sm[];
     __shared__ long long scratch64[33];
     const int E = (int)a.E, P = (int)a.P;
@@ -546,6 +561,7 @@ k_route_single(RouteDev a, int64_t *counts, int32_t *offsets, int32_t *recv_cum,
     __syncthreads();   // counters cleared
 
     int32_t *mine = hw + warp * E;
+    const int nbits = expert_bits(a.E);
     int rl[kSingleWindows];
 #pragma unroll
     for (int j = 0; j < kSingleWindows; ++j) {
@@ -553,13 +569,18 @@ k_route_single(RouteDev a, int64_t *counts, int32_t *offsets, int32_t *recv_cum,
         const int i = w0 + 32 * j + lane;
         const int e = e_reg[j];
         const int p = (e >= 0) ? (i / K32) / M32 : 0;
-        const uint32_t grp = __match_any_sync(kFull, e);
-        const uint32_t grp_p = __match_any_sync(kFull, e >= 0 ? p * E + e : -1);
+        const uint32_t grp = warp_match(e, nbits);
         rl[j] = (e >= 0) ? mine[e] + __popc(grp & lanemask_lt()) : -1;
         __syncwarp();
         if (e >= 0 && lane == __ffs(grp) - 1) mine[e] += __popc(grp);
-        // hp is shared by all warps: one atomic per (partition, expert) group
-        if (e >= 0 && lane == __ffs(grp_p) - 1) atomicAdd(&hp[p * E + e], (int)__popc(grp_p));
+        // partition counts (shared by all warps, hence atomic): one add per
+        // expert group when the window lies in one partition, else one per route
+        const int i_last = min(w0 + 32 * j + 31, w1 - 1);
+        if ((w0 + 32 * j) / K32 / M32 == i_last / K32 / M32) {
+            if (e >= 0 && lane == __ffs(grp) - 1) atomicAdd(&hp[p * E + e], (int)__popc(grp));
+        } else if (e >= 0) {
+            atomicAdd(&hp[p * E + e], 1);
+        }
         __syncwarp();
     }
     __syncthreads();
@@ -604,35 +625,28 @@ k_route_single(RouteDev a, int64_t *counts, int32_t *offsets, int32_t *recv_cum,
         const int e = q / P, p = q - e * P;
         recv_cum[q] = off_s[e] + hp[p * E + e];
     }
-    // final rows and triplets
+    // final rows
 #pragma unroll
     for (int j = 0; j < kSingleWindows; ++j) {
         if (j >= nwin) break;
         const int i = w0 + 32 * j + lane;
         if (i >= w1) continue;
-        int32_t row = e_reg[j];   // -1 inactive, -2 / -3 special expert
-        if (e_reg[j] >= 0) {
-            row = off_s[e_reg[j]] + mine[e_reg[j]] + rl[j];
-            const int t = i / K32;
-            const int p = t / M32;
-            assist[3 * row + 0] = p;
-            assist[3 * row + 1] = t - p * M32;
-            assist[3 * row + 2] = i - t * K32;
-        }
-        route_row[i] = row;
+        // -1 inactive, -2 / -3 special expert; triplets are written by the next kernel
+        route_row[i] = (e_reg[j] >= 0) ? off_s[e_reg[j]] + mine[e_reg[j]] + rl[j] : e_reg[j];
     }
 }
 
 // ---------------------------------------------------------------- one-cluster routing
 // Mid-size batches: one thread-block cluster of up to 16 CTAs.  CTA j of the
 // cluster takes the j-th contiguous range of the route array and counts and
-// ranks it as k_route_single does (per warp, __match_any_sync), keeping its
-// per-expert totals and per-(partition, expert) counts in shared memory.  One
-// hardware cluster barrier replaces the grid barrier, and each CTA reads the
-// other CTAs' totals straight from their shared memory (distributed shared
-// memory) instead of a global round trip.  Every CTA then scans the totals
-// over experts itself, writes the final rows and triplets of its range and the
-// receive counts of the partitions that end inside it.
+// ranks it as k_route_single does (per warp, warp_match), keeping its
+// per-(partition, expert) counts in shared memory.  Each CTA stores its
+// per-expert totals into every CTA's shared memory (distributed shared
+// memory stores, which complete under the barrier's release), and one
+// hardware cluster barrier replaces the grid barrier and the global round
+// trip of the histograms.  Every CTA then scans the totals over experts
+// itself and writes the final rows of its range and the receive counts of
+// the partitions that end inside it.
 constexpr int kClThreads = 1024;
 constexpr int kClWarps = kClThreads / 32;
 constexpr int kClWindows = 4;      // 32-route windows per warp
@@ -640,40 +654,43 @@ constexpr int kClMaxParts = 8;     // partitions one CTA's range may touch
 constexpr int kClMaxCtas = 16;
 constexpr int64_t kClMaxRoutesPerCta = (int64_t)kClWarps * kClWindows * 32;   // 4096
 
-size_t route_cluster_smem(int64_t E) {
-    return (size_t)(kClWarps + kClMaxParts + 2) * (size_t)E * sizeof(int32_t);
+size_t route_cluster_smem(int64_t E, int64_t C) {
+    return (size_t)(kClWarps + kClMaxParts + 1 + C) * (size_t)E * sizeof(int32_t);
 }
 
-__device__ __forceinline__ int ld_peer_s32(const int32_t *local, uint32_t rank) {
+// Store v at the address of `local` in the shared memory of CTA `rank`.
+__device__ __forceinline__ void st_peer_s32(int32_t *local, uint32_t rank, int v) {
     uint32_t remote;
-    int v;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
-    return v;
+    asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
 }
 
 __global__ void __launch_bounds__(kClThreads)
 k_route_cluster(RouteDev a, int64_t per_cta, int64_t *counts, int32_t *offsets, int32_t *recv_cum,
-                int32_t *sched, int32_t *route_row, int32_t *assist) {
+                int32_t *sched, int32_t *route_row) {
     extern __shared__ int32_t sm[];
     __shared__ long long scratch64[33];
-    __shared__ int32_t bad_s;
+    __shared__ int32_t bad_s[kClMaxCtas];   // each CTA's invalid-id flag
     const int E = (int)a.E, P = (int)a.P;
+    const int C = (int)gridDim.x;           // the grid is one cluster
     int32_t *hw = sm;                       // [32][E] warp counts, then warp bases
     int32_t *hp = hw + kClWarps * E;        // [kClMaxParts][E] per (partition in range, expert)
-    int32_t *tot_s = hp + kClMaxParts * E;  // [E] this CTA's totals (read by the peers)
-    int32_t *base_s = tot_s + E;            // [E] this CTA's base of each expert
+    int32_t *base_s = hp + kClMaxParts * E; // [E] this CTA's base of each expert
+    int32_t *all_tot = base_s + E;          // [C][E] every CTA's totals, stored by that CTA
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t rank = cluster_ctarank();
-    const int C = (int)gridDim.x;           // the grid is one cluster
+    // this CTA has started: peers may store into its shared memory once every
+    // CTA has arrived here (the wait comes just before the first such store)
+    cluster_arrive();
     for (int i = tid; i < (kClWarps + kClMaxParts) * E; i += kClThreads) sm[i] = 0;
-    if (tid == 0) bad_s = 0;
-    pdl_wait();
 
+    // The ids and the mask are inputs, which no kernel of this library writes,
+    // so they are loaded before waiting on the previous kernel of the stream;
+    // everything this kernel writes is written after the wait.
     // T * K <= kClMaxCtas * kClMaxRoutesPerCta, so indices fit in 32 bits
-    const int n = (int)(a.T * a.K), K32 = (int)a.K, M32 = (int)a.M;
+    const int n = (int)(a.T * a.K), K32 = (int)a.K, M32 = (int)a.M, MK = M32 * K32;
     const int r0 = min((int)(rank * per_cta), n), r1 = min(r0 + (int)per_cta, n);
-    const int pfirst = (r0 < r1) ? (r0 / K32) / M32 : 0;
+    const int pfirst = (r0 < r1) ? r0 / MK : 0;
     const int per = ((r1 - r0 + kClWarps - 1) / kClWarps + 31) / 32 * 32;
     const int w0 = min(r0 + warp * per, r1), w1 = min(w0 + per, r1);
     const int nwin = (w1 - w0 + 31) / 32;   // warp-uniform, <= kClWindows
@@ -691,6 +708,7 @@ k_route_cluster(RouteDev a, int64_t per_cta, int64_t *counts, int32_t *offsets, 
             else if (a.mask_kind == 2) m_reg[j] = __ldg(a.mask + i);
         }
     }
+    pdl_wait();
     bool bad = false;
 #pragma unroll
     for (int j = 0; j < kClWindows; ++j) {
@@ -705,60 +723,60 @@ k_route_cluster(RouteDev a, int64_t per_cta, int64_t *counts, int32_t *offsets, 
     __syncthreads();   // counters cleared
 
     int32_t *mine = hw + warp * E;
+    const int nbits = expert_bits(a.E);
     int rl[kClWindows];
 #pragma unroll
     for (int j = 0; j < kClWindows; ++j) {
         if (j >= nwin) break;
         const int i = w0 + 32 * j + lane;
         const int e = e_reg[j];
-        const int q = (e >= 0) ? (i / K32) / M32 - pfirst : 0;   // partition within the range
-        const uint32_t grp = __match_any_sync(kFull, e);
+        const uint32_t grp = warp_match(e, nbits);
         rl[j] = (e >= 0) ? mine[e] + __popc(grp & lanemask_lt()) : -1;
         __syncwarp();
         if (e >= 0 && lane == __ffs(grp) - 1) mine[e] += __popc(grp);
         // partition counts (shared by all warps, hence atomic): one add per
         // expert group when the window lies in one partition (the common
         // case), else one per route
-        const int i_last = min(w0 + 32 * j + 31, w1 - 1);
-        const bool one_part = (w0 + 32 * j) / K32 / M32 == i_last / K32 / M32;
-        if (one_part) {
-            if (e >= 0 && lane == __ffs(grp) - 1) atomicAdd(&hp[q * E + e], (int)__popc(grp));
+        const int pw0 = (w0 + 32 * j) / MK, pw1 = min(w0 + 32 * j + 31, w1 - 1) / MK;
+        if (pw0 == pw1) {
+            if (e >= 0 && lane == __ffs(grp) - 1) atomicAdd(&hp[(pw0 - pfirst) * E + e], (int)__popc(grp));
         } else if (e >= 0) {
-            atomicAdd(&hp[q * E + e], 1);
+            atomicAdd(&hp[(i / MK - pfirst) * E + e], 1);
         }
         __syncwarp();
     }
-    if (__any_sync(kFull, bad) && lane == 0) bad_s = 1;
-    __syncthreads();
+    const int bad_cta = __syncthreads_or(bad);
+    cluster_wait();   // every CTA of the cluster has started
     // per expert: warp counts -> exclusive warp bases, partition counts ->
     // inclusive running sums within the range, and the CTA total
     if (tid < E) {
         int run = 0;
+#pragma unroll 8
         for (int w = 0; w < kClWarps; ++w) {
             const int v = hw[w * E + tid];
             hw[w * E + tid] = run;
             run += v;
         }
-        tot_s[tid] = run;
+        for (int j = 0; j < C; ++j) st_peer_s32(all_tot + rank * E + tid, (uint32_t)j, run);
         int pr = 0;
         for (int q = 0; q < kClMaxParts; ++q) {
             pr += hp[q * E + tid];
             hp[q * E + tid] = pr;
         }
     }
-    cluster_sync();   // every CTA's totals are complete and visible to the cluster
+    if (tid < C) st_peer_s32(bad_s + rank, (uint32_t)tid, bad_cta);
+    cluster_sync();   // every CTA's stores into this CTA have completed and are visible
 
     // totals over the cluster and this CTA's share below it
     int tv = 0, below = 0;
     if (tid < E) {
         for (int j = 0; j < C; ++j) {
-            const int v = ld_peer_s32(tot_s + tid, (uint32_t)j);
+            const int v = all_tot[j * E + tid];
             tv += v;
             if (j < (int)rank) below += v;
         }
     }
-    int bad_all = 0;
-    if (rank == 0 && tid < C) bad_all = ld_peer_s32(&bad_s, (uint32_t)tid);
+    int bad_all = (rank == 0 && tid < C) ? bad_s[tid] : 0;
     const long long packed = (long long)tv | ((long long)((tv + kGemmBM - 1) / kGemmBM) << 32);
     long long ptotal;
     const long long pscan = block_exclusive_scan64_1024(packed, scratch64, &ptotal);
@@ -779,7 +797,6 @@ k_route_cluster(RouteDev a, int64_t per_cta, int64_t *counts, int32_t *offsets, 
     }
     // receive counts of the partitions whose last route lies in this range
     if (r0 < r1) {
-        const int MK = M32 * K32;
         const int plast = (r1 - 1) / MK;
         for (int q = 0; q <= plast - pfirst; ++q) {
             const int p = pfirst + q;
@@ -789,24 +806,15 @@ k_route_cluster(RouteDev a, int64_t per_cta, int64_t *counts, int32_t *offsets, 
                 recv_cum[(int64_t)e * P + p] = base_s[e] + hp[q * E + e];
         }
     }
-    // final rows and triplets
+    // final rows
 #pragma unroll
     for (int j = 0; j < kClWindows; ++j) {
         if (j >= nwin) break;
         const int i = w0 + 32 * j + lane;
         if (i >= w1) continue;
-        int32_t row = e_reg[j];   // -1 inactive, -2 / -3 special expert
-        if (e_reg[j] >= 0) {
-            row = base_s[e_reg[j]] + mine[e_reg[j]] + rl[j];
-            const int t = i / K32;
-            const int p = t / M32;
-            assist[3 * row + 0] = p;
-            assist[3 * row + 1] = t - p * M32;
-            assist[3 * row + 2] = i - t * K32;
-        }
-        route_row[i] = row;
+        // -1 inactive, -2 / -3 special expert; triplets are written by the next kernel
+        route_row[i] = (e_reg[j] >= 0) ? base_s[e_reg[j]] + mine[e_reg[j]] + rl[j] : e_reg[j];
     }
-    cluster_sync();   // the peers have finished reading this CTA's shared memory
 }
 
 __global__ void k_route_resolve(RouteDev a, int32_t *route_row, int32_t *assist) {
@@ -885,7 +893,7 @@ bool cluster_fits(int64_t C, size_t smem) {
 
 moe_status launch_route_fused(RouteDev &r, int64_t chunks, int64_t *counts, int32_t *offsets,
                               int32_t *recv_cum, int32_t *sched, int32_t *route_row,
-                              int32_t *assist, cudaStream_t stream) {
+                              cudaStream_t stream) {
     const size_t ssm = route_single_smem(r.E, r.P);
     if (r.T * r.K <= kSingleMaxRoutes && ssm <= kSingleSmemMax) {
         static size_t configured = 0;
@@ -897,7 +905,7 @@ moe_status launch_route_fused(RouteDev &r, int64_t chunks, int64_t *counts, int3
         }
         r.rows_final = 1;
         MOE_LAUNCH("route_single", k_route_single, 1, kSingleThreads, ssm, stream, r, counts,
-                   offsets, recv_cum, sched, route_row, assist);
+                   offsets, recv_cum, sched, route_row);
         return MOE_OK;
     }
     // one cluster: ranges of at most 4096 routes, each touching at most
@@ -907,13 +915,12 @@ moe_status launch_route_fused(RouteDev &r, int64_t chunks, int64_t *counts, int3
         const int64_t C = std::min<int64_t>(kClMaxCtas, std::max<int64_t>(2, (n + 1023) / 1024));
         const int64_t per_cta = ((n + C - 1) / C + 31) / 32 * 32;
         const int64_t parts = per_cta / (r.M * r.K) + 2;
-        const size_t csm = route_cluster_smem(r.E);
+        const size_t csm = route_cluster_smem(r.E, C);
         if (per_cta <= kClMaxRoutesPerCta && parts <= kClMaxParts && csm <= kSingleSmemMax &&
             cluster_fits(C, csm)) {
             r.rows_final = 1;
             MOE_LAUNCH_CLUSTER("route_cluster", k_route_cluster, (unsigned)C, kClThreads, csm, stream,
-                               (unsigned)C, r, per_cta, counts, offsets, recv_cum, sched, route_row,
-                               assist);
+                               (unsigned)C, r, per_cta, counts, offsets, recv_cum, sched, route_row);
             return MOE_OK;
         }
     }
@@ -936,7 +943,7 @@ moe_status launch_route_fused(RouteDev &r, int64_t chunks, int64_t *counts, int3
         r.rows_final = 1;
         const int tok = launch_begin("route_fused", stream, (unsigned)chunks);
         cudaError_t err = cudaLaunchKernelEx(&cfg, k_route_fused, r, chunks, counts, offsets,
-                                             recv_cum, sched, route_row, assist);
+                                             recv_cum, sched, route_row);
         if (err == cudaSuccess) err = cudaGetLastError();
         launch_end(tok, stream);
         if (err == cudaSuccess) return MOE_OK;
@@ -950,7 +957,7 @@ moe_status launch_route_fused(RouteDev &r, int64_t chunks, int64_t *counts, int3
 moe_status launch_route_resolve(const RouteDev &r, int32_t *route_row, int32_t *assist,
                                 cudaStream_t stream) {
     const int64_t n = r.T * r.K;
-    if (n == 0 || r.rows_final) return MOE_OK;
+    if (n == 0) return MOE_OK;
     int64_t blocks = (n + 255) / 256;
     const int64_t cap = (int64_t)num_sms() * 8;
     if (blocks > cap) blocks = cap;
