@@ -15,7 +15,10 @@ see the GPU under load), then exactly K steps, each preceded by an untimed L2
 flush (a 512 MiB write) and timed with CUDA events on the launching stream;
 barrier + synchronize on both sides; max over ranks.  A second pass of K steps
 with the library's per-kernel event profiling gives each kernel's average
-duration for the roofline.  `e2e` repeats the step through the same C ABI
+duration for the roofline.  `timing` adds the median of the K step times and,
+for the identity-expert workloads, the step hot in L2 (no flush) and the step
+captured once as a CUDA graph and replayed (flushed and hot), so that launch
+overhead shows separately.  `e2e` repeats the step through the same C ABI
 calls with pinned host inputs: host->device copies, the step, and the
 device->host copy of the output are inside the timed region.
 
@@ -498,6 +501,40 @@ def run_layer_secondary(args, B, dev, stream, flush, pk):
             "unit": "tokens/s", "ms_per_step": ms, "steps": steps, "roofline": roofline, **extra}
 
 
+def timing_variants(path, flush, stream, steps):
+    """The step without the L2 flush (hot L2), and the step captured once as a
+    CUDA graph and replayed, with and without the flush, so that the launch
+    overhead of the eager step shows separately.  Medians over `steps`."""
+    import torch
+
+    def timed(run, flush_each):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for i in range(steps):
+            if flush_each:
+                flush.fill_(1)
+            ev[i][0].record(stream)
+            run()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        return float(np.median([a.elapsed_time(b) for a, b in ev]))
+
+    out = {"hot_l2_ms": timed(path.step, False)}
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            path.step()
+        torch.cuda.synchronize()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        out["graph_ms"] = timed(g.replay, True)
+        out["graph_hot_l2_ms"] = timed(g.replay, False)
+    except Exception as exc:   # reported, not fatal: the eager numbers stand
+        out["graph_error"] = str(exc)[:200]
+    return out
+
+
 def run_ours(args, rank, world, dist):
     import torch
     from combine_route_count_prefix_gb300 import binding as B
@@ -549,6 +586,9 @@ def run_ours(args, rank, world, dist):
     clk = clocks.stop()
     ms_step = max_over_ranks(float(np.mean(ms)), dist, dev)
     value = whole_job_tokens_per_s(T, world, ms_step)
+    timing = {"median_ms": float(np.median(ms))}
+    if w.identity:
+        timing.update(timing_variants(path, flush, stream, args.steps))
 
     # ---------------- per-kernel durations (same K steps, profiled)
     B.profile_enable(True)
@@ -643,6 +683,7 @@ def run_ours(args, rank, world, dist):
                 "copies": "pinned host buffers; neighbouring steps' copies overlap compute on "
                           "their own streams (double-buffered device tensors)"},
         "gpu_launches": launches, "clocks": clk, "routed_rows": R,
+        "timing": timing,
     }
     if step_bytes:
         gbs = step_bytes / (ms_step * 1e-3) / 1e9

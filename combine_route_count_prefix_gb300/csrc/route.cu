@@ -44,6 +44,7 @@
 #include "ptx.cuh"
 
 #include <algorithm>
+#include <mutex>
 #include <cooperative_groups.h>
 
 namespace moe {
@@ -859,8 +860,24 @@ moe_status launch_route(const RouteDev &r, int64_t chunks, int64_t *counts, int3
 }
 
 // Whether a cluster of C CTAs of k_route_cluster with `smem` bytes each can be
-// scheduled (16 CTAs need the non-portable cluster size).
+// scheduled (16 CTAs need the non-portable cluster size).  The answers are
+// cached per (C, smem): the occupancy query is a driver call.
+bool cluster_fits_query(int64_t C, size_t smem);
 bool cluster_fits(int64_t C, size_t smem) {
+    struct Entry { int64_t C; size_t smem; bool ok; };
+    static std::mutex mu;
+    static Entry cache[8];
+    static int used = 0, next = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+        if (cache[i].C == C && cache[i].smem == smem) return cache[i].ok;
+    const bool ok = cluster_fits_query(C, smem);
+    cache[next] = Entry{C, smem, ok};
+    next = (next + 1) % 8;
+    if (used < 8) ++used;
+    return ok;
+}
+bool cluster_fits_query(int64_t C, size_t smem) {
     static size_t configured = 0;
     if (smem > configured) {
         if (cudaFuncSetAttribute(k_route_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize,
