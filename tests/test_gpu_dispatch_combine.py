@@ -46,6 +46,13 @@ CASES = {
     # shared memory and too many partitions per cluster CTA: the per-chunk
     # kernel with the grid barrier
     "wide_partitions": wl.custom(P=64, M=4, H=64, E=1024, K=8, mask_kind=1, mask_p=0.9),
+    # rows wider than one register pass of the row copy (8192 elements), with a
+    # ragged second pass, and combine segments that do not divide the row
+    "wide_hidden": wl.custom(P=2, M=40, H=12296, E=16, K=3, mask_kind=1, mask_p=0.8,
+                             has_shared=True),
+    # seven combine segments per row
+    "very_wide": wl.custom(P=1, M=24, H=24576, E=32, K=8, mask_kind=2, mask_p=0.9,
+                           has_shared=True),
 }
 
 
