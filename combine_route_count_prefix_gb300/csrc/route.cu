@@ -36,9 +36,15 @@
 //                  call's status word.
 // The final row, base[chunk][e] + rank in chunk, is resolved by the kernel
 // that next touches each token (row copy, quantisation, or k_route_resolve
-// when no rows are copied), which also writes the triplet of the row.  The
-// single-kernel forms below write final rows themselves; the triplets are
-// still written by that next kernel.
+// when no rows are copied), which also writes the triplet of the row.
+// Single-kernel forms, which write the final rows themselves (the triplets
+// still come from that next kernel):
+//   k_route_single   one CTA, at most 2048 routes
+//   k_route_cluster  one thread-block cluster of up to 16 CTAs, at most 65536
+//                    routes; a hardware cluster barrier and distributed
+//                    shared memory replace the grid barrier
+//   k_route_fused    one cooperative CTA per chunk with a grid barrier, while
+//                    all chunks fit on the GPU at once
 // No global atomics decide a position, so the result is deterministic.
 #include "common.cuh"
 #include "ptx.cuh"
