@@ -55,6 +55,24 @@ void launch_end(int token, cudaStream_t stream) {
     if (token < (int)g_records.size()) cudaEventRecord(g_records[token].stop, stream);
 }
 
+bool set_smem_limit(const void *kernel, size_t bytes) {
+    static std::mutex mu;
+    static std::vector<std::pair<const void *, size_t>> done;
+    std::lock_guard<std::mutex> lk(mu);
+    size_t *have = nullptr;
+    for (auto &d : done)
+        if (d.first == kernel) have = &d.second;
+    if (have && *have >= bytes) return true;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (have) *have = bytes;
+    else done.emplace_back(kernel, bytes);
+    return true;
+}
+
 int num_sms() {
     static int cached[64] = {0};
     int dev = 0;

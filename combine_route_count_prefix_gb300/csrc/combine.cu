@@ -410,14 +410,8 @@ moe_status launch_combine(const void *y, const int32_t *route_row, const float *
     a.tokens_per_cta = 0;
     a.status = status;
     const size_t smem = smem_bytes(a.K, a.slots, a.stages, a.seg_vecs);
-    static size_t configured[2] = {0, 0};
-    if (smem > configured[special]) {
-        if (cudaFuncSetAttribute(special ? k_combine<true> : k_combine<false>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        configured[special] = smem;
-    }
+    if (!set_smem_limit(special ? (const void *)k_combine<true> : (const void *)k_combine<false>, smem))
+        return MOE_ERR_CUDA;
     if (special) {
         MOE_LAUNCH("combine", k_combine<true>, (unsigned)grid, kThreads, smem, stream, a);
     } else {

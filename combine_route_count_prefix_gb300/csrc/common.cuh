@@ -28,6 +28,9 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // and, when profiling is on, bracket the launch with a CUDA event pair recorded
 // on the launching stream.
 int launch_begin(const char *name, cudaStream_t stream, unsigned grid);
+// Raises a kernel's dynamic shared-memory limit to at least `bytes`, once per
+// kernel and size (thread-safe); false if the runtime refuses.
+bool set_smem_limit(const void *kernel, size_t bytes);
 void launch_end(int token, cudaStream_t stream);
 int num_sms();
 

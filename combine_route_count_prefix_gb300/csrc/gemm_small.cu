@@ -441,13 +441,7 @@ k_gemm_small(const __grid_constant__ CUtensorMap tmRows, const __grid_constant__
 template <int EPI>
 moe_status launch_small_epi(const CUtensorMap &mr, const CUtensorMap &mw, const SmallDev &d,
                             cudaStream_t stream) {
-    static bool configured = false;
-    if (!configured) {
-        if (cudaFuncSetAttribute(k_gemm_small<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)SMEM_BYTES) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        configured = true;
-    }
+    if (!set_smem_limit((const void *)k_gemm_small<EPI>, SMEM_BYTES)) return MOE_ERR_CUDA;
     const char *names[3] = {"gemm_s32_small", "gemm1_swiglu_small", "gemm2_dequant_small"};
     MOE_LAUNCH(names[EPI], k_gemm_small<EPI>, num_sms(), THREADS, SMEM_BYTES, stream, mr, mw, d);
     return MOE_OK;

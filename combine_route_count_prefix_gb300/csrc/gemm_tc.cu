@@ -921,13 +921,7 @@ k_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 template <int EPI>
 moe_status launch_epi(const CUtensorMap &ma, const CUtensorMap &mb, const GemmDev &d,
                       cudaStream_t stream) {
-    static bool configured = false;
-    if (!configured) {
-        if (cudaFuncSetAttribute(k_grouped_gemm<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)SMEM_BYTES) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        configured = true;
-    }
+    if (!set_smem_limit((const void *)k_grouped_gemm<EPI>, SMEM_BYTES)) return MOE_ERR_CUDA;
     const char *names[3] = {"gemm_s32", "gemm1_swiglu", "gemm2_dequant"};
     MOE_LAUNCH(names[EPI], k_grouped_gemm<EPI>, num_sms(), THREADS, SMEM_BYTES, stream, ma, mb, d);
     return MOE_OK;
@@ -1071,13 +1065,7 @@ moe_status launch_ffn_fused(const GemmArgs &g1, const GemmArgs &g2, void *q2, fl
     d.done1 = done1;
     d.ready2 = ready2;
     d.Nh4 = (int)(g2.Kd / 4);
-    static bool configured = false;
-    if (!configured) {
-        if (cudaFuncSetAttribute(k_ffn_fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)SMEM_BYTES) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        configured = true;
-    }
+    if (!set_smem_limit((const void *)k_ffn_fused, SMEM_BYTES)) return MOE_ERR_CUDA;
     if (cudaMemsetAsync(done1, 0, flag_bytes, stream) != cudaSuccess ||
         cudaMemsetAsync(ready2, 0, flag_bytes, stream) != cudaSuccess)
         return MOE_ERR_CUDA;

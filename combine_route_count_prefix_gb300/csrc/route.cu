@@ -919,13 +919,7 @@ moe_status launch_route_fused(RouteDev &r, int64_t chunks, int64_t *counts, int3
                               cudaStream_t stream) {
     const size_t ssm = route_single_smem(r.E, r.P);
     if (r.T * r.K <= kSingleMaxRoutes && ssm <= kSingleSmemMax) {
-        static size_t configured = 0;
-        if (ssm > configured) {
-            if (cudaFuncSetAttribute(k_route_single, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)ssm) != cudaSuccess)
-                return MOE_ERR_CUDA;
-            configured = ssm;
-        }
+        if (!set_smem_limit((const void *)k_route_single, ssm)) return MOE_ERR_CUDA;
         r.rows_final = 1;
         MOE_LAUNCH("route_single", k_route_single, 1, kSingleThreads, ssm, stream, r, counts,
                    offsets, recv_cum, sched, route_row);
