@@ -18,7 +18,8 @@ with the library's per-kernel event profiling gives each kernel's average
 duration for the roofline.  `timing` adds the median of the K step times and,
 for the identity-expert workloads, the step hot in L2 (no flush) and the step
 captured once as a CUDA graph and replayed (flushed and hot), so that launch
-overhead shows separately.  `e2e` repeats the step through the same C ABI
+overhead shows separately; `dispatch_quant` times moe_dispatch_quant (int8 rows
+and per-row scales) on the same inputs.  `e2e` repeats the step through the same C ABI
 calls with pinned host inputs: host->device copies, the step, and the
 device->host copy of the output are inside the timed region.
 
@@ -501,6 +502,41 @@ def run_layer_secondary(args, B, dev, stream, flush, pk):
             "unit": "tokens/s", "ms_per_step": ms, "steps": steps, "roofline": roofline, **extra}
 
 
+def quant_dispatch_item(B, path, w, inp, flush, stream, steps, pk):
+    """moe_dispatch_quant (int8 rows + per-row dynamic scales) on the same
+    inputs: its own event-timed calls, each after the L2 flush, and its HBM
+    rate against the measured peak.  Algorithmic bytes: ids + mask, x once per
+    token with an active route, R int8 rows + R scales, route_row, triplets."""
+    import torch
+    T, K, H = w.num_tokens, w.topk, w.hidden
+    d = B.dispatch_quant(path.x, path.ids, w.num_experts, w.num_partitions, mask=path.mask)
+    ws = d["workspace"]
+    for _ in range(3):
+        B.dispatch_quant(path.x, path.ids, w.num_experts, w.num_partitions, mask=path.mask, ws=ws, out=d)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for i in range(steps):
+        flush.fill_(1)
+        ev[i][0].record(stream)
+        B.dispatch_quant(path.x, path.ids, w.num_experts, w.num_partitions, mask=path.mask, ws=ws, out=d)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    us = float(np.mean([a.elapsed_time(b) for a, b in ev])) * 1e3
+    R = int(d["expert_offsets"][-1].item())
+    mask = inp["mask"]
+    act = np.ones((T, K), bool)
+    if mask is not None:
+        act &= (mask[:, None] if mask.ndim == 1 else mask).astype(bool)
+    tok_active = int(act.any(axis=1).sum())
+    nbytes = (T * K * 4 + (0 if mask is None else mask.size) + tok_active * 2 * H + R * H + R * 4
+              + T * K * 4 + R * 12)
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"us_per_call": us, "algorithmic_bytes": nbytes, "gbs": gbs,
+            "frac_of_hbm_peak": gbs / pk["hbm_gbs"], "rows": R,
+            "note": "routing + int8 rows + per-row scales; event-timed per call after an L2 flush"}
+
+
 def timing_variants(path, flush, stream, steps):
     """The step without the L2 flush (hot L2), and the step captured once as a
     CUDA graph and replayed, with and without the flush, so that the launch
@@ -600,6 +636,8 @@ def run_ours(args, rank, world, dist):
     prof = B.profile_report()
     pk = peaks()
     roofline, step_bytes, extra = path.roofline(prof, pk)
+    quant_item = (quant_dispatch_item(B, path, w, inp, flush, stream, args.steps, pk)
+                  if w.identity and w.hidden <= 8192 else None)
     roofline["per_kernel_us"] = {k: round(ms_ / n * 1e3, 3) for k, (n, ms_) in prof.items()}
     roofline["per_kernel_grid"] = dict(B.LAST_GRIDS)
 
@@ -692,6 +730,8 @@ def run_ours(args, rank, world, dist):
     line.update({k: v for k, v in extra.items() if v is not None})
     if secondary is not None:
         line["full_layer"] = secondary
+    if quant_item is not None:
+        line["dispatch_quant"] = quant_item
     print(json.dumps(line), flush=True)
 
 

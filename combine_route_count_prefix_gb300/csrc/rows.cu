@@ -206,33 +206,50 @@ k_dispatch_quant(RouteDev ra, const uint4 *__restrict__ x, const float4 *__restr
     __shared__ int32_t experts[kMaxTopK];
     __shared__ int32_t nrows;
     __shared__ float scratch[32];
-    pdl_wait();
     const int K = (int)ra.K;
-    for (int64_t t = blockIdx.x; t < ra.T; t += gridDim.x) {
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            int n = 0;
-            for (int k = 0; k < K; ++k) {
-                const int32_t r = resolve_route_row(ra, t, k, route_row, assist);
-                if (r >= 0) {
-                    rows[n] = r;
-                    experts[n] = ra.ids[t * K + k];
-                    ++n;
-                }
-            }
-            nrows = n;
+    // The token's row is read before its route rows are resolved, and the first
+    // token's before the wait on the routing kernel (x and the mask are inputs
+    // nothing in flight writes); a token the mask switches off entirely is not
+    // read.  The route rows are resolved by one lane per slot, in parallel.
+    uint4 raw[kVec];
+    auto load_row = [&](int64_t t) {
+        bool on = t < ra.T;
+        if (on && ra.mask_kind == 1) on = ra.mask[t] != 0;
+        if (on && ra.mask_kind == 2) {
+            bool any = false;
+            for (int k = 0; k < K; ++k) any = any || ra.mask[t * K + k] != 0;
+            on = any;
         }
-        __syncthreads();
-        const int n = nrows;
-        if (n == 0) continue;
-        float f[kVec][8];
 #pragma unroll
         for (int u = 0; u < kVec; ++u) {
             const int64_t j = threadIdx.x + (int64_t)u * kRowThreads;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (j < H8) v = ld_stream(x + t * H8 + j);
-            unpack_bf16x8(v, f[u]);
+            raw[u] = (on && j < H8) ? ld_stream(x + t * H8 + j) : make_uint4(0, 0, 0, 0);
         }
+    };
+    load_row(blockIdx.x);
+    pdl_wait();
+    for (int64_t t = blockIdx.x; t < ra.T; t += gridDim.x) {
+        if (t != blockIdx.x) load_row(t);
+        __syncthreads();   // the previous token's rows are no longer read
+        if (threadIdx.x < 32) {
+            // lane k resolves slot k; the active rows are packed in slot order
+            const int k = threadIdx.x;
+            const int32_t e = k < K ? ra.ids[t * K + k] : 0;
+            const int32_t r = k < K ? resolve_route_row(ra, t, k, route_row, assist) : -1;
+            const uint32_t act = __ballot_sync(kFull, r >= 0);
+            if (r >= 0) {
+                const int pos = __popc(act & lanemask_lt());
+                rows[pos] = r;
+                experts[pos] = e;
+            }
+            if (k == 0) nrows = __popc(act);
+        }
+        __syncthreads();
+        const int n = nrows;
+        float f[kVec][8];
+#pragma unroll
+        for (int u = 0; u < kVec; ++u) unpack_bf16x8(raw[u], f[u]);
+        if (n == 0) continue;
         for (int d = 0; d < (kSmooth ? n : 1); ++d) {
             float v[kVec][8];
             float amax = 0.0f;
