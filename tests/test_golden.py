@@ -133,3 +133,56 @@ def test_gpu_quant_golden(B):
     for t, r in enumerate(rows):                                      # row t holds token t
         assert s[t] == r["s"]
         np.testing.assert_array_equal(q[t], np.array(r["q"], np.int8))
+
+
+# ---------------------------------------------------------------- zero and copy experts
+
+def _special_inputs():
+    g = _load("special_experts.json")
+    ids = np.array(g["expert_ids"], np.int32)
+    H = g["hidden"]
+    x = np.repeat(np.array(g["x_rows"], np.float32)[:, None], H, axis=1)
+    probs = np.array(g["expert_scales"], np.float32)
+    shared = np.full_like(x, g["shared_value"])
+    return g, ids, x, probs, shared
+
+
+def test_oracle_special_experts_golden():
+    g, ids, x, probs, shared = _special_inputs()
+    exp, H = g["expected"], g["hidden"]
+    r = oracle.route(ids, g["num_experts"], g["num_partitions"], None,
+                     zero_experts=g["zero_experts"], copy_experts=g["copy_experts"])
+    np.testing.assert_array_equal(r["counts"], np.array(exp["counts"], np.int64))
+    np.testing.assert_array_equal(r["offsets"], np.array(exp["offsets"], np.int32))
+    np.testing.assert_array_equal(r["recv_cum"], np.array(exp["recv_cum"], np.int32))
+    np.testing.assert_array_equal(r["route_row"], np.array(exp["route_row"], np.int32))
+    np.testing.assert_array_equal(r["assist"], np.array(exp["assist"], np.int32).reshape(-1, 3))
+    xb = _bf16_bits(x)
+    y = oracle.gather(xb, r["route_row"], ids.shape[1], r["R"])   # identity expert
+    for sh, key in ((None, "out_no_shared"), (_bf16_bits(shared), "out_with_shared")):
+        out = oracle.combine(y, r["route_row"], probs, sh, ori_x=xb)
+        want = _bf16_bits(np.repeat(np.array(exp[key], np.float32)[:, None], H, axis=1))
+        np.testing.assert_array_equal(out, want)
+
+
+@pytest.mark.gpu
+def test_gpu_special_experts_golden(B):
+    g, ids, x, probs, shared = _special_inputs()
+    exp, H = g["expected"], g["hidden"]
+    E, P, Z, C = g["num_experts"], g["num_partitions"], g["zero_experts"], g["copy_experts"]
+    xd = torch.from_numpy(x).cuda().to(torch.bfloat16)
+    d = B.dispatch(xd, torch.from_numpy(ids).cuda(), E, P, zero_experts=Z, copy_experts=C)
+    torch.cuda.synchronize()
+    R = exp["offsets"][-1]
+    np.testing.assert_array_equal(d["expert_token_nums"].cpu().numpy(), exp["counts"])
+    np.testing.assert_array_equal(d["expert_offsets"].cpu().numpy(), exp["offsets"])
+    np.testing.assert_array_equal(d["ep_recv_counts"].cpu().numpy(), exp["recv_cum"])
+    np.testing.assert_array_equal(d["route_row"].cpu().numpy(), exp["route_row"])
+    np.testing.assert_array_equal(d["assist"][:R].cpu().numpy(), np.array(exp["assist"]).reshape(-1, 3))
+    pd = torch.from_numpy(probs).cuda()
+    for sh, key in ((None, "out_no_shared"), (shared, "out_with_shared")):
+        shd = None if sh is None else torch.from_numpy(sh).cuda().to(torch.bfloat16)
+        out = B.combine(d["expand_x"], d["route_row"], pd, E, P, shared=shd, ori_x=xd,
+                        zero_experts=Z, copy_experts=C)
+        want = np.repeat(np.array(exp[key], np.float32)[:, None], H, axis=1)
+        np.testing.assert_array_equal(out.float().cpu().numpy(), want)
