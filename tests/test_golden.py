@@ -186,3 +186,34 @@ def test_gpu_special_experts_golden(B):
                         zero_experts=Z, copy_experts=C)
         want = np.repeat(np.array(exp[key], np.float32)[:, None], H, axis=1)
         np.testing.assert_array_equal(out.float().cpu().numpy(), want)
+
+
+# ---------------------------------------------------------------- quantised dispatch
+
+def _dq_inputs():
+    g = _load("dispatch_quant_smooth.json")
+    return (g, np.array(g["expert_ids"], np.int32), np.array(g["x"], np.float32),
+            np.array(g["smooth"], np.float32))
+
+
+def test_oracle_dispatch_quant_golden():
+    g, ids, x, smooth = _dq_inputs()
+    r = oracle.route(ids, g["num_experts"], g["num_partitions"])
+    for sm, key in ((smooth, "expected_smooth"), (None, "expected_plain")):
+        q, sc = oracle.dispatch_quant(_bf16_bits(x), ids, r["route_row"], r["R"], sm)
+        np.testing.assert_array_equal(q, np.array(g[key]["q"], np.int8))
+        np.testing.assert_array_equal(sc, np.array(g[key]["s"], np.float32))
+
+
+@pytest.mark.gpu
+def test_gpu_dispatch_quant_golden(B):
+    g, ids, x, smooth = _dq_inputs()
+    xd = torch.from_numpy(x).cuda().to(torch.bfloat16)
+    for sm, key in ((smooth, "expected_smooth"), (None, "expected_plain")):
+        d = B.dispatch_quant(xd, torch.from_numpy(ids).cuda(), g["num_experts"], g["num_partitions"],
+                             smooth=None if sm is None else torch.from_numpy(sm).cuda())
+        torch.cuda.synchronize()
+        R = len(g[key]["s"])
+        np.testing.assert_array_equal(d["expand_x"][:R].cpu().numpy(), np.array(g[key]["q"], np.int8))
+        np.testing.assert_array_equal(d["dynamic_scales"][:R].cpu().numpy(),
+                                      np.array(g[key]["s"], np.float32))
