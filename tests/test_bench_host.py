@@ -1,0 +1,76 @@
+"""Host-side pieces of bench.py that the reported numbers rest on: the
+algorithmic byte counts of the identity-expert step, the ncu traffic table
+lookup (keyed by the kernel source's hash), the whole-job rate and the peaks."""
+import json
+import os
+import sys
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from combine_route_count_prefix_gb300 import workloads as wl  # noqa: E402
+
+
+def test_identity_bytes_by_hand():
+    # 4 tokens, K = 2, H = 8, token mask [1, 1, 0, 1], shared expert
+    w = wl.custom(P=2, M=2, H=8, E=3, K=2, mask_kind=1, mask_p=0.5, has_shared=True)
+    inp = {"mask": np.array([1, 1, 0, 1], np.uint8), "shared": np.zeros((4, 8), np.uint16)}
+    R = 6                                    # the active routes of the three unmasked tokens
+    b = bench.identity_bytes(w, inp, R)
+    row = 8 * 2
+    assert b["dispatch_rows"] == 3 * row + R * row + 4 * 2 * 4          # x once, rows, route_row
+    assert b["routing"] == 4 * 2 * 4 + 4 + 4 * 2 * 4 + R * 12          # ids, mask, route_row, triplets
+    assert b["combine"] == R * row + 4 * row * 2 + 4 * 2 * 8 + 4        # rows, shared + out, probs + route_row, mask
+    assert b["total"] == b["dispatch_rows"] + b["routing"] + b["combine"]
+
+
+def test_identity_bytes_route_mask_counts_tokens_with_any_active_route():
+    w = wl.custom(P=1, M=3, H=8, E=4, K=2, mask_kind=2, mask_p=0.5)
+    inp = {"mask": np.array([[0, 0], [1, 0], [0, 1]], np.uint8), "shared": None}
+    b = bench.identity_bytes(w, inp, 2)
+    assert b["dispatch_rows"] == 2 * 16 + 2 * 16 + 3 * 2 * 4
+
+
+def test_whole_job_rate_is_weak_scaling():
+    assert bench.whole_job_tokens_per_s(2048, 1, 0.1) == pytest.approx(2048 / 1e-4)
+    assert bench.whole_job_tokens_per_s(2048, 4, 0.1) == pytest.approx(4 * 2048 / 1e-4)
+
+
+def test_recorded_traffic_follows_the_source_hash(monkeypatch):
+    # every row of the table resolves while its source is unchanged ...
+    rows = []
+    for line in open(os.path.join(ROOT, "profiles", "traffic.md")):
+        parts = [p.strip() for p in line.strip().strip("|").split("|")]
+        if len(parts) >= 5 and parts[2].endswith(".cu"):
+            rows.append((parts[0], parts[1]))
+    assert rows
+    for kernel, workload in rows:
+        v = bench.recorded_traffic(kernel, workload)
+        assert v is not None and v > 0, (kernel, workload)
+    # ... and turns null as soon as the source differs
+    monkeypatch.setattr(bench, "source_hash", lambda *names: "000000000000")
+    for kernel, workload in rows:
+        assert bench.recorded_traffic(kernel, workload) is None
+    assert bench.recorded_traffic("no_such_kernel", "decode_dispatch_combine") is None
+
+
+def test_peaks_read_the_measured_file_when_present():
+    p = bench.peaks()
+    assert p["hbm_gbs"] > 0 and p["bf16_tflops"] > 0 and p["bf16_tflops_sustained"] > 0
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        assert p["source"] == "measured" and p["hbm_gbs"] == float(d["hbm_gbs"])
+    else:
+        assert p["source"] == "fallback"
+
+
+def test_workload_config_names_the_workload():
+    w = wl.WORKLOADS["decode_dispatch_combine"]
+    c = bench.workload_config(w)
+    assert c["workload"] == "decode_dispatch_combine" and c["tokens"] == 2048
+    assert c["mask"] == "per-token" and c["shared_expert"] is True
