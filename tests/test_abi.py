@@ -76,3 +76,66 @@ def test_status_strings(B):
     L = B.lib()
     assert L.moe_status_string(0) == b"ok"
     assert L.moe_status_string(561003) == b"workspace too small"
+
+
+# Host-side validation with fake device addresses: every case below fails a check
+# that runs before any CUDA call, so no pointer is dereferenced and no GPU is needed.
+# They run only where there is no GPU, so that a check moved behind a launch could
+# never hand a kernel a fake address.
+def _no_gpu():
+    import torch
+    return not torch.cuda.is_available()
+
+
+host_only = pytest.mark.skipif(not _no_gpu(), reason="fake device addresses: host-only checks")
+A = ctypes.c_void_p(1 << 20)           # 1 MiB: aligned for every requirement
+A2 = ctypes.c_void_p(2 << 20)
+MIS = ctypes.c_void_p((1 << 20) + 8)   # 8-byte aligned only
+
+
+def _dispatch(L, s, x=A, mask=None, ws=A2, ws_bytes=1 << 30):
+    return L.moe_dispatch(ctypes.byref(s), x, A, mask, A, A, A, A, A, A, ws,
+                          ctypes.c_size_t(ws_bytes), None)
+
+
+@host_only
+def test_dispatch_argument_checks_before_launch(B):
+    L = B.lib()
+    s = B.make_shape(16, 2, 128, 8, 2)
+    assert _dispatch(L, s, mask=A) == 161002                    # a mask with mask_kind 0
+    s1 = B.make_shape(16, 2, 128, 8, 2, mask_kind=1)
+    assert _dispatch(L, s1, mask=None) == 161001                # mask_kind 1 without a mask
+    assert _dispatch(L, s, x=MIS) == 561004                     # x not 16-byte aligned
+    assert _dispatch(L, s, ws=MIS) == 561004                    # workspace not 1024-aligned
+    need = B.dispatch_workspace_size(s)
+    assert _dispatch(L, s, ws_bytes=need - 1) == 561003         # workspace one byte short
+
+
+@host_only
+def test_combine_argument_checks_before_launch(B):
+    L = B.lib()
+    s = B.make_shape(16, 2, 128, 8, 2)
+    # no shared term declared, one given
+    assert L.moe_combine(ctypes.byref(s), A, A, A, None, A, None, A, None) == 161002
+    sh = B.make_shape(16, 2, 128, 8, 2, has_shared=True)
+    # shared term declared, none given
+    assert L.moe_combine(ctypes.byref(sh), A, A, A, None, None, None, A, None) == 161001
+    # output not 16-byte aligned
+    assert L.moe_combine(ctypes.byref(s), A, A, A, None, None, None, MIS, None) == 561004
+
+
+@host_only
+def test_layer_argument_checks_before_launch(B):
+    L = B.lib()
+    s = B.make_shape(16, 2, 128, 8, 2, 256)
+
+    def layer(shape, w1=A, ws=A2, ws_bytes=1 << 40, shared=None):
+        return L.moe_layer(ctypes.byref(shape), A, A, A, None, shared, w1, A, A, A, A, ws,
+                           ctypes.c_size_t(ws_bytes), None)
+
+    assert layer(s, shared=A) == 161002                          # shared term not declared
+    assert layer(s, w1=MIS) == 561004                            # packed weights not 1024-aligned
+    need = B.layer_workspace_size(s)
+    assert layer(s, ws_bytes=need - 1) == 561003
+    d = B.make_shape(16, 2, 128, 8, 2)                           # N = 0: no FFN to run
+    assert layer(d) == 561002
