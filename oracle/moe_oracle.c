@@ -32,7 +32,8 @@
  *
  * Parity pins: every function below is checked by the CPU test suite against
  * something other than itself (library restatements, closed forms,
- * brute force, invariants).  The FFN's numeric conventions above are pinned
+ * brute force, invariants, and small fixtures worked by hand from the cited
+ * definitions).  The FFN's numeric conventions above are pinned
  * only by those readings, not by a value printed on the pages: for them
  * parity is "unpinned" in the sense that the pages print no number to match.
  */
