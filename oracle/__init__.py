@@ -5,9 +5,13 @@ benchmark's CPU-baseline leg may import this package.  The product path (the
 CUDA library and its Python binding) never calls it, and this package imports
 nothing from the product package.
 
-The arithmetic lives in ``moe_oracle.c`` (plain C, single-threaded, compiled
-with ``-O2 -ffp-contract=off`` and no fast-math).  This module only compiles it
-and marshals numpy arrays.  bf16 tensors travel as ``uint16`` bit patterns.
+The arithmetic lives in ``moe_oracle.c`` (plain C, compiled with ``-O2
+-ffp-contract=off`` and no fast-math).  Each token and each row is computed by
+one thread; the ``*_mt`` drivers only cut the tokens or rows into contiguous
+slices and run the unchanged per-token / per-row functions on them in
+parallel (``threads`` arguments; 0 = all host cores).  This module only
+compiles the C and marshals numpy arrays.  bf16 tensors travel as ``uint16``
+bit patterns.
 
 Pages cited in the C source:
   "dispatch_combine_shmem.py" (TileLang-Ascend dispatch/combine example),
@@ -35,7 +39,7 @@ def build(force: bool = False) -> str:
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-pthread",
            "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
@@ -73,9 +77,21 @@ def _load():
     lib.oracle_layer_tokens.argtypes = [I64, I64, I64, I64, I64, I64, I64, P, P, ctypes.c_int,
                                         P, P, P, P, P, P, P, I64, P, P]
     lib.oracle_layer_tokens.restype = ctypes.c_int
-    lib.oracle_identity_tokens.argtypes = [I64, I64, I64, I64, I64, I64, P, P, ctypes.c_int,
-                                           P, P, P, I64, P, P]
-    lib.oracle_identity_tokens.restype = None
+    lib.oracle_f32_to_bf16_n.argtypes = [I64, P, P]
+    lib.oracle_f32_to_bf16_n.restype = None
+    lib.oracle_bf16_to_f32_n.argtypes = [I64, P, P]
+    lib.oracle_bf16_to_f32_n.restype = None
+    INT = ctypes.c_int
+    lib.oracle_gather_mt.argtypes = [I64, I64, I64, P, P, P, INT]
+    lib.oracle_gather_mt.restype = None
+    lib.oracle_combine_mt.argtypes = [I64, I64, I64, P, P, P, P, P, P, INT]
+    lib.oracle_combine_mt.restype = None
+    lib.oracle_layer_tokens_mt.argtypes = [I64, I64, I64, I64, I64, I64, I64, P, P, INT,
+                                           P, P, P, P, P, P, P, I64, P, P, INT]
+    lib.oracle_layer_tokens_mt.restype = INT
+    lib.oracle_ffn_rows_mt.argtypes = [I64, I64, I64, P, P, P, P, P, P, P,
+                                       P, P, P, P, P, P, INT]
+    lib.oracle_ffn_rows_mt.restype = INT
     lib.oracle_dispatch_quant.argtypes = [I64, I64, I64, P, P, P, P, P, P]
     lib.oracle_dispatch_quant.restype = None
     _lib = lib
@@ -91,6 +107,16 @@ def _p(a):
 
 def _c(a, dtype):
     return None if a is None else np.ascontiguousarray(a, dtype=dtype)
+
+
+def _threads(threads):
+    """0 or None: every host core."""
+    return int(threads) if threads else (os.cpu_count() or 1)
+
+
+def host_threads() -> int:
+    """Threads the ``*_mt`` drivers use by default (the host's core count)."""
+    return _threads(0)
 
 
 def _mask_kind(mask, T, K):
@@ -109,19 +135,22 @@ def _mask_kind(mask, T, K):
 # --------------------------------------------------------------------------
 
 def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
-    """Vector form of the oracle's bf16 widening (uint16 -> float32)."""
+    """The oracle's bf16 widening, element by element (uint16 -> float32)."""
     lib = _load()
-    flat = np.ascontiguousarray(bits, dtype=np.uint16).ravel()
-    return np.array([lib.oracle_bf16_to_f32(int(b)) for b in flat],
-                    dtype=np.float32).reshape(np.shape(bits))
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.zeros(b.shape, np.float32)
+    lib.oracle_bf16_to_f32_n(b.size, _p(b), _p(out))
+    return out
 
 
 def f32_to_bf16(vals: np.ndarray) -> np.ndarray:
-    """Vector form of the oracle's round-to-nearest-even narrowing."""
+    """The oracle's round-to-nearest-even narrowing, element by element.
+    The float32 words reach the C code unchanged (signalling NaNs included)."""
     lib = _load()
-    flat = np.ascontiguousarray(vals, dtype=np.float32).ravel()
-    return np.array([lib.oracle_f32_to_bf16(float(v)) for v in flat],
-                    dtype=np.uint16).reshape(np.shape(vals))
+    v = np.ascontiguousarray(vals, dtype=np.float32)
+    out = np.zeros(v.shape, np.uint16)
+    lib.oracle_f32_to_bf16_n(v.size, _p(v), _p(out))
+    return out
 
 
 def silu(v: float) -> float:
@@ -158,14 +187,18 @@ def route(ids: np.ndarray, num_experts: int, num_partitions: int, mask=None, zer
                 num_invalid=int(ninv[0]))
 
 
-def gather(x: np.ndarray, route_row: np.ndarray, K: int, rows: int) -> np.ndarray:
-    """expand_x[r] = x[token of r] (bf16 bit copy).  Returns uint16 [rows, H]."""
+def gather(x: np.ndarray, route_row: np.ndarray, K: int, rows: int, threads=1) -> np.ndarray:
+    """expand_x[r] = x[token of r] (bf16 bit copy).  Returns uint16 [rows, H].
+    threads > 1 (0 = all cores) splits the tokens over threads."""
     lib = _load()
     x = _c(x, np.uint16)
     T, H = x.shape
     rr = _c(route_row, np.int32)
     out = np.zeros((max(rows, 0), H), np.uint16)
-    lib.oracle_gather(T, H, int(K), _p(x), _p(rr), _p(out) if rows > 0 else None)
+    if rows > 0 and _threads(threads) > 1:
+        lib.oracle_gather_mt(T, H, int(K), _p(x), _p(rr), _p(out), _threads(threads))
+    else:
+        lib.oracle_gather(T, H, int(K), _p(x), _p(rr), _p(out) if rows > 0 else None)
     return out
 
 
@@ -226,9 +259,10 @@ def grouped_gemm_s32(offsets, A, W):
     return C, bool(ovf)
 
 
-def combine(y, route_row, probs, shared=None, ori_x=None):
+def combine(y, route_row, probs, shared=None, ori_x=None, threads=1):
     """out[t] = bf16(sum_k probs*y[row] + shared); zero-expert slots add
-    probs*0, copy-expert slots probs*ori_x[t].  Returns uint16 [T, H]."""
+    probs*0, copy-expert slots probs*ori_x[t].  Returns uint16 [T, H].
+    threads > 1 (0 = all cores) splits the tokens over threads."""
     lib = _load()
     y = _c(y, np.uint16)
     probs = _c(probs, np.float32)
@@ -238,13 +272,18 @@ def combine(y, route_row, probs, shared=None, ori_x=None):
     sh = _c(shared, np.uint16)
     ox = _c(ori_x, np.uint16)
     out = np.zeros((T, H), np.uint16)
-    lib.oracle_combine(T, H, K, _p(y), _p(rr), _p(probs), _p(sh), _p(ox), _p(out))
+    if _threads(threads) > 1:
+        lib.oracle_combine_mt(T, H, K, _p(y), _p(rr), _p(probs), _p(sh), _p(ox), _p(out),
+                              _threads(threads))
+    else:
+        lib.oracle_combine(T, H, K, _p(y), _p(rr), _p(probs), _p(sh), _p(ox), _p(out))
     return out
 
 
 def layer_tokens(x, ids, probs, w1, scale1, w2, scale2, tokens, mask=None, shared=None,
-                 zero_experts=0, copy_experts=0):
-    """out[t] of the whole layer for the listed tokens (uint16 [n, H])."""
+                 zero_experts=0, copy_experts=0, threads=1):
+    """out[t] of the whole layer for the listed tokens (uint16 [n, H]).
+    threads > 1 (0 = all cores) splits the token list over threads."""
     lib = _load()
     x = _c(x, np.uint16)
     ids = _c(ids, np.int32)
@@ -255,39 +294,55 @@ def layer_tokens(x, ids, probs, w1, scale1, w2, scale2, tokens, mask=None, share
     kind, m = _mask_kind(mask, T, K)
     tok = _c(tokens, np.int64)
     out = np.zeros((tok.shape[0], H), np.uint16)
-    ovf = lib.oracle_layer_tokens(T, H, E, int(zero_experts), int(copy_experts), K, N, _p(x),
-                                  _p(ids), kind, _p(m),
-                                  _p(_c(probs, np.float32)), _p(_c(shared, np.uint16)),
-                                  _p(w1), _p(_c(scale1, np.float32)),
-                                  _p(_c(w2, np.int8)), _p(_c(scale2, np.float32)),
-                                  tok.shape[0], _p(tok), _p(out))
+    args = (T, H, E, int(zero_experts), int(copy_experts), K, N, _p(x), _p(ids), kind, _p(m),
+            _p(_c(probs, np.float32)), _p(_c(shared, np.uint16)), _p(w1),
+            _p(_c(scale1, np.float32)), _p(_c(w2, np.int8)), _p(_c(scale2, np.float32)),
+            tok.shape[0], _p(tok), _p(out))
+    if _threads(threads) > 1:
+        ovf = lib.oracle_layer_tokens_mt(*args, _threads(threads))
+    else:
+        ovf = lib.oracle_layer_tokens(*args)
     return out, bool(ovf)
 
 
-def identity_tokens(x, ids, probs, num_experts, tokens, mask=None, shared=None, zero_experts=0,
-                    copy_experts=0):
-    """out[t] with an identity expert, for the listed tokens (uint16 [n, H])."""
+def ffn_rows(x, tokens, experts, w1, scale1, w2, scale2, threads=0):
+    """Every FFN stage for dispatched rows: row i is token tokens[i] of x run
+    through expert experts[i] (indices into w1 [E', N, H], scale1 [E', N],
+    w2 [E', H, N/2], scale2 [E', H]).  Returns a dict of q1 int8 [n, H],
+    s1 [n], g [n, N/2], q2 int8 [n, N/2], s2 [n], y uint16 [n, H] and
+    overflow.  Rows are split over threads (0 = all cores)."""
     lib = _load()
     x = _c(x, np.uint16)
-    ids = _c(ids, np.int32)
-    T, K = ids.shape
     H = x.shape[1]
-    kind, m = _mask_kind(mask, T, K)
+    w1 = _c(w1, np.int8)
+    E, N, _ = w1.shape
+    Nh = N // 2
     tok = _c(tokens, np.int64)
-    out = np.zeros((tok.shape[0], H), np.uint16)
-    lib.oracle_identity_tokens(T, H, int(num_experts), int(zero_experts), int(copy_experts), K,
-                               _p(x), _p(ids), kind, _p(m),
-                               _p(_c(probs, np.float32)), _p(_c(shared, np.uint16)),
-                               tok.shape[0], _p(tok), _p(out))
-    return out
+    ex = _c(experts, np.int64)
+    n = tok.shape[0]
+    assert ex.shape == (n,) and (n == 0 or (ex.min() >= 0 and ex.max() < E))
+    assert n == 0 or (tok.min() >= 0 and tok.max() < x.shape[0])
+    q1 = np.zeros((n, H), np.int8); s1 = np.zeros(n, np.float32)
+    g = np.zeros((n, Nh), np.float32); q2 = np.zeros((n, Nh), np.int8)
+    s2 = np.zeros(n, np.float32); y = np.zeros((n, H), np.uint16)
+    ovf = 0
+    if n:
+        ovf = lib.oracle_ffn_rows_mt(n, H, N, _p(x), _p(tok), _p(ex), _p(w1),
+                                     _p(_c(scale1, np.float32)), _p(_c(w2, np.int8)),
+                                     _p(_c(scale2, np.float32)), _p(q1), _p(s1), _p(g), _p(q2),
+                                     _p(s2), _p(y), _threads(threads))
+    return dict(q1=q1, s1=s1, g=g, q2=q2, s2=s2, y=y, overflow=bool(ovf))
 
 
 def dispatch_combine_identity(x, ids, probs, num_experts, num_partitions,
-                              mask=None, shared=None, zero_experts=0, copy_experts=0):
+                              mask=None, shared=None, zero_experts=0, copy_experts=0, threads=1):
     """The identity-expert path in full: route, gather, combine (copy experts
-    read x itself).  Returns (route dict, expand_x uint16 [R, H], out uint16 [T, H])."""
+    read x itself).  Returns (route dict, expand_x uint16 [R, H], out uint16 [T, H]).
+    threads > 1 (0 = all cores) splits the gather's and the combine's tokens
+    over threads; routing is one sequential pass."""
     r = route(ids, num_experts, num_partitions, mask, zero_experts, copy_experts)
     T, K = np.shape(ids)
-    ex = gather(x, r["route_row"], K, r["R"])
-    out = combine(ex, r["route_row"], probs, shared, ori_x=x if copy_experts else None)
+    ex = gather(x, r["route_row"], K, r["R"], threads=threads)
+    out = combine(ex, r["route_row"], probs, shared, ori_x=x if copy_experts else None,
+                  threads=threads)
     return r, ex, out

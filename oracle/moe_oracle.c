@@ -38,6 +38,7 @@
  * parity is "unpinned" in the sense that the pages print no number to match.
  */
 #include <math.h>
+#include <pthread.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -65,6 +66,19 @@ uint16_t oracle_f32_to_bf16(float f)
     uint32_t keep_lsb = (u >> 16) & 1u;
     u += 0x7fffu + keep_lsb;
     return (uint16_t)(u >> 16);
+}
+
+/* Array forms of the two conversions, element by element (the values
+ * travel as raw 32-bit words, so a signalling NaN reaches the narrowing
+ * unchanged). */
+void oracle_f32_to_bf16_n(int64_t n, const float *v, uint16_t *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_f32_to_bf16(v[i]);
+}
+
+void oracle_bf16_to_f32_n(int64_t n, const uint16_t *b, float *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_to_f32(b[i]);
 }
 
 /* ------------------------------------------------------------------ */
@@ -469,28 +483,191 @@ int oracle_layer_tokens(int64_t T, int64_t H, int64_t E, int64_t Z, int64_t C,
     return overflow;
 }
 
-/* Identity-expert version of the above (y = the dispatched row itself; a
- * copy expert also returns x[t], a zero expert returns 0):
- * out[t] = bf16(sum_k probs[t,k] * v_k + float(shared[t])). */
-void oracle_identity_tokens(int64_t T, int64_t H, int64_t E, int64_t Z, int64_t C,
-                            int64_t K, const uint16_t *x, const int32_t *ids, int mask_kind,
-                            const uint8_t *mask, const float *probs,
-                            const uint16_t *shared, int64_t n_tokens,
-                            const int64_t *tokens, uint16_t *out_rows)
+/* ------------------------------------------------------------------ */
+/* Threaded drivers.  They add no arithmetic: each worker calls one of   */
+/* the functions above, unchanged, on its own contiguous slice of tokens */
+/* or rows.  Those functions treat every token and every row on its own, */
+/* so the slices together give exactly the result of one call over the   */
+/* whole range, whatever the number of threads.                          */
+/* ------------------------------------------------------------------ */
+
+typedef struct {
+    void (*fn)(void *arg, int64_t lo, int64_t hi, int *flag);
+    void *arg;
+    int64_t lo, hi;
+    int flag;
+} oracle_slice;
+
+static void *oracle_slice_run(void *p)
 {
-    for (int64_t i = 0; i < n_tokens; ++i) {
-        int64_t t = tokens[i];
-        for (int64_t h = 0; h < H; ++h) {
-            float acc = 0.0f;
-            for (int64_t k = 0; k < K; ++k) {
-                int cls = route_class(t, k, K, E, Z, C, ids, mask_kind, mask);
-                if (cls == ROUTE_OFF || cls == ROUTE_INVALID) continue;
-                float v = cls == ROUTE_ZERO ? 0.0f : oracle_bf16_to_f32(x[t * H + h]);
-                float prod = probs[t * K + k] * v;
-                acc = acc + prod;
-            }
-            if (shared) acc = acc + oracle_bf16_to_f32(shared[t * H + h]);
-            out_rows[i * H + h] = oracle_f32_to_bf16(acc);
-        }
+    oracle_slice *j = (oracle_slice *)p;
+    j->fn(j->arg, j->lo, j->hi, &j->flag);
+    return NULL;
+}
+
+/* Runs fn on [0, n) cut into nthreads contiguous slices; returns the OR of
+ * the slices' flags.  A thread that cannot be started runs its slice here. */
+static int oracle_parallel(int64_t n, int nthreads,
+                           void (*fn)(void *, int64_t, int64_t, int *), void *arg)
+{
+    enum { MAX_THREADS = 512 };
+    pthread_t tid[MAX_THREADS];
+    int started[MAX_THREADS];
+    oracle_slice job[MAX_THREADS];
+    if (nthreads > MAX_THREADS) nthreads = MAX_THREADS;
+    if (nthreads > n) nthreads = (int)n;
+    if (nthreads < 1) nthreads = 1;
+    for (int i = 0; i < nthreads; ++i) {
+        job[i].fn = fn;
+        job[i].arg = arg;
+        job[i].lo = n * i / nthreads;
+        job[i].hi = n * (i + 1) / nthreads;
+        job[i].flag = 0;
     }
+    for (int i = 1; i < nthreads; ++i)
+        started[i] = pthread_create(&tid[i], NULL, oracle_slice_run, &job[i]) == 0;
+    oracle_slice_run(&job[0]);
+    int flag = job[0].flag;
+    for (int i = 1; i < nthreads; ++i) {
+        if (started[i]) pthread_join(tid[i], NULL);
+        else oracle_slice_run(&job[i]);
+        flag |= job[i].flag;
+    }
+    return flag;
+}
+
+typedef struct {
+    int64_t H, K;
+    const uint16_t *x;
+    const int32_t *route_row;
+    uint16_t *out;
+} gather_args;
+
+static void gather_slice(void *p, int64_t lo, int64_t hi, int *flag)
+{
+    const gather_args *a = (const gather_args *)p;
+    (void)flag;
+    oracle_gather(hi - lo, a->H, a->K, a->x + lo * a->H, a->route_row + lo * a->K, a->out);
+}
+
+/* oracle_gather with its tokens split over nthreads threads. */
+void oracle_gather_mt(int64_t T, int64_t H, int64_t K, const uint16_t *x,
+                      const int32_t *route_row, uint16_t *out, int nthreads)
+{
+    gather_args a = {H, K, x, route_row, out};
+    oracle_parallel(T, nthreads, gather_slice, &a);
+}
+
+typedef struct {
+    int64_t H, K;
+    const uint16_t *y;
+    const int32_t *route_row;
+    const float *probs;
+    const uint16_t *shared, *ori_x;
+    uint16_t *out;
+} combine_args;
+
+static void combine_slice(void *p, int64_t lo, int64_t hi, int *flag)
+{
+    const combine_args *a = (const combine_args *)p;
+    (void)flag;
+    oracle_combine(hi - lo, a->H, a->K, a->y, a->route_row + lo * a->K, a->probs + lo * a->K,
+                   a->shared ? a->shared + lo * a->H : NULL,
+                   a->ori_x ? a->ori_x + lo * a->H : NULL, a->out + lo * a->H);
+}
+
+/* oracle_combine with its tokens split over nthreads threads. */
+void oracle_combine_mt(int64_t T, int64_t H, int64_t K, const uint16_t *y,
+                       const int32_t *route_row, const float *probs,
+                       const uint16_t *shared, const uint16_t *ori_x, uint16_t *out,
+                       int nthreads)
+{
+    combine_args a = {H, K, y, route_row, probs, shared, ori_x, out};
+    oracle_parallel(T, nthreads, combine_slice, &a);
+}
+
+typedef struct {
+    int64_t T, H, E, Z, C, K, N;
+    const uint16_t *x;
+    const int32_t *ids;
+    int mask_kind;
+    const uint8_t *mask;
+    const float *probs;
+    const uint16_t *shared;
+    const int8_t *w1;
+    const float *scale1;
+    const int8_t *w2;
+    const float *scale2;
+    const int64_t *tokens;
+    uint16_t *out_rows;
+} layer_args;
+
+static void layer_slice(void *p, int64_t lo, int64_t hi, int *flag)
+{
+    const layer_args *a = (const layer_args *)p;
+    *flag |= oracle_layer_tokens(a->T, a->H, a->E, a->Z, a->C, a->K, a->N, a->x, a->ids,
+                                 a->mask_kind, a->mask, a->probs, a->shared, a->w1, a->scale1,
+                                 a->w2, a->scale2, hi - lo, a->tokens + lo,
+                                 a->out_rows + lo * a->H);
+}
+
+/* oracle_layer_tokens with the token list split over nthreads threads.
+ * Returns 1 on an int32 overflow in any accumulator. */
+int oracle_layer_tokens_mt(int64_t T, int64_t H, int64_t E, int64_t Z, int64_t C,
+                           int64_t K, int64_t N,
+                           const uint16_t *x, const int32_t *ids, int mask_kind,
+                           const uint8_t *mask, const float *probs,
+                           const uint16_t *shared,
+                           const int8_t *w1, const float *scale1,
+                           const int8_t *w2, const float *scale2,
+                           int64_t n_tokens, const int64_t *tokens,
+                           uint16_t *out_rows, int nthreads)
+{
+    layer_args a = {T, H, E, Z, C, K, N, x, ids, mask_kind, mask, probs, shared,
+                    w1, scale1, w2, scale2, tokens, out_rows};
+    return oracle_parallel(n_tokens, nthreads, layer_slice, &a);
+}
+
+typedef struct {
+    int64_t H, N;
+    const uint16_t *x;
+    const int64_t *token, *expert;
+    const int8_t *w1;
+    const float *scale1;
+    const int8_t *w2;
+    const float *scale2;
+    int8_t *q1;
+    float *s1, *g;
+    int8_t *q2;
+    float *s2;
+    uint16_t *y;
+} ffn_rows_args;
+
+static void ffn_rows_slice(void *p, int64_t lo, int64_t hi, int *flag)
+{
+    const ffn_rows_args *a = (const ffn_rows_args *)p;
+    const int64_t H = a->H, N = a->N, Nh = N / 2;
+    for (int64_t i = lo; i < hi; ++i) {
+        const int64_t t = a->token[i], e = a->expert[i];
+        *flag |= oracle_ffn_row(H, N, a->x + t * H, a->w1 + e * N * H, a->scale1 + e * N,
+                                a->w2 + e * H * Nh, a->scale2 + e * H,
+                                a->q1 + i * H, a->s1 + i, NULL, a->g + i * Nh,
+                                a->q2 + i * Nh, a->s2 + i, NULL, a->y + i * H);
+    }
+}
+
+/* Every stage of the FFN for n dispatched rows: row i holds token token[i]
+ * of x and runs expert expert[i]'s FFN (oracle_ffn_row).  Outputs per row:
+ * q1 int8 [n, H], s1 [n], g [n, N/2], q2 int8 [n, N/2], s2 [n], y bf16
+ * [n, H].  Rows are split over nthreads threads.  Returns 1 on an int32
+ * overflow in any accumulator. */
+int oracle_ffn_rows_mt(int64_t n, int64_t H, int64_t N, const uint16_t *x,
+                       const int64_t *token, const int64_t *expert,
+                       const int8_t *w1, const float *scale1,
+                       const int8_t *w2, const float *scale2,
+                       int8_t *q1, float *s1, float *g, int8_t *q2, float *s2,
+                       uint16_t *y, int nthreads)
+{
+    ffn_rows_args a = {H, N, x, token, expert, w1, scale1, w2, scale2, q1, s1, g, q2, s2, y};
+    return oracle_parallel(n, nthreads, ffn_rows_slice, &a);
 }

@@ -173,6 +173,32 @@ def test_bf16_narrowing_matches_torch():
     np.testing.assert_array_equal(back, torch.from_numpy(expect.view(np.int16)).view(torch.bfloat16).float().numpy())
 
 
+def test_bf16_narrowing_nan_inputs():
+    """NaN inputs of both signs, quiet and signalling, with small and large
+    payloads.  Against torch's narrowing: a NaN gives a NaN, and only a NaN
+    (a lost NaN branch would round 0x7fffffff up to -0 and a signalling NaN
+    down to infinity).  IEEE 754 (operations on a signalling NaN deliver a
+    quiet NaN): the result's quiet bit is set.  The sign is kept (the
+    oracle's reading; torch returns one canonical NaN)."""
+    words = np.array([0x7FC00000, 0xFFC00000,          # quiet NaN, both signs
+                      0x7F800001, 0xFF800001,          # signalling, lowest payload
+                      0x7FBFFFFF, 0xFFBFFFFF,          # signalling, highest payload
+                      0x7FFFFFFF, 0xFFFFFFFF,          # quiet, all payload bits
+                      0x7FC0FFFF, 0x7F80FFFF,          # payload only below bit 16
+                      0x7F800000, 0xFF800000],         # +-inf: not NaN
+                     np.uint32)
+    v = words.view(np.float32)
+    got = oracle.f32_to_bf16(v)
+    ref = _to_bits(torch.from_numpy(v.copy()).to(torch.bfloat16))
+    got_nan = ((got & 0x7F80) == 0x7F80) & ((got & 0x007F) != 0)
+    ref_nan = ((ref & 0x7F80) == 0x7F80) & ((ref & 0x007F) != 0)
+    np.testing.assert_array_equal(got_nan, ref_nan)
+    assert got_nan[:10].all() and not got_nan[10:].any()
+    assert ((got[:10] & 0x0040) != 0).all()                      # quiet
+    np.testing.assert_array_equal(got[:10] >> 15, (words[:10] >> 31).astype(np.uint16))
+    np.testing.assert_array_equal(got[10:], ref[10:])           # infinities exact
+
+
 def test_silu_against_float64():
     assert oracle.silu(0.0) == 0.0
     for v in np.linspace(-30, 30, 601, dtype=np.float32):
@@ -507,3 +533,48 @@ def test_dispatch_quant_matches_row_quantisation_and_scaling():
         assert s[row] == sc
         # dequantised row within half a step of v
         assert np.all(np.abs(q[row].astype(np.float64) * s[row] - v) <= 0.5 * s[row] * (1 + 1e-6))
+
+
+# ---------------------------------------------------------------- threaded drivers
+
+@pytest.mark.parametrize("threads", [2, 3, 7])
+def test_threaded_gather_and_combine_equal_single_thread(threads):
+    """The threaded drivers cut tokens into slices and call the pinned
+    single-threaded functions; any thread count gives the same bits."""
+    w = wl.custom(P=3, M=37, H=72, E=9, K=3, mask_kind=2, mask_p=0.8, has_shared=True)
+    inp = wl.make_inputs(w, seed=4)
+    r = oracle.route(inp["ids"], w.num_experts, w.num_partitions, inp["mask"])
+    K = w.topk
+    ex1 = oracle.gather(inp["x"], r["route_row"], K, r["R"])
+    exn = oracle.gather(inp["x"], r["route_row"], K, r["R"], threads=threads)
+    np.testing.assert_array_equal(ex1, exn)
+    o1 = oracle.combine(ex1, r["route_row"], inp["probs"], inp["shared"])
+    on = oracle.combine(ex1, r["route_row"], inp["probs"], inp["shared"], threads=threads)
+    np.testing.assert_array_equal(o1, on)
+
+
+def test_threaded_layer_and_ffn_rows_equal_single_thread():
+    w = wl.custom(P=2, M=5, H=64, E=4, K=2, N=256, mask_kind=1, mask_p=0.7, has_shared=True)
+    inp = wl.make_inputs(w, seed=5)
+    W1, S1, W2, S2 = wl.all_expert_weights(w, seed=5)
+    T = w.num_tokens
+    tokens = np.array([7, 0, 3, 9, 4, 1], np.int64)
+    one, ovf1 = oracle.layer_tokens(inp["x"], inp["ids"], inp["probs"], W1, S1, W2, S2, tokens,
+                                    mask=inp["mask"], shared=inp["shared"])
+    many, ovfn = oracle.layer_tokens(inp["x"], inp["ids"], inp["probs"], W1, S1, W2, S2, tokens,
+                                     mask=inp["mask"], shared=inp["shared"], threads=4)
+    np.testing.assert_array_equal(one, many)
+    assert not ovf1 and not ovfn
+    # every (token, expert) pair of the tokens above, one row each
+    rows_t = np.repeat(np.arange(T), w.topk)
+    rows_e = inp["ids"].ravel().astype(np.int64)
+    st = oracle.ffn_rows(inp["x"], rows_t, rows_e, W1, S1, W2, S2, threads=3)
+    assert not st["overflow"]
+    for i in range(rows_t.size):
+        e = rows_e[i]
+        ref = oracle.ffn_row(inp["x"][rows_t[i]], W1[e], S1[e], W2[e], S2[e])
+        np.testing.assert_array_equal(st["q1"][i], ref["q1"])
+        np.testing.assert_array_equal(st["g"][i], ref["g"])
+        np.testing.assert_array_equal(st["q2"][i], ref["q2"])
+        np.testing.assert_array_equal(st["y"][i], ref["y"])
+        assert st["s1"][i] == np.float32(ref["s1"]) and st["s2"][i] == np.float32(ref["s2"])
