@@ -357,19 +357,31 @@ moe_status moe_combine(const moe_shape *shape, const void *expand_x, const int32
 }
 
 // ---------------------------------------------------------------- weights
+// Formats a packed buffer holds, by the shape's ffn_path: fp16 images for the
+// large-tile kernels, biased bytes for the small-batch kernel, both for AUTO
+// (which picks by the row count of each call).  In a buffer holding both, the
+// bytes follow the images.
+static bool packs_f16(int32_t path) { return path != MOE_FFN_PATH_SMALL; }
+static bool packs_i8(int32_t path) {
+    return path == MOE_FFN_PATH_SMALL || path == MOE_FFN_PATH_AUTO;
+}
+
 moe_status moe_packed_weight_bytes(const moe_shape *shape, size_t *w1_bytes, size_t *w2_bytes) {
     MOE_TRY(check_shape(shape, true));
     if (!w1_bytes || !w2_bytes) return MOE_ERR_NULLPTR;
     const moe_shape &s = *shape;
-    *w1_bytes = (size_t)s.num_experts * s.ffn * s.hidden * 3;
-    *w2_bytes = (size_t)s.num_experts * s.hidden * (s.ffn / 2) * 3;
+    const size_t per = (packs_f16(s.ffn_path) ? 2 : 0) + (packs_i8(s.ffn_path) ? 1 : 0);
+    *w1_bytes = (size_t)s.num_experts * s.ffn * s.hidden * per;
+    *w2_bytes = (size_t)s.num_experts * s.hidden * (s.ffn / 2) * per;
     return MOE_OK;
 }
 
-// The int8 part of a packed buffer follows the fp16 images (E*rows*cols*2 bytes,
-// a multiple of 1024 because N % 256 == 0 and H % 16 == 0).
-static const void *packed_i8(const void *packed, int64_t E, int64_t rows, int64_t cols) {
-    return static_cast<const uint8_t *>(packed) + (size_t)E * rows * cols * 2;
+// The biased-byte part of a packed buffer: after the fp16 images (E*rows*cols*2
+// bytes, a multiple of 1024 because N % 256 == 0 and H % 16 == 0) when the
+// buffer holds both formats, else at its start.
+static const void *packed_i8(const void *packed, int32_t path, int64_t E, int64_t rows,
+                             int64_t cols) {
+    return static_cast<const uint8_t *>(packed) + (packs_f16(path) ? (size_t)E * rows * cols * 2 : 0);
 }
 
 static bool use_small_path(int32_t path, int64_t rows, int64_t E) {
@@ -379,11 +391,12 @@ static bool use_small_path(int32_t path, int64_t rows, int64_t E) {
     return rows <= (int64_t)MOE_FFN_SMALL_ROWS_PER_EXPERT * E;
 }
 
-static moe_status run_gemm(bool small, int32_t path, Epi epi, const GemmArgs &g, cudaStream_t stream);
-
+// Large-tile calls: AUTO and LARGE_PAIR take the SM-pair kernel (it falls back
+// to one-SM tiles where no pair cluster fits), LARGE the one-SM kernel.
 static moe_status run_gemm(bool small, int32_t path, Epi epi, const GemmArgs &g, cudaStream_t stream) {
     if (small) return launch_grouped_gemm_small(epi, g, stream);
-    return launch_grouped_gemm(epi, g, stream, path == MOE_FFN_PATH_LARGE_PAIR);
+    return launch_grouped_gemm(epi, g, stream,
+                               path == MOE_FFN_PATH_LARGE_PAIR || path == MOE_FFN_PATH_AUTO);
 }
 
 moe_status moe_pack_weights(const moe_shape *shape, const int8_t *w1, const int8_t *w2,
@@ -395,10 +408,17 @@ moe_status moe_pack_weights(const moe_shape *shape, const int8_t *w1, const int8
         !aligned(w2_packed, kAlign))
         return MOE_ERR_ALIGNMENT;
     const int64_t E = s.num_experts, N = s.ffn, H = s.hidden, Nh = s.ffn / 2;
-    MOE_TRY(launch_pack_w1(w1, w1_packed, E, N, H, stream));
-    MOE_TRY(launch_i8_to_f16(w2, w2_packed, E * H * Nh, stream));
-    MOE_TRY(launch_pack_w1_i8(w1, const_cast<void *>(packed_i8(w1_packed, E, N, H)), E, N, H, stream));
-    MOE_TRY(launch_bias_i8(w2, const_cast<void *>(packed_i8(w2_packed, E, H, Nh)), E * H * Nh, stream));
+    const int32_t path = s.ffn_path;
+    if (packs_f16(path)) {
+        MOE_TRY(launch_pack_w1(w1, w1_packed, E, N, H, stream));
+        MOE_TRY(launch_i8_to_f16(w2, w2_packed, E * H * Nh, stream));
+    }
+    if (packs_i8(path)) {
+        MOE_TRY(launch_pack_w1_i8(w1, const_cast<void *>(packed_i8(w1_packed, path, E, N, H)), E,
+                                  N, H, stream));
+        MOE_TRY(launch_bias_i8(w2, const_cast<void *>(packed_i8(w2_packed, path, E, H, Nh)),
+                               E * H * Nh, stream));
+    }
     return MOE_OK;
 }
 
@@ -413,7 +433,7 @@ static moe_status run_ffn_core(const moe_shape &s, const Layout &L, void *ws,
     GemmArgs g1{};
     g1.a_img = at<void>(ws, L.q1);
     g1.cap_rows = cap;
-    g1.b_img = small ? packed_i8(w1p, s.num_experts, s.ffn, s.hidden) : w1p;
+    g1.b_img = small ? packed_i8(w1p, s.ffn_path, s.num_experts, s.ffn, s.hidden) : w1p;
     g1.E = s.num_experts;
     g1.Nout = s.ffn;
     g1.Kd = s.hidden;
@@ -426,7 +446,7 @@ static moe_status run_ffn_core(const moe_shape &s, const Layout &L, void *ws,
     GemmArgs g2{};
     g2.a_img = at<void>(ws, L.q2);
     g2.cap_rows = cap;
-    g2.b_img = small ? packed_i8(w2p, s.num_experts, s.hidden, Nh) : w2p;
+    g2.b_img = small ? packed_i8(w2p, s.ffn_path, s.num_experts, s.hidden, Nh) : w2p;
     g2.E = s.num_experts;
     g2.Nout = s.hidden;
     g2.Kd = Nh;
@@ -462,9 +482,11 @@ moe_status moe_grouped_ffn(const moe_shape *shape, const void *expand_x,
                            cudaStream_t stream) {
     MOE_TRY(check_shape(shape, true));
     const moe_shape &s = *shape;
-    if (!expand_x || !expert_offsets || !w1_packed || !scale1 || !w2_packed || !scale2 || !y ||
-        !workspace)
+    // with T == 0 the per-row arrays are empty and may be NULL
+    const bool empty = s.num_tokens == 0;
+    if (!expert_offsets || !w1_packed || !scale1 || !w2_packed || !scale2 || !workspace)
         return MOE_ERR_NULLPTR;
+    if (!empty && (!expand_x || !y)) return MOE_ERR_NULLPTR;
     if (!aligned(expand_x, 16) || !aligned(y, 16) || !aligned(scale1, 16) || !aligned(scale2, 16) ||
         !aligned(w1_packed, kAlign) || !aligned(w2_packed, kAlign) || !aligned(workspace, kAlign))
         return MOE_ERR_ALIGNMENT;
@@ -487,9 +509,10 @@ moe_status moe_grouped_ffn_q(const moe_shape *shape, const int8_t *expand_x,
                              size_t workspace_bytes, cudaStream_t stream) {
     MOE_TRY(check_shape(shape, true));
     const moe_shape &s = *shape;
-    if (!expand_x || !dynamic_scales || !expert_offsets || !w1_packed || !scale1 || !w2_packed ||
-        !scale2 || !y || !workspace)
+    const bool empty = s.num_tokens == 0;   // the per-row arrays may then be NULL
+    if (!expert_offsets || !w1_packed || !scale1 || !w2_packed || !scale2 || !workspace)
         return MOE_ERR_NULLPTR;
+    if (!empty && (!expand_x || !dynamic_scales || !y)) return MOE_ERR_NULLPTR;
     if (!aligned(expand_x, 16) || !aligned(y, 16) || !aligned(scale1, 16) || !aligned(scale2, 16) ||
         !aligned(w1_packed, kAlign) || !aligned(w2_packed, kAlign) || !aligned(workspace, kAlign))
         return MOE_ERR_ALIGNMENT;
@@ -521,12 +544,13 @@ moe_status moe_layer(const moe_shape *shape, const void *x, const int32_t *exper
                      size_t workspace_bytes, cudaStream_t stream) {
     MOE_TRY(check_shape(shape, true));
     const moe_shape &s = *shape;
-    if (!x || !expert_ids || !expert_scales || !w1_packed || !scale1 || !w2_packed || !scale2 ||
-        !x_out || !workspace)
-        return MOE_ERR_NULLPTR;
-    if (s.has_shared && !shared_expert_x) return MOE_ERR_NULLPTR;
+    // with T == 0 the per-token and per-route arrays are empty and may be NULL
+    const bool empty = s.num_tokens == 0;
+    if (!w1_packed || !scale1 || !w2_packed || !scale2 || !workspace) return MOE_ERR_NULLPTR;
+    if (!empty && (!x || !expert_ids || !expert_scales || !x_out)) return MOE_ERR_NULLPTR;
+    if (!empty && s.has_shared && !shared_expert_x) return MOE_ERR_NULLPTR;
     if (!s.has_shared && shared_expert_x) return MOE_ERR_PARAM_INVALID;
-    if (s.mask_kind != 0 && !x_active_mask) return MOE_ERR_NULLPTR;
+    if (!empty && s.mask_kind != 0 && !x_active_mask) return MOE_ERR_NULLPTR;
     if (s.mask_kind == 0 && x_active_mask) return MOE_ERR_PARAM_INVALID;
     if (!aligned(x, 16) || !aligned(x_out, 16) || !aligned(scale1, 16) || !aligned(scale2, 16) ||
         (shared_expert_x && !aligned(shared_expert_x, 16)) || !aligned(w1_packed, kAlign) ||

@@ -75,7 +75,7 @@ constexpr size_t P_RING_BYTES = (size_t)P_STAGES * P_STAGE_BYTES;
 constexpr size_t P_SMEM_BYTES = P_RING_BYTES + 1024 + kBarrierBytes +
                                 2 * (kMaxExperts + 1) * sizeof(int32_t);
 static_assert(P_SMEM_BYTES <= 232448, "shared memory budget");
-static_assert((3 * P_STAGES + 5) * 8 + 16 <= (int)kBarrierBytes, "barriers");
+static_assert((2 * P_STAGES + 5) * 8 + 16 <= (int)kBarrierBytes, "barriers");
 
 // Shared-memory descriptor of a K-major tile with BK-element rows: 128-byte
 // rows with the 128-byte swizzle, or 64-byte rows with the 64-byte swizzle
@@ -115,6 +115,8 @@ struct Tile {
     int e, row0, rows, nb;
 };
 
+// m-block-major order: tile = m-block * n_blocks + column block (the fused
+// FFN counts finished tiles per m-block in this order).
 __device__ __forceinline__ Tile decode_tile(int64_t tile, int n_blocks, int E, const int32_t *s_sched,
                                             const int32_t *s_off) {
     Tile t;
@@ -131,6 +133,32 @@ __device__ __forceinline__ Tile decode_tile(int64_t tile, int n_blocks, int E, c
     return t;
 }
 
+// Expert-major, then column-block-major order: expert e owns tiles
+// [blk[e] * n_blocks, blk[e + 1] * n_blocks), where blk[e] counts the row
+// blocks (of `rows_per_block` rows) of the experts before e, and walks every
+// row block of one weight column block before the next column block.  The
+// CTAs in flight then share few weight tiles, each read by all of the
+// expert's row blocks while it is in L2, and the expert's rows stay in L2
+// across its column blocks.  Returns the expert, the block's first row, its
+// row count past row0 (may exceed the block; clipped by the caller) and the
+// column block.
+__device__ __forceinline__ Tile decode_tile_nmajor(int64_t tile, int n_blocks, int E,
+                                                   const int32_t *s_blk, const int32_t *s_off,
+                                                   int rows_per_block) {
+    Tile t;
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {   // last expert whose first tile is <= tile
+        const int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)s_blk[mid] * n_blocks <= tile) lo = mid; else hi = mid - 1;
+    }
+    const int nm = s_blk[lo + 1] - s_blk[lo];   // >= 1: an expert with no rows owns no tile
+    const int64_t local = tile - (int64_t)s_blk[lo] * n_blocks;
+    t.e = lo;
+    t.nb = (int)(local / nm);
+    t.row0 = s_off[lo] + (int)(local % nm) * rows_per_block;
+    t.rows = s_off[lo + 1] - t.row0;
+    return t;
+}
 
 // ---------------------------------------------------------------- epilogues
 // acc[i] is the exact int32 sum for row `row` and tile column hf*128 + i.
@@ -256,7 +284,8 @@ k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
             for (int s = 0; s < STAGES; ++s) issued_phase[s] = -1;
             for (int64_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-                const Tile t = decode_tile(tile, p.n_blocks, p.E, s_sched, s_off);
+                Tile t = decode_tile_nmajor(tile, p.n_blocks, p.E, s_sched, s_off, BM);
+                t.rows = min(t.rows, BM);
                 bool ok = true;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
@@ -319,7 +348,8 @@ k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         int accb = 0;
         uint32_t acc_phase = 0;
         for (int64_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-            const Tile t = decode_tile(tile, p.n_blocks, p.E, s_sched, s_off);
+            Tile t = decode_tile_nmajor(tile, p.n_blocks, p.E, s_sched, s_off, BM);
+            t.rows = min(t.rows, BM);
             int32_t acc[128];
             bool ok = true;
             for (int c = 0; c < num_chunks; ++c) {
@@ -677,20 +707,17 @@ struct PairTile {
     int e, row0, rows, nb;   // row0/rows: this CTA's 128-row half (rows may be <= 0)
 };
 
+// This CTA's half of pair tile `tile` (decode_tile_nmajor's order over
+// 256-row blocks).
 __device__ __forceinline__ PairTile decode_pair_tile(int64_t tile, int n_blocks, int E,
                                                      const int32_t *s_psched, const int32_t *s_off,
                                                      uint32_t rank) {
+    const Tile b = decode_tile_nmajor(tile, n_blocks, E, s_psched, s_off, 2 * BM);
     PairTile t;
-    const int pb = (int)(tile / n_blocks);
-    t.nb = (int)(tile % n_blocks);
-    int lo = 0, hi = E - 1;
-    while (lo < hi) {   // last expert whose first 256-row block is <= pb
-        const int mid = (lo + hi + 1) >> 1;
-        if (s_psched[mid] <= pb) lo = mid; else hi = mid - 1;
-    }
-    t.e = lo;
-    t.row0 = s_off[lo] + (pb - s_psched[lo]) * (2 * BM) + (int)rank * BM;
-    t.rows = min(BM, s_off[lo + 1] - t.row0);
+    t.e = b.e;
+    t.nb = b.nb;
+    t.row0 = b.row0 + (int)rank * BM;
+    t.rows = min(BM, b.rows - (int)rank * BM);
     return t;
 }
 
@@ -699,9 +726,14 @@ __device__ __forceinline__ PairTile decode_pair_tile(int64_t tile, int n_blocks,
 // [128 r, 128 r + 128) of its B; one thread of CTA 0 issues M = 256, N = 256
 // MMAs over both CTAs' halves, and each CTA's TMEM receives its own 128 rows of
 // the accumulator, which its own epilogue warps drain as in k_grouped_gemm.
-//   warp 0      TMA producer (each CTA, its own halves) into a 6-stage ring
-//   warp 1      TMEM (pair allocation); CTA 0: MMA issuer; CTA 1: relays the
-//               landing of its halves to CTA 0's barrier (cluster-scope arrive)
+// Per SM, a k-block moves 32 KB of operands for the same arithmetic that
+// costs the one-SM kernel 48 KB.
+//   warp 0      TMA producer (each CTA, its own halves) into a 6-stage ring.
+//               Both CTAs' loads complete on CTA 0's stage barrier (the
+//               CTA-pair form of the tensor copy), which CTA 0's producer
+//               arms with the bytes of both halves, so one wait covers the
+//               whole stage and no thread relays the peer's landing.
+//   warp 1      TMEM (pair allocation); CTA 0: MMA issuer
 //   warps 2..9  epilogue; their accumulator-free signal goes to CTA 0
 // Commits arrive on both CTAs' barriers (multicast).  Every wait is bounded;
 // both CTAs meet at a cluster barrier before either frees TMEM or exits.
@@ -712,11 +744,10 @@ k_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + P_RING_BYTES);
-    uint64_t *peer_full = full + P_STAGES;
-    uint64_t *empty = peer_full + P_STAGES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + P_RING_BYTES);   // used in CTA 0
+    uint64_t *empty = full + P_STAGES;
     uint64_t *acc_full = empty + P_STAGES;
-    uint64_t *acc_empty = acc_full + 2;
+    uint64_t *acc_empty = acc_full + 2;                                   // used in CTA 0
     uint64_t *drain = acc_empty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -729,9 +760,8 @@ k_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < P_STAGES; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&peer_full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&full[s], 1);        // CTA 0's producer arms it with both halves' bytes
+            mbar_init(&empty[s], 1);       // one commit per stage use
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
@@ -781,11 +811,12 @@ k_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer (both CTAs)
+            const uint32_t full0 = cluster_addr(full, 0);   // CTA 0's full[0]
             int stage = 0;
             uint32_t phase = 0;
-            int issued_phase[P_STAGES];
+            int armed_phase[P_STAGES];
 #pragma unroll
-            for (int s = 0; s < P_STAGES; ++s) issued_phase[s] = -1;
+            for (int s = 0; s < P_STAGES; ++s) armed_phase[s] = -1;
             bool ok = true;
             for (int64_t tile = first; ok && tile < total_tiles; tile += step) {
                 const PairTile t = decode_pair_tile(tile, p.n_blocks, p.E, s_psched, s_off, rank);
@@ -793,34 +824,33 @@ k_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     // freed by CTA 0's commit once the MMAs have read both halves
                     if (!wait_bounded_cluster(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
                     uint8_t *sa = smem + (size_t)stage * P_STAGE_BYTES;
-                    mbar_arrive_expect_tx(&full[stage], P_STAGE_BYTES);
+                    if (leader) {
+                        mbar_arrive_expect_tx(&full[stage], 2 * P_STAGE_BYTES);
+                        armed_phase[stage] = (int)phase;
+                    }
                     // rows past this CTA's half (or past the buffer) only reach
                     // accumulator rows that are never stored
-                    tma_load_2d(sa, &tmA, &full[stage], kb * BK, t.row0);
-                    tma_load_3d(sa + A_BYTES, &tmB, &full[stage], kb * BK,
-                                t.nb * BN + (int)rank * (BN / 2), t.e);
-                    issued_phase[stage] = (int)phase;
+                    const uint32_t fb = full0 + (uint32_t)(stage * sizeof(uint64_t));
+                    tma_load_2d_pair(sa, &tmA, fb, kb * BK, t.row0);
+                    tma_load_3d_pair(sa + A_BYTES, &tmB, fb, kb * BK,
+                                     t.nb * BN + (int)rank * (BN / 2), t.e);
                     if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
                 }
             }
-            for (int s = 0; s < P_STAGES; ++s)
-                if (issued_phase[s] >= 0)
-                    wait_bounded(&full[s], (uint32_t)issued_phase[s], abort_flag, p.status, false);
+            if (leader) {
+                // every armed stage must have landed (both CTAs' halves) before exit
+                for (int s = 0; s < P_STAGES; ++s)
+                    if (armed_phase[s] >= 0)
+                        wait_bounded(&full[s], (uint32_t)armed_phase[s], abort_flag, p.status, false);
+            } else if (!ok) {
+                // the peer's loads complete on CTA 0's barriers; after a give-up,
+                // leave the copies still in flight time to land before exit
+                const uint64_t t0 = globaltimer();
+                while (globaltimer() - t0 < 100000ull) __nanosleep(2000);
+            }
         }
     } else if (warp == 1) {
-        if (lane == 0 && !leader) {
-            // ------------------------------------------------ relay (CTA 1)
-            int stage = 0;
-            uint32_t phase = 0;
-            bool ok = true;
-            for (int64_t tile = first; ok && tile < total_tiles; tile += step) {
-                for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!wait_bounded(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
-                    mbar_arrive_cluster(&peer_full[stage], 0);
-                    if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
-                }
-            }
-        } else if (lane == 0) {
+        if (lane == 0 && leader) {
             // ------------------------------------------------ MMA issuer (CTA 0)
             constexpr uint32_t idesc = idesc_f16(2 * BM, BN);
             int stage = 0;
@@ -835,11 +865,7 @@ k_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const uint32_t d_tmem = tmem_base + (uint32_t)(accb * BN);
                     const int kb1 = min(kb0 + CHUNK_KB, p.num_kb);
                     for (int kb = kb0; kb < kb1; ++kb) {
-                        if (!wait_bounded(&full[stage], phase, abort_flag, p.status) ||
-                            !wait_bounded_cluster(&peer_full[stage], phase, abort_flag, p.status)) {
-                            ok = false;
-                            break;
-                        }
+                        if (!wait_bounded_cluster(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
                         tc_fence_after();
                         const uint32_t a_addr = smem_u32(smem + (size_t)stage * P_STAGE_BYTES);
                         const uint32_t b_addr = a_addr + A_BYTES;
@@ -892,10 +918,7 @@ k_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    if (leader) mbar_arrive(&acc_empty[accb]);
-                    else mbar_arrive_cluster(&acc_empty[accb], 0);
-                }
+                if (lane == 0) mbar_arrive_cluster(&acc_empty[accb], 0);
                 if (++accb == 2) { accb = 0; acc_phase ^= 1u; }
             }
             if (!ok) break;

@@ -27,6 +27,8 @@
  *     call.  moe_read_device_status reads and clears it.
  *   - Every tensor pointer must be 16-byte aligned; workspace and packed
  *     weights must be 1024-byte aligned.
+ *   - With T == 0 the per-token, per-route and per-row arrays are empty and
+ *     may be NULL; the per-expert outputs of a dispatch are still written.
  *   - Results are deterministic: repeated calls give bitwise-identical
  *     outputs ("aclnnMoeDistributeCombineV4", Constraints: Deterministic
  *     Computation).
@@ -95,13 +97,15 @@ typedef struct moe_shape {
     int32_t reserved;        /* must be 0 */
 } moe_shape;
 
-/* Grouped-GEMM kernels of the expert FFN.  Both give bit-identical results.
+/* Grouped-GEMM kernels of the expert FFN.  All give bit-identical results.
  *   LARGE: 128-row x 256-channel tiles on fp16 images of the weights, one
  *          SM each; for many rows per expert, where the tensor cores bound
  *          the time.
- *   LARGE_PAIR: 256-row tiles, each computed by a pair of SMs (a cluster of
- *          two CTAs sharing one 256-row MMA, B split between them).  Same
- *          results; measured slower than LARGE on GB300, kept as an option.
+ *   LARGE_PAIR: 256-row x 256-channel tiles, each computed by a pair of SMs
+ *          (a cluster of two CTAs sharing one 256-row MMA, each holding half
+ *          of the rows and half of the weight channels, so a k-step moves a
+ *          third less data per SM than LARGE).  Falls back to LARGE's kernel
+ *          where no pair cluster fits.
  *   FUSED: LARGE's tiles with GMM1, the second quantisation and GMM2 in one
  *          persistent kernel; GMM2 starts on an m-block as soon as its rows
  *          are quantised ("PTO MegaMoE ...", the quantisation overlapping GMM2).
@@ -112,7 +116,10 @@ typedef struct moe_shape {
  *          (only those present); for few rows per expert, where reading the
  *          weights bounds the time ("PTO MegaMoE ...", Supported Cases: the M
  *          sweep from 16 tokens per rank).
- *   AUTO:  SMALL when T*K <= MOE_FFN_SMALL_ROWS_PER_EXPERT * E, else LARGE. */
+ *   AUTO:  SMALL when T*K <= MOE_FFN_SMALL_ROWS_PER_EXPERT * E, else LARGE_PAIR.
+ * moe_pack_weights writes the weight format(s) of the path in the shape it is
+ * given, and the FFN calls read the format of theirs: pack with the same
+ * ffn_path the FFN runs with (AUTO packs both formats). */
 #define MOE_FFN_PATH_AUTO 0
 #define MOE_FFN_PATH_LARGE 1
 #define MOE_FFN_PATH_SMALL 2
@@ -206,12 +213,14 @@ moe_status moe_combine(const moe_shape *shape, const void *expand_x, const int32
  * packed weights" and fixpipe scales.  The caller's int8 weights are
  *   w1 int8 [E, N, H]   (row n = GMM1 output channel n, H contiguous)
  *   w2 int8 [E, H, N/2] (row c = GMM2 output channel c, N/2 contiguous)
- * Packing, done once per model, writes both kernels' operand formats into
- * each packed buffer: fp16 images of the int8 values (exact) for the LARGE
- * path, followed by byte copies biased by +128 for the SMALL path; W1's rows
- * are reordered in each (differently) so that every GEMM1 tile holds complete
- * SwiGLU pairs.
- * Packed sizes: E*N*H*3 and E*H*(N/2)*3 bytes.  The packed buffers are opaque.
+ * Packing, done once per model, writes the operand format(s) of shape->ffn_path:
+ *   LARGE, LARGE_PAIR, FUSED: fp16 images of the int8 values (exact), 2 bytes
+ *          per weight (E*N*H*2 and E*H*(N/2)*2 bytes);
+ *   SMALL: the values as bytes biased by +128, 1 byte per weight;
+ *   AUTO:  both, the bytes after the images, 3 bytes per weight.
+ * W1's rows are reordered in each format (differently) so that every GEMM1
+ * tile holds complete SwiGLU pairs.  The packed buffers are opaque; an FFN
+ * call must use the ffn_path they were packed with.
  * ------------------------------------------------------------------------ */
 moe_status moe_packed_weight_bytes(const moe_shape *shape, size_t *w1_bytes, size_t *w2_bytes);
 moe_status moe_pack_weights(const moe_shape *shape, const int8_t *w1, const int8_t *w2,
@@ -317,13 +326,19 @@ moe_status moe_grouped_gemm_s32(int64_t rows, int64_t E, int64_t N, int64_t Kd,
  * routing scratch lives in a fixed array in the library's own device memory
  * (moe_dispatch_noalloc_scratch_bytes() bytes, held on every GPU that loads
  * the library until the process exits).  Limit: chunks*E + chunks <= 262144,
- * where chunks = P * ceil(M / 256); larger problems return MOE_ERR_TOO_LARGE
+ * where chunks = P * ceil(M / c) and the routing chunk c depends on T only:
+ * c = 64, doubled while c < 256 and c * 128 < T (so c = 64 for T <= 8192,
+ * 128 for T <= 16384, 256 above).  Larger problems return MOE_ERR_TOO_LARGE
  * before any launch.  The first call on a device looks up the array's device
- * address (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture on the device.  All calls share the array:
- * calls whose kernels overlap on the GPU race.  Invalid ids are treated as
- * inactive, as in moe_dispatch; the status word is kept in the scratch and is
- * not reported.  No cudaMalloc, cudaFree or other allocating call is made.
+ * address (cudaGetSymbolAddress) with that device current and caches it; make
+ * that first call before any stream capture on the device.  The cached
+ * address does not survive a cudaDeviceReset in the calling process.  All
+ * calls share the array: calls whose kernels overlap on the GPU race.  Every
+ * scratch entry a call reads is written earlier in the same call, so nothing
+ * needs clearing between calls.  Invalid ids are treated as inactive, as in
+ * moe_dispatch; the status word is kept in the scratch and is not reported.
+ * Pointer alignment as in moe_dispatch.  No cudaMalloc, cudaFree or other
+ * allocating call is made.
  * ------------------------------------------------------------------------ */
 size_t moe_dispatch_noalloc_scratch_bytes(void);
 moe_status moe_dispatch_noalloc(const moe_shape *shape, const void *x, const int32_t *expert_ids,
@@ -336,6 +351,21 @@ moe_status moe_dispatch_noalloc(const moe_shape *shape, const void *x, const int
  * stores it in *status_host (0 = no device-side error, else MOE_DEV_* bits)
  * and clears it. */
 moe_status moe_read_device_status(void *workspace, cudaStream_t stream, int32_t *status_host);
+
+/* ------------------------------------------------------------------------
+ * Self-test of the bounded waits.  Every in-kernel wait of this library gives
+ * up after a time limit (about 2 s), records MOE_DEV_TIMEOUT in the status
+ * word and lets the kernel finish, so a lost completion surfaces as a status
+ * instead of a hung stream (the pages bound waiting on the host side too:
+ * "aclnnMoeDistributeCombineV4", the A2 sample synchronises its stream with a
+ * 10 000 ms timeout).  This call runs that wait loop on a barrier nothing
+ * arrives on, with no copy or MMA attached, for limit_ns nanoseconds
+ * (0 < limit_ns <= 2e9): the status word of `workspace` must then read
+ * MOE_DEV_TIMEOUT (moe_read_device_status), and the 8 bytes at offset 8 hold
+ * the nanoseconds the wait took.  workspace: >= 16 bytes, 1024-aligned.
+ * ------------------------------------------------------------------------ */
+moe_status moe_wait_selftest(void *workspace, size_t workspace_bytes, uint64_t limit_ns,
+                             cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
  * Instrumentation.

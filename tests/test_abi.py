@@ -46,8 +46,14 @@ def test_workspace_sizes_and_shape_checks(B):
     cap = 16384 * 8
     assert n >= cap * 7168 * 2 * 2 + cap * 2048 * 6      # q1 + y + g + q2
     a, b = B.packed_weight_bytes(s)
-    # fp16 images for the large-tile GEMM + int8 copies for the small-batch GEMM
+    # AUTO: fp16 images for the large-tile GEMMs + biased bytes for the small-batch GEMM
     assert a == 128 * 4096 * 7168 * 3 and b == 128 * 7168 * 2048 * 3
+    for path, per in (("large", 2), ("large_pair", 2), ("fused", 2), ("small", 1)):
+        sp = B.make_shape(16384, 8, 7168, 128, 8, 4096, ffn_path=path)
+        assert B.packed_weight_bytes(sp) == (128 * 4096 * 7168 * per, 128 * 7168 * 2048 * per)
+    # the large prefill workload's weights on the large-tile path: 2 bytes per weight
+    sp = B.make_shape(32768, 8, 7168, 256, 8, 4096, ffn_path="large_pair")
+    assert sum(B.packed_weight_bytes(sp)) == 256 * 4096 * 7168 * 3 // 2 * 2
     for bad in [B.make_shape(10, 3, 128, 8, 2),      # T % P
                 B.make_shape(16, 2, 100, 8, 2),      # H % 8
                 B.make_shape(16, 2, 128, 2000, 2),   # E too large
@@ -139,3 +145,34 @@ def test_layer_argument_checks_before_launch(B):
     assert layer(s, ws_bytes=need - 1) == 561003
     d = B.make_shape(16, 2, 128, 8, 2)                           # N = 0: no FFN to run
     assert layer(d) == 561002
+
+
+ODD4 = ctypes.c_void_p((1 << 20) + 2)   # 2-byte aligned only
+ODD8 = ctypes.c_void_p((1 << 20) + 4)   # 4-byte aligned only
+
+
+@host_only
+def test_noalloc_dispatch_alignment_checks_before_launch(B):
+    """moe_dispatch_noalloc applies moe_dispatch's alignment rules: 16 bytes for
+    x and expand_x, 8 for expert_token_nums, 4 for the index arrays."""
+    L = B.lib()
+    s = B.make_shape(16, 2, 128, 8, 2)
+
+    def call(**bad):
+        a = dict(x=A, ids=A, mask=None, expand_x=A2, assist=A, counts=A, offsets=A, recv=A,
+                 route_row=A)
+        a.update(bad)
+        return L.moe_dispatch_noalloc(ctypes.byref(s), a["x"], a["ids"], a["mask"],
+                                      a["expand_x"], a["assist"], a["counts"], a["offsets"],
+                                      a["recv"], a["route_row"], None)
+
+    assert call(x=MIS) == 561004
+    assert call(expand_x=MIS) == 561004
+    assert call(counts=ODD8) == 561004
+    for name in ("ids", "assist", "offsets", "recv", "route_row"):
+        assert call(**{name: ODD4}) == 561004, name
+    # the 4-byte index arrays accept 4-byte alignment; the 8-byte counts do not
+    big = B.make_shape(65536, 65536, 8, 1024, 1)   # 65536 single-token partitions: too large
+    rc = L.moe_dispatch_noalloc(ctypes.byref(big), A, ODD8, None, A2, ODD8, A, ODD8, ODD8,
+                                ODD8, None)
+    assert rc == 561007
