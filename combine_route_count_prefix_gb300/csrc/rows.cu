@@ -197,8 +197,11 @@ __device__ __forceinline__ uint2 pack_i8x8(const float (&c)[8]) {
     return make_uint2(w[0], w[1]);
 }
 
+// The row stays in registers as its raw 16-byte vectors only: each pass
+// (amax, then codes) unpacks them again, so a CTA needs about 60 registers a
+// thread and eight or more CTAs (tokens) per SM keep their loads in flight.
 template <bool kSmooth>
-__global__ void __launch_bounds__(kRowThreads)
+__global__ void __launch_bounds__(kRowThreads, 8)
 k_dispatch_quant(RouteDev ra, const uint4 *__restrict__ x, const float4 *__restrict__ smooth,
                  int32_t *__restrict__ route_row, int32_t *__restrict__ assist,
                  uint2 *__restrict__ q, float *__restrict__ s_out, int64_t H8) {
@@ -226,6 +229,16 @@ k_dispatch_quant(RouteDev ra, const uint4 *__restrict__ x, const float4 *__restr
             raw[u] = (on && j < H8) ? ld_stream(x + t * H8 + j) : make_uint4(0, 0, 0, 0);
         }
     };
+    // v = float(x) (* smooth[e] for the destination expert, one rounded multiply)
+    auto values = [&](int u, int64_t j, const float4 *sm, float (&v)[8]) {
+        unpack_bf16x8(raw[u], v);
+        if (kSmooth) {
+            const float4 a = __ldg(sm + j * 2), b = __ldg(sm + j * 2 + 1);
+            const float m[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(v[i], m[i]);
+        }
+    };
     load_row(blockIdx.x);
     pdl_wait();
     for (int64_t t = blockIdx.x; t < ra.T; t += gridDim.x) {
@@ -246,51 +259,39 @@ k_dispatch_quant(RouteDev ra, const uint4 *__restrict__ x, const float4 *__restr
         }
         __syncthreads();
         const int n = nrows;
-        float f[kVec][8];
-#pragma unroll
-        for (int u = 0; u < kVec; ++u) unpack_bf16x8(raw[u], f[u]);
         if (n == 0) continue;
+        // without smooth scales every destination gets the token's own codes
         for (int d = 0; d < (kSmooth ? n : 1); ++d) {
-            float v[kVec][8];
+            const float4 *sm = kSmooth ? smooth + (int64_t)experts[d] * H8 * 2 : nullptr;
             float amax = 0.0f;
 #pragma unroll
             for (int u = 0; u < kVec; ++u) {
                 const int64_t j = threadIdx.x + (int64_t)u * kRowThreads;
-                if (kSmooth && j < H8) {
-                    const float4 a = __ldg(smooth + ((int64_t)experts[d] * H8 + j) * 2);
-                    const float4 b = __ldg(smooth + ((int64_t)experts[d] * H8 + j) * 2 + 1);
-                    const float sm[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+                if (j < H8) {
+                    float v[8];
+                    values(u, j, sm, v);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) v[u][i] = __fmul_rn(f[u][i], sm[i]);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) v[u][i] = f[u][i];
+                    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
                 }
-                if (j < H8)
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[u][i]));
             }
             amax = block_max(amax, scratch);
             const float sc = __fdiv_rn(amax, 127.0f);
             const float rs = __frcp_rn(sc);
-            uint2 packed[kVec];
+            const int d0 = kSmooth ? d : 0, d1 = kSmooth ? d + 1 : n;
 #pragma unroll
             for (int u = 0; u < kVec; ++u) {
-                float c[8];
+                const int64_t j = threadIdx.x + (int64_t)u * kRowThreads;
+                if (j < H8) {
+                    float v[8], c[8];
+                    values(u, j, sm, v);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) c[i] = quant_code(v[u][i], sc, rs);
-                packed[u] = pack_i8x8(c);
-            }
-            const int d0 = kSmooth ? d : 0, d1 = kSmooth ? d + 1 : n;
-            for (int dd = d0; dd < d1; ++dd) {
-                const int64_t r = rows[dd];
-#pragma unroll
-                for (int u = 0; u < kVec; ++u) {
-                    const int64_t j = threadIdx.x + (int64_t)u * kRowThreads;
-                    if (j < H8) q[r * H8 + j] = packed[u];
+                    for (int i = 0; i < 8; ++i) c[i] = quant_code(v[i], sc, rs);
+                    const uint2 packed = pack_i8x8(c);
+                    for (int dd = d0; dd < d1; ++dd) q[(int64_t)rows[dd] * H8 + j] = packed;
                 }
-                if (threadIdx.x == 0) s_out[r] = sc;
             }
+            if (threadIdx.x == 0)
+                for (int dd = d0; dd < d1; ++dd) s_out[rows[dd]] = sc;
         }
     }
 }
