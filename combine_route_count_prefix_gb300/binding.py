@@ -35,7 +35,7 @@ EXPORTED = [
     "moe_read_device_status", "moe_launch_count", "moe_profile_enable",
     "moe_profile_report", "moe_status_string",
     "moe_dispatch_noalloc", "moe_dispatch_noalloc_scratch_bytes",
-    "moe_dispatch_quant", "moe_grouped_ffn_q",
+    "moe_dispatch_quant", "moe_grouped_ffn_q", "moe_wait_selftest",
 ]
 
 
@@ -99,6 +99,7 @@ def lib():
         "moe_dispatch_noalloc": [SP, P, P, P, P, P, P, P, P, P, P],
         "moe_dispatch_quant": [SP, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P],
         "moe_grouped_ffn_q": [SP, P, P, P, P, P, P, P, P, P, SZ, P],
+        "moe_wait_selftest": [P, SZ, ctypes.c_uint64, P],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -426,6 +427,17 @@ def grouped_gemm_s32(expert_offsets, A, W, ws=None, C=None, stream=None, path="a
     _call("moe_grouped_gemm_s32", rows, E, N, Kd, _ptr(expert_offsets), _ptr(A), _ptr(W), _ptr(C),
           FFN_PATHS[path], _ptr(ws), ctypes.c_size_t(ws.numel()), _stream(stream))
     return C, ws
+
+
+def wait_selftest(limit_ns, ws=None, stream=None):
+    """moe_wait_selftest: a bounded wait on a barrier nothing arrives on.
+    Returns the workspace (status word at offset 0, the wait's duration in
+    nanoseconds as int64 at offset 8)."""
+    if ws is None:
+        _, ws = _alloc_ws(1024, torch.device("cuda"))
+    _call("moe_wait_selftest", _ptr(ws), ctypes.c_size_t(ws.numel()), ctypes.c_uint64(int(limit_ns)),
+          _stream(stream))
+    return ws
 
 
 def read_device_status(ws, stream=None) -> int:

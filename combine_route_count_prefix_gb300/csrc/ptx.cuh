@@ -104,18 +104,20 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
 }
 
 // Waits for phase `parity` of `bar`.  Gives up when the CTA's abort flag is set
-// or after kTimeoutNs, setting the abort flag and the status bit.  The first
-// test is inline; the bounded loop is a separate function entered only when
-// the phase is not complete yet, so that a wait which succeeds at once costs
-// one instruction and no call (a call spills the caller's live registers).
+// or after limit_ns (kTimeoutNs unless a caller passes a shorter limit),
+// setting the abort flag and the status bit.  The first test is inline; the
+// bounded loop is a separate function entered only when the phase is not
+// complete yet, so that a wait which succeeds at once costs one instruction
+// and no call (a call spills the caller's live registers).
 static __device__ __noinline__ bool wait_bounded_loop(uint64_t *bar, uint32_t parity,
                                                       volatile int *abort_flag, int32_t *status,
-                                                      bool honour_abort) {
+                                                      bool honour_abort,
+                                                      unsigned long long limit_ns = kTimeoutNs) {
     const uint64_t t0 = globaltimer();
     for (;;) {
         if (mbar_try_wait_sleep(bar, parity, kWaitSliceNs)) return true;
         if (honour_abort && *abort_flag) return false;
-        if (globaltimer() - t0 > kTimeoutNs) {
+        if (globaltimer() - t0 > limit_ns) {
             *abort_flag = 1;
             if (status) atomicOr(status, MOE_DEV_TIMEOUT);
             return false;
