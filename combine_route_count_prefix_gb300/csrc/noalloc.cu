@@ -81,7 +81,12 @@ moe_status moe_dispatch_noalloc(const moe_shape *shape, const void *x, const int
     if (!empty && expand_x && !x) return MOE_ERR_NULLPTR;
     if (!empty && s.mask_kind != 0 && !x_active_mask) return MOE_ERR_NULLPTR;
     if (s.mask_kind == 0 && x_active_mask) return MOE_ERR_PARAM_INVALID;
-    if (expand_x && (((uintptr_t)x % 16) != 0 || ((uintptr_t)expand_x % 16) != 0))
+    // the same alignment rules as moe_dispatch: 16-byte row vectors, 8-byte
+    // counts, 4-byte indices
+    auto misaligned = [](const void *ptr, uintptr_t a) { return ((uintptr_t)ptr % a) != 0; };
+    if (expand_x && (misaligned(x, 16) || misaligned(expand_x, 16))) return MOE_ERR_ALIGNMENT;
+    if (misaligned(expert_ids, 4) || misaligned(assist, 4) || misaligned(expert_token_nums, 8) ||
+        misaligned(expert_offsets, 4) || misaligned(ep_recv_counts, 4) || misaligned(route_row, 4))
         return MOE_ERR_ALIGNMENT;
     const int64_t chunks = route_chunks(s);
     const size_t entries = (size_t)(chunks * s.num_experts + chunks);

@@ -6,12 +6,16 @@ of a caller workspace, and must give exactly what moe_dispatch gives.
 
 Checked through the C ABI on two calls in a row with different inputs, so
 that anything left over in the shared array from the first call would show in
-the second.  Collected last so that a stop at the first failure has run every
-other test already."""
+the second: against moe_dispatch, and against the CPU oracle's routing and row
+gather.  Above 65536 routes the routing runs as one CTA per chunk, whose
+per-chunk histograms and flags live in the shared array, so that size is
+covered too.  Collected last so that a stop at the first failure has run
+every other test already."""
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from combine_route_count_prefix_gb300 import workloads as wl
 from gpu_util import dev, dev_bf16, load_binding
 
@@ -37,6 +41,17 @@ def _compare(B, w, seed):
     R = int(ref["expert_offsets"][-1].item())
     assert torch.equal(got["assist"][:R], ref["assist"][:R])
     assert torch.equal(got["expand_x"][:R].view(torch.int16), ref["expand_x"][:R].view(torch.int16))
+    # and against the oracle directly
+    o = oracle.route(inp["ids"], w.num_experts, w.num_partitions, inp["mask"])
+    assert o["R"] == R
+    np.testing.assert_array_equal(got["route_row"].cpu().numpy(), o["route_row"])
+    np.testing.assert_array_equal(got["expert_token_nums"].cpu().numpy(), o["counts"])
+    np.testing.assert_array_equal(got["expert_offsets"].cpu().numpy(), o["offsets"])
+    np.testing.assert_array_equal(got["ep_recv_counts"].cpu().numpy(), o["recv_cum"])
+    np.testing.assert_array_equal(got["assist"][:R].cpu().numpy(), o["assist"])
+    rows = oracle.gather(inp["x"], o["route_row"], w.topk, R, threads=0)
+    np.testing.assert_array_equal(
+        got["expand_x"][:R].view(torch.int16).cpu().numpy().view(np.uint16), rows)
     return R
 
 
@@ -46,6 +61,18 @@ def test_noalloc_dispatch_matches_dispatch_twice(B):
     r1 = _compare(B, a, seed=1)
     r2 = _compare(B, b, seed=2)
     assert r1 > 0 and r2 > 0
+
+
+def test_noalloc_dispatch_per_chunk_routing_twice(B):
+    """8 x 2048 tokens, top-8, 128 experts: 131072 routes, routed one CTA per
+    chunk (128 chunks x 128 experts + 128 flags = 16512 scratch entries).
+    Two calls with different ids and masks."""
+    a = wl.custom(P=8, M=2048, H=64, E=128, K=8, mask_kind=2, mask_p=0.9)
+    b = wl.custom(P=8, M=2048, H=64, E=128, K=8, mask_kind=1, mask_p=0.5)
+    assert a.num_tokens * a.topk > 65536
+    r1 = _compare(B, a, seed=3)
+    r2 = _compare(B, b, seed=4)
+    assert r1 != r2
 
 
 def test_noalloc_dispatch_full_decode_workload(B):
