@@ -170,15 +170,28 @@ def expert_weights(w: Workload, e: int, seed: int = 0):
     return w1, s1, w2, s2
 
 
-def all_expert_weights(w: Workload, seed: int = 0):
-    """Stacked weights of every expert: W1 [E, N, H], scale1 [E, N], W2 [E, H, N/2], scale2 [E, H]."""
+def all_expert_weights(w: Workload, seed: int = 0, threads: int = 1):
+    """Stacked weights of every expert: W1 [E, N, H], scale1 [E, N], W2 [E, H, N/2], scale2 [E, H].
+    Experts are drawn from their own streams, so ``threads`` > 1 (0 = every
+    host core) draws them in parallel with the same result."""
+    import concurrent.futures as cf
+    import os
     E, N, H = w.num_experts, w.ffn, w.hidden
     w1 = np.empty((E, N, H), np.int8)
     s1 = np.empty((E, N), np.float32)
     w2 = np.empty((E, H, N // 2), np.int8)
     s2 = np.empty((E, H), np.float32)
-    for e in range(E):
+
+    def one(e):
         w1[e], s1[e], w2[e], s2[e] = expert_weights(w, e, seed)
+
+    n = threads or os.cpu_count() or 1
+    if n <= 1:
+        for e in range(E):
+            one(e)
+    else:
+        with cf.ThreadPoolExecutor(n) as ex:
+            list(ex.map(one, range(E)))
     return w1, s1, w2, s2
 
 

@@ -64,28 +64,35 @@ def _stage_check(B, w, seed, path="auto"):
     s2 = v["s2"][:R].cpu().numpy()
     y = host_bits(v["y"][:R])
     e_of_row = np.searchsorted(r["offsets"], np.arange(R), side="right") - 1
-    q2_flips = 0
-    y_rows_exact = 0
-    for i in range(R):
-        e, t = e_of_row[i], r["row_token"][i]
-        st = oracle.ffn_row(inp["x"][t], W1[e], S1[e], W2[e], S2[e])
-        np.testing.assert_array_equal(q1[i], st["q1"])
-        assert s1[i] == np.float32(st["s1"])
-        assert f32_ulps(g[i], st["g"]).max() <= 8, (i, f32_ulps(g[i], st["g"]).max())
-        d = np.abs(q2[i].astype(np.int32) - st["q2"].astype(np.int32))
-        assert d.max() <= 1
-        q2_flips += int((d > 0).sum())
-        if (d == 0).all() and s2[i] == np.float32(st["s2"]):
-            np.testing.assert_array_equal(y[i], st["y"])
-            y_rows_exact += 1
-    assert q2_flips <= 0.001 * R * (N // 2), q2_flips
-    assert y_rows_exact >= 0.9 * R
+    st = oracle.ffn_rows(inp["x"], r["row_token"], e_of_row, W1, S1, W2, S2)
+    q2_flips, y_rows_exact = _compare_rows(dict(q1=q1, s1=s1, g=g, q2=q2, s2=s2, y=y), st)
     ref, ovf = oracle.layer_tokens(inp["x"], inp["ids"], inp["probs"], W1, S1, W2, S2,
                                    np.arange(T), mask=inp["mask"], shared=inp["shared"])
     assert not ovf
     ulp, rel = output_errors(host_bits(out), ref)
     assert ulp <= 2.0 and rel <= 1e-3, (ulp, rel)
     return dict(q2_flips=q2_flips, R=R, ulp=ulp, rel=rel)
+
+
+def _compare_rows(got, st):
+    """Row by row against the oracle's stages (same row order): q1/s1
+    bit-exact, g within 8 fp32 ulp, q2 within 1 LSB on at most 0.1 % of its
+    elements, y bit-exact on every row whose q2 and s2 equal the oracle's and
+    at least 90 % of rows exact.  Returns (q2 flips, rows with y exact)."""
+    n, Nh = got["q2"].shape
+    assert not st["overflow"]
+    np.testing.assert_array_equal(got["q1"], st["q1"])
+    np.testing.assert_array_equal(got["s1"], st["s1"])
+    gu = f32_ulps(got["g"], st["g"])
+    assert gu.max(initial=0) <= 8, (gu.max(), np.unravel_index(gu.argmax(), gu.shape))
+    d = np.abs(got["q2"].astype(np.int32) - st["q2"].astype(np.int32))
+    assert d.max(initial=0) <= 1
+    flips = int((d > 0).sum())
+    assert flips <= 0.001 * n * Nh, flips
+    same = (d == 0).all(axis=1) & (got["s2"] == st["s2"])
+    np.testing.assert_array_equal(got["y"][same], st["y"][same])
+    assert same.sum() >= 0.9 * n, (int(same.sum()), n)
+    return flips, int(same.sum())
 
 
 @pytest.mark.parametrize("path", PATHS)
@@ -179,68 +186,95 @@ def test_layer_deterministic(B):
         np.testing.assert_array_equal(outs[0], o)
 
 
-def _sampled_full_size(B, name, n_tokens, seed=0, path="auto"):
-    """Full-size layer in the benchmark's launch configuration; the oracle
-    computes a sample of tokens one by one."""
+def _sample_rows(offsets, rng, block=128):
+    """Per expert: its first and last row and one random row of every
+    `block`-row block (each m-block of the one-SM tiles, each half of a pair
+    tile)."""
+    rows = []
+    for e in range(offsets.size - 1):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if a == b:
+            continue
+        pick = {a, b - 1}
+        for s0 in range(a, b, block):
+            pick.add(int(rng.integers(s0, min(s0 + block, b))))
+        rows.extend(sorted(pick))
+    return np.array(rows, np.int64)
+
+
+def _full_size_check(B, name, tokens_per_partition_out, seed=0, path="auto"):
+    """A full-size layer workload in the benchmark's launch configuration.
+    Routing, counts, offsets and triplets: every entry, bit-exact.  FFN
+    stages (q1, s1, g, q2, s2, y): sampled rows of every expert (first, last,
+    one per 128-row block), computed by the oracle from the same inputs.
+    Output: tokens spread over every partition, computed by the oracle token
+    by token through the whole layer."""
     w = wl.WORKLOADS[name]
     T, P, H, E, K, N = (w.num_tokens, w.num_partitions, w.hidden, w.num_experts, w.topk, w.ffn)
+    M = w.tokens_per_partition
     inp = wl.make_inputs(w, seed=seed)
-    shape = B.make_shape(T, P, H, E, K, N, 0, inp["shared"] is not None, ffn_path=path)
-    w1 = torch.empty((E, N, H), dtype=torch.int8, device="cuda")
-    w2 = torch.empty((E, H, N // 2), dtype=torch.int8, device="cuda")
-    s1 = torch.empty((E, N), dtype=torch.float32, device="cuda")
-    s2 = torch.empty((E, H), dtype=torch.float32, device="cuda")
-    g = np.random.default_rng(seed + 100)
-    sample = np.sort(g.choice(T, n_tokens, replace=False))
-    need = set(inp["ids"][sample].ravel().tolist())
-    host = {}
-    for e in range(E):
-        a, b, c, d = wl.expert_weights(w, e, seed)
-        w1[e].copy_(torch.from_numpy(a))
-        s1[e].copy_(torch.from_numpy(b))
-        w2[e].copy_(torch.from_numpy(c))
-        s2[e].copy_(torch.from_numpy(d))
-        if e in need:
-            host[e] = (a, b, c, d)
-    (o1, w1p), (o2, w2p) = B.pack_weights(shape, w1, w2)
-    del w1, w2
-    out, ws = B.layer(shape, dev_bf16(inp["x"]), dev(inp["ids"]), dev(inp["probs"]), w1p, s1, w2p,
-                      s2, shared=dev_bf16(inp["shared"]))
+    W1, S1, W2, S2 = wl.all_expert_weights(w, seed=seed, threads=0)
+    shape = B.make_shape(T, P, H, E, K, N, w.mask_kind, w.has_shared, ffn_path=path)
+    w1d, w2d = dev(W1), dev(W2)
+    (o1, w1p), (o2, w2p) = B.pack_weights(shape, w1d, w2d)
+    torch.cuda.synchronize()
+    del w1d, w2d
+    out, ws = B.layer(shape, dev_bf16(inp["x"]), dev(inp["ids"]), dev(inp["probs"]), w1p, dev(S1),
+                      w2p, dev(S2), mask=dev(inp["mask"]), shared=dev_bf16(inp["shared"]))
     torch.cuda.synchronize()
     assert B.read_device_status(ws) == 0
-    got = host_bits(out)[sample]
-    # oracle on the sampled tokens: per-token computation with only the experts they use
-    W1 = np.zeros((E, 1, 1), np.int8)
-    ref = np.zeros((n_tokens, H), np.uint16)
-    for i, t in enumerate(sample):
-        ids_t = inp["ids"][t: t + 1]
-        experts = sorted(set(ids_t.ravel().tolist()))
-        remap = {e: j for j, e in enumerate(experts)}
-        W1 = np.stack([host[e][0] for e in experts])
-        S1 = np.stack([host[e][1] for e in experts])
-        W2 = np.stack([host[e][2] for e in experts])
-        S2 = np.stack([host[e][3] for e in experts])
-        ids_local = np.vectorize(remap.get)(ids_t).astype(np.int32)
-        sh = None if inp["shared"] is None else inp["shared"][t: t + 1]
-        ref[i], _ = oracle.layer_tokens(inp["x"][t: t + 1], ids_local, inp["probs"][t: t + 1],
-                                        W1, S1, W2, S2, np.array([0]), shared=sh)
-    ulp, rel = output_errors(got, ref)
+    v = B.stage_views(shape, ws, for_layer=True)
+    r = oracle.route(inp["ids"], E, P, inp["mask"])
+    R = r["R"]
+    np.testing.assert_array_equal(v["route_row"].cpu().numpy(), r["route_row"])
+    np.testing.assert_array_equal(v["expert_offsets"].cpu().numpy(), r["offsets"])
+    np.testing.assert_array_equal(v["expert_token_nums"].cpu().numpy(), r["counts"])
+    np.testing.assert_array_equal(v["ep_recv_counts"].cpu().numpy(), r["recv_cum"])
+    np.testing.assert_array_equal(v["assist"][:R].cpu().numpy(), r["assist"])
+
+    rng = np.random.default_rng(seed + 1000)
+    rows = _sample_rows(r["offsets"], rng)
+    e_of = np.searchsorted(r["offsets"], rows, side="right") - 1
+    assert np.unique(e_of).size == int((r["counts"] > 0).sum())   # every expert with rows
+    st = oracle.ffn_rows(inp["x"], r["row_token"][rows], e_of, W1, S1, W2, S2)
+    idx = torch.from_numpy(rows).cuda()
+    got = dict(q1=host_f16_as_i8(v["q1"][idx]), s1=v["s1"][idx].cpu().numpy(),
+               g=v["g"][idx].cpu().numpy(), q2=host_f16_as_i8(v["q2"][idx]),
+               s2=v["s2"][idx].cpu().numpy(), y=host_bits(v["y"][idx]))
+    _compare_rows(got, st)
+
+    tokens = np.concatenate([p * M + np.sort(rng.choice(M, tokens_per_partition_out, replace=False))
+                             for p in range(P)]).astype(np.int64)
+    ref, ovf = oracle.layer_tokens(inp["x"], inp["ids"], inp["probs"], W1, S1, W2, S2, tokens,
+                                   mask=inp["mask"], shared=inp["shared"], threads=0)
+    assert not ovf
+    ulp, rel = output_errors(host_bits(out)[tokens], ref)
     assert ulp <= 2.0 and rel <= 1e-3, (ulp, rel)
+    return rows.size, tokens.size
 
 
-def test_full_layer_sampled(B):
-    _sampled_full_size(B, "full_layer", n_tokens=6)
+def test_full_layer_full_size(B):
+    """16384 tokens, 128 experts, FFN 4096: ~1300 sampled rows covering every
+    expert's 128-row blocks, and 512 output tokens (64 per partition)."""
+    nrows, ntok = _full_size_check(B, "full_layer", tokens_per_partition_out=64)
+    assert ntok == 512 and nrows > 128 * 8
 
 
-def test_large_prefill_sampled(B):
-    _sampled_full_size(B, "large_prefill", n_tokens=4)
+def test_large_prefill_full_size(B):
+    """32768 tokens, 256 experts, FFN 4096, shared expert: sampled rows of
+    every expert and 256 output tokens (32 per partition)."""
+    nrows, ntok = _full_size_check(B, "large_prefill", tokens_per_partition_out=32)
+    assert ntok == 256 and nrows > 256 * 8
 
 
 @pytest.mark.parametrize("path", ["auto", "large"])
-def test_small_batch_layer_sampled(B, path):
+def test_small_batch_layer_every_token(B, path):
     """The smallest point of the tokens-per-rank sweep (8 x 16 tokens, 128
-    experts): "auto" takes the small-batch kernels here."""
-    _sampled_full_size(B, "small_batch_layer", n_tokens=8, path=path)
+    experts): "auto" takes the small-batch kernels here.  Every output token
+    and every routed row's stages against the oracle."""
+    w = wl.WORKLOADS["small_batch_layer"]
+    nrows, ntok = _full_size_check(B, "small_batch_layer", tokens_per_partition_out=16, path=path)
+    assert ntok == w.num_tokens
 
 
 def test_quantisation_codes_exact_on_ties_and_many_scales(B):
