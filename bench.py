@@ -1,7 +1,7 @@
 """Benchmark of the single-GPU MoE dispatch / grouped FFN / combine path.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--layer]
+                    [--workload NAME] [--no-layer]
 
 One step is one pass of the hot path over one batch: for the identity-expert
 workloads (decode_dispatch_combine, skewed_dispatch_combine) that is
@@ -26,8 +26,15 @@ device->host copy of the output are inside the timed region.
 Under torchrun (N > 1) every rank runs the same workload on its own GPU with
 its own seed and no collective on the data path (weak scaling, replicas).
 
---impl reference times the CPU oracle (single-threaded C, as it stands) on a
-bounded sample of the same workload; under torchrun only rank 0 runs it.
+The identity-expert workloads also report the full layer workload (8 x 2048
+tokens, 128 experts, FFN 4096) as a secondary item, `full_layer`: tokens/s,
+the grouped GEMMs against the measured bf16 peaks (burst and sustained), its
+own clock samples and oracle baseline (--no-layer skips it).
+
+cpu_baseline and --impl reference time the CPU oracle as it stands on every
+host core (its threaded drivers only split tokens over threads): the whole
+identity-expert workload per step, or a few tokens per thread through the
+whole layer; under torchrun only rank 0 runs the reference arm.
 """
 from __future__ import annotations
 
@@ -61,8 +68,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode_dispatch_combine", choices=list(wl.WORKLOADS))
-    ap.add_argument("--layer", action="store_true",
-                    help="also time the full layer workload (full_layer) as a secondary line item")
+    ap.add_argument("--no-layer", action="store_true",
+                    help="skip the full layer workload (full_layer) that the identity-expert "
+                         "workloads report as a secondary line item")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--tokens-per-partition", type=int, default=0,
                     help="override M (tokens per partition) of the workload")
@@ -212,42 +220,48 @@ def whole_job_tokens_per_s(tokens_per_rank, world, ms_per_step):
 
 
 # ------------------------------------------------------------------ reference arm (CPU oracle)
-def oracle_sample(w, inp, seed):
-    """A bounded sample of the workload for the CPU oracle: returns
-    (step callable returning tokens processed, description)."""
+def host_cores():
+    """Cores this process may run on (what `nproc` reports)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(w, inp, seed, threads):
+    """A bounded sample of the workload for the CPU oracle on `threads`
+    threads: returns (step callable returning tokens processed, description).
+    Identity-expert workloads run whole (routing in one sequential pass, the
+    row gather and the combine split by tokens over the threads); the layer
+    workloads run a few tokens per thread through the whole layer."""
     import oracle
     oracle.build()
-    M = w.tokens_per_partition
     if w.identity:
-        parts = min(2, w.num_partitions)
-        S = parts * M
-        samp = {k: (None if v is None else v[:S]) for k, v in inp.items()}
+        T = w.num_tokens
 
         def step():
-            oracle.dispatch_combine_identity(samp["x"], samp["ids"], samp["probs"], w.num_experts,
-                                             parts, mask=samp["mask"], shared=samp["shared"])
-            return S
-        return step, (f"dispatch+combine of {parts} of {w.num_partitions} partitions "
-                      f"({S} tokens) per step")
-    n_tok = 1
-    need = sorted(set(inp["ids"][:n_tok].ravel().tolist()))
-    weights = {e: wl.expert_weights(w, e, seed) for e in need}
+            oracle.dispatch_combine_identity(inp["x"], inp["ids"], inp["probs"], w.num_experts,
+                                             w.num_partitions, mask=inp["mask"],
+                                             shared=inp["shared"], threads=threads)
+            return T
+        return step, (f"the whole workload per step ({T} tokens, all {w.num_partitions} "
+                      f"partitions): routing, row gather and combine, {threads} threads")
+    W1, S1, W2, S2 = wl.all_expert_weights(w, seed=seed, threads=threads)
+    n_tok = 2 * threads
+    g = np.random.default_rng(seed + 7)
+    state = {"i": 0}
+    order = g.permutation(w.num_tokens).astype(np.int64)
 
     def step():
-        for t in range(n_tok):
-            experts = sorted(set(inp["ids"][t].tolist()))
-            remap = {e: j for j, e in enumerate(experts)}
-            W1 = np.stack([weights[e][0] for e in experts])
-            S1 = np.stack([weights[e][1] for e in experts])
-            W2 = np.stack([weights[e][2] for e in experts])
-            S2 = np.stack([weights[e][3] for e in experts])
-            ids_l = np.array([[remap[e] for e in inp["ids"][t]]], np.int32)
-            mask = None if inp["mask"] is None else inp["mask"][t: t + 1]
-            shared = None if inp["shared"] is None else inp["shared"][t: t + 1]
-            oracle.layer_tokens(inp["x"][t: t + 1], ids_l, inp["probs"][t: t + 1], W1, S1, W2, S2,
-                                np.array([0]), mask=mask, shared=shared)
+        i = state["i"]
+        tok = np.sort(order[i: i + n_tok])
+        state["i"] = (i + n_tok) % max(1, w.num_tokens - n_tok)
+        oracle.layer_tokens(inp["x"], inp["ids"], inp["probs"], W1, S1, W2, S2, tok,
+                            mask=inp["mask"], shared=inp["shared"], threads=threads)
         return n_tok
-    return step, f"{n_tok} token per step through the whole layer (its {w.topk} experts' FFNs)"
+    return step, (f"{n_tok} tokens per step through the whole layer (each token's "
+                  f"{w.topk} expert FFNs and combine; weights drawn by the input recipe), "
+                  f"{threads} threads")
 
 
 def run_reference(args, rank, world):
@@ -255,7 +269,8 @@ def run_reference(args, rank, world):
         return
     w = select_workload(args)
     inp = wl.make_inputs(w, seed=args.seed)
-    step, sample = oracle_sample(w, inp, args.seed)
+    threads = host_cores()
+    step, sample = oracle_sample(w, inp, args.seed, threads)
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
@@ -270,8 +285,8 @@ def run_reference(args, rank, world):
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": workload_config(w),
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
+                         "nproc": host_cores(), "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -288,19 +303,21 @@ def workload_config(w):
 
 # ------------------------------------------------------------------ our arm
 def cpu_baseline_sample(w, inp, seed, budget_s=10.0):
-    """The oracle as it stands, single-threaded, on a bounded sample of the
+    """The oracle as it stands, on every host core, on a bounded sample of the
     same workload, repeated for about budget_s seconds."""
-    step, sample = oracle_sample(w, inp, seed)
+    threads = host_cores()
+    step, sample = oracle_sample(w, inp, seed, threads)
+    step()                                      # first call: library load, page-in
     t0 = time.perf_counter()
     units = reps = 0
     while True:
         units += step()
         reps += 1
         dt = time.perf_counter() - t0
-        if dt > budget_s or reps >= 500:
+        if dt > budget_s or reps >= 2000:
             break
-    return {"value": units / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{sample}, repeated {reps}x over {dt:.1f} s"}
+    return {"value": units / dt, "unit": "tokens/s", "cores": threads, "nproc": host_cores(),
+            "kind": "oracle", "sample": f"{sample}, repeated {reps}x over {dt:.1f} s"}
 
 
 def select_workload(args):
@@ -317,17 +334,12 @@ def select_workload(args):
 
 
 def device_weights(w, dev, seed):
-    """Seeded synthetic expert weights drawn on the device (same distributions as
-    the recipe; a torch generator, so that the large workloads start quickly)."""
+    """Expert weights of the input recipe (the same values the tests use),
+    drawn on the host cores in parallel and copied to the device."""
     import torch
-    E, N, H = w.num_experts, w.ffn, w.hidden
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(seed)
-    w1 = torch.randint(-127, 128, (E, N, H), dtype=torch.int8, device=dev, generator=gen)
-    w2 = torch.randint(-127, 128, (E, H, N // 2), dtype=torch.int8, device=dev, generator=gen)
-    s1 = torch.empty((E, N), device=dev).uniform_(1e-3, 1e-2, generator=gen)
-    s2 = torch.empty((E, H), device=dev).uniform_(1e-3, 1e-2, generator=gen)
-    return w1, s1, w2, s2
+    W1, S1, W2, S2 = wl.all_expert_weights(w, seed=seed, threads=0)
+    return (torch.from_numpy(W1).to(dev), torch.from_numpy(S1).to(dev),
+            torch.from_numpy(W2).to(dev), torch.from_numpy(S2).to(dev))
 
 
 class IdentityPath:
@@ -442,9 +454,15 @@ class LayerPath:
                         "stage output (g fp32 / y bf16) bytes per launch",
                         peak_source=pk["source"] + " hbm_gbs"), step_bytes, extra
         achieved = fl[dom] / (us * 1e-6) / 1e12
+        extra["gemm_frac"] = {k: {"of_sustained": v / pk["bf16_tflops_sustained"],
+                                  "of_burst": v / pk["bf16_tflops"]}
+                              for k, v in extra["gemm_tflops"].items()}
         return dict(bound="tensor", kernel=dom, achieved=achieved,
                     peak=pk["bf16_tflops_sustained"], unit="TFLOP/s",
                     frac=achieved / pk["bf16_tflops_sustained"],
+                    frac_of_burst=achieved / pk["bf16_tflops"], peak_burst=pk["bf16_tflops"],
+                    peak_choice="sustained: the GEMMs run back to back inside a multi-ms "
+                                "layer step after a soak, under the power cap",
                     traffic=recorded_traffic(dom, w.name), algorithmic_flops=fl[dom],
                     algorithmic_unit="2*R*H*N (GEMM1) or 2*R*(N/2)*H (GEMM2) flops per launch",
                     peak_source=pk["source"] + " bf16_tflops_sustained (cuBLAS bf16; the int8 "
@@ -471,15 +489,25 @@ class LayerPath:
         return "int8 GEMMs (exact, on fp16 images), fp32 epilogues, bf16 rows"
 
 
-def run_layer_secondary(args, B, dev, stream, flush, pk):
+def run_layer_secondary(args, B, dev, stream, flush, pk, want_cpu):
     """The full layer workload (16384 tokens, 128 experts, FFN 4096) as a
-    secondary line item: tokens/s and the grouped GEMMs' roofline."""
+    secondary line item: tokens/s, the grouped GEMMs' roofline against the
+    burst and the sustained bf16 peaks, the clocks of its own timed region and
+    its own oracle baseline."""
     import torch
     w = wl.WORKLOADS["full_layer"]
     inp = wl.make_inputs(w, seed=args.seed)
     path = LayerPath(B, w, inp, dev, args.seed, args.ffn_path)
     for _ in range(3):
         path.step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    t_end = time.time() + max(args.soak, 1.0)          # untimed soak for the clock samples
+    while time.time() < t_end:
+        flush.fill_(1)
+        path.step()
+        torch.cuda.synchronize()
     steps = max(3, min(args.steps, 10))
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
@@ -490,6 +518,7 @@ def run_layer_secondary(args, B, dev, stream, flush, pk):
         path.step()
         ev[i][1].record(stream)
     torch.cuda.synchronize()
+    clk = clocks.stop()
     ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
     B.profile_enable(True)
     for i in range(steps):
@@ -497,9 +526,17 @@ def run_layer_secondary(args, B, dev, stream, flush, pk):
         path.step()
     torch.cuda.synchronize()
     B.profile_enable(False)
-    roofline, _, extra = path.roofline(B.profile_report(), pk)
-    return {"workload": w.name, "value": whole_job_tokens_per_s(w.num_tokens, 1, ms),
-            "unit": "tokens/s", "ms_per_step": ms, "steps": steps, "roofline": roofline, **extra}
+    prof = B.profile_report()
+    roofline, _, extra = path.roofline(prof, pk)
+    roofline["per_kernel_us"] = {k: round(ms_ / n * 1e3, 3) for k, (n, ms_) in prof.items()}
+    item = {"workload": w.name, "config": workload_config(w),
+            "value": whole_job_tokens_per_s(w.num_tokens, 1, ms), "unit": "tokens/s",
+            "ms_per_step": ms, "steps": steps, "roofline": roofline, "clocks": clk, **extra}
+    del path
+    torch.cuda.empty_cache()
+    if want_cpu:
+        item["cpu_baseline"] = cpu_baseline_sample(w, inp, args.seed, budget_s=8.0)
+    return item
 
 
 def quant_dispatch_item(B, path, w, inp, flush, stream, steps, pk):
@@ -702,8 +739,9 @@ def run_ours(args, rank, world, dist):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, dev)
 
     secondary = None
-    if args.layer and w.identity:
-        secondary = run_layer_secondary(args, B, dev, stream, flush, pk)
+    if not args.no_layer and w.identity:
+        secondary = run_layer_secondary(args, B, dev, stream, flush, pk,
+                                        want_cpu=(world == 1 and not args.no_cpu_baseline))
 
     if rank != 0:
         return

@@ -41,19 +41,23 @@ def test_whole_job_rate_is_weak_scaling():
 
 
 def test_recorded_traffic_follows_the_source_hash(monkeypatch):
-    # every row of the table resolves while its source is unchanged ...
+    # a row resolves exactly while its kernel's source file still has the
+    # recorded hash (a row captured before a kernel change reads as null) ...
     rows = []
     for line in open(os.path.join(ROOT, "profiles", "traffic.md")):
         parts = [p.strip() for p in line.strip().strip("|").split("|")]
         if len(parts) >= 5 and parts[2].endswith(".cu"):
-            rows.append((parts[0], parts[1]))
+            rows.append((parts[0], parts[1], parts[2], parts[3]))
     assert rows
-    for kernel, workload in rows:
+    for kernel, workload, src, sha in rows:
         v = bench.recorded_traffic(kernel, workload)
-        assert v is not None and v > 0, (kernel, workload)
+        if bench.source_hash(src) == sha:
+            assert v is not None and v > 0, (kernel, workload)
+        else:
+            assert v is None, (kernel, workload)
     # ... and turns null as soon as the source differs
     monkeypatch.setattr(bench, "source_hash", lambda *names: "000000000000")
-    for kernel, workload in rows:
+    for kernel, workload, _, _ in rows:
         assert bench.recorded_traffic(kernel, workload) is None
     assert bench.recorded_traffic("no_such_kernel", "decode_dispatch_combine") is None
 
