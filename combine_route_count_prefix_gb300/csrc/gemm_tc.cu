@@ -472,10 +472,10 @@ __device__ __forceinline__ void quant2_row(const FusedDev &p, int64_t r, int lan
         for (int u = 0; u < kV; ++u) {
             const int j = lane + 32 * u;
             if (j < p.Nh4) {
-                uint2 o;
-                o.x = pack_half2(quant_code(v[u].x, s, rs), quant_code(v[u].y, s, rs));
-                o.y = pack_half2(quant_code(v[u].z, s, rs), quant_code(v[u].w, s, rs));
-                dst[j] = o;
+                const float a[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                float c[4];
+                quant_codes<4>(a, s, rs, c);
+                dst[j] = make_uint2(pack_half2(c[0], c[1]), pack_half2(c[2], c[3]));
             }
         }
         if (lane == 0) p.s2[r] = s;
@@ -490,10 +490,10 @@ __device__ __forceinline__ void quant2_row(const FusedDev &p, int64_t r, int lan
         const float rs = __frcp_rn(s);
         for (int j = lane; j < p.Nh4; j += 32) {
             const float4 v = __ldcg(src + j);
-            uint2 o;
-            o.x = pack_half2(quant_code(v.x, s, rs), quant_code(v.y, s, rs));
-            o.y = pack_half2(quant_code(v.z, s, rs), quant_code(v.w, s, rs));
-            dst[j] = o;
+            const float a[4] = {v.x, v.y, v.z, v.w};
+            float c[4];
+            quant_codes<4>(a, s, rs, c);
+            dst[j] = make_uint2(pack_half2(c[0], c[1]), pack_half2(c[2], c[3]));
         }
         if (lane == 0) p.s2[r] = s;
     }

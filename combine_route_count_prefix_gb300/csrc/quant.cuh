@@ -6,25 +6,57 @@
 
 namespace moe {
 
+// Two floats -> one fp16x2 word (lo in the low half), round to nearest; exact
+// for the integer codes in [-127, 127].
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
-    __half a = __float2half_rn(lo), b = __float2half_rn(hi);
-    return (uint32_t)__half_as_ushort(a) | ((uint32_t)__half_as_ushort(b) << 16);
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-// Dynamic int8 quantisation code of v with scale s (s = amax / 127): the
-// round-half-even integer of the IEEE quotient v/s, clamped to [-127, 127];
-// 0 when s == 0.  rs = 1/s rounded to nearest.
+// Four integer-valued floats in [-128, 127] -> their two's-complement bytes in
+// one word (a in the low byte).  Adding 1.5 * 2^23 is exact for them and leaves
+// the integer in the low mantissa bits, so its low byte is the code's byte.
+__device__ __forceinline__ uint32_t pack_i8x4(float a, float b, float c, float d) {
+    const float kMagic = 12582912.0f;
+    const uint32_t ua = __float_as_uint(__fadd_rn(a, kMagic));
+    const uint32_t ub = __float_as_uint(__fadd_rn(b, kMagic));
+    const uint32_t uc = __float_as_uint(__fadd_rn(c, kMagic));
+    const uint32_t ud = __float_as_uint(__fadd_rn(d, kMagic));
+    const uint32_t ab = __byte_perm(ua, ub, 0x0040);   // a.b0, b.b0 in bytes 0, 1
+    const uint32_t cd = __byte_perm(uc, ud, 0x0040);
+    return __byte_perm(ab, cd, 0x5410);
+}
+
+// Dynamic int8 quantisation codes of n values with scale s (s = amax / 127):
+// for each value the round-half-even integer of the IEEE quotient v/s, clamped
+// to [-127, 127]; all 0 when s == 0.  rs = 1/s rounded to nearest.
 // Fast path: x = v * rs differs from the exact quotient by at most 2^-23
 // relatively, i.e. by less than 1.6e-5 for |v/s| <= 128, so rint(x) equals
-// rint(v/s) unless x lies within that distance of a half-integer.  Those
-// rare cases (and non-finite x) take the IEEE division, so the code is the
-// same as rint(__fdiv_rn(v, s)) for every input.
-__device__ __forceinline__ float quant_code(float v, float s, float rs) {
-    if (s == 0.0f) return 0.0f;
-    const float x = __fmul_rn(v, rs);
-    float q = rintf(x);
-    if (!(fabsf(fabsf(x - q) - 0.5f) >= 3.0e-5f)) q = rintf(__fdiv_rn(v, s));
-    return fminf(fmaxf(q, -127.0f), 127.0f);
+// rint(v/s) unless x lies within that distance of a half-integer.  Those rare
+// values (and non-finite x) take the IEEE division, so every code is the same
+// as rint(__fdiv_rn(v, s)).  The check covers all n values before the one
+// branch to the division, so the common case has no branch per value.
+template <int n>
+__device__ __forceinline__ void quant_codes(const float (&v)[n], float s, float rs, float (&q)[n]) {
+    if (s == 0.0f) {
+#pragma unroll
+        for (int i = 0; i < n; ++i) q[i] = 0.0f;
+        return;
+    }
+    uint32_t slow = 0;
+#pragma unroll
+    for (int i = 0; i < n; ++i) {
+        const float x = __fmul_rn(v[i], rs);
+        q[i] = rintf(x);
+        slow |= (uint32_t)(!(fabsf(fabsf(__fsub_rn(x, q[i])) - 0.5f) >= 3.0e-5f)) << i;
+    }
+    if (slow) {
+#pragma unroll
+        for (int i = 0; i < n; ++i)
+            if ((slow >> i) & 1u) q[i] = rintf(__fdiv_rn(v[i], s));
+    }
+#pragma unroll
+    for (int i = 0; i < n; ++i) q[i] = fminf(fmaxf(q[i], -127.0f), 127.0f);
 }
 
 }  // namespace moe

@@ -165,12 +165,11 @@ k_quant_bf16_rows(RouteDev ra, const uint4 *__restrict__ src, int32_t *__restric
         uint4 qv[kVec];
 #pragma unroll
         for (int u = 0; u < kVec; ++u) {
-            float f[8];
+            float f[8], c[8];
             unpack_bf16x8(v[u], f);
-            qv[u].x = pack_half2(quant_code(f[0], s, rs), quant_code(f[1], s, rs));
-            qv[u].y = pack_half2(quant_code(f[2], s, rs), quant_code(f[3], s, rs));
-            qv[u].z = pack_half2(quant_code(f[4], s, rs), quant_code(f[5], s, rs));
-            qv[u].w = pack_half2(quant_code(f[6], s, rs), quant_code(f[7], s, rs));
+            quant_codes<8>(f, s, rs, c);
+            qv[u] = make_uint4(pack_half2(c[0], c[1]), pack_half2(c[2], c[3]),
+                               pack_half2(c[4], c[5]), pack_half2(c[6], c[7]));
         }
         for (int d = 0; d < n; ++d) {
             const int64_t r = rows[d];
@@ -191,10 +190,7 @@ k_quant_bf16_rows(RouteDev ra, const uint4 *__restrict__ src, int32_t *__restric
 // scale.  Without smooth scales the token is quantised once and its codes are
 // written to every one of its rows.
 __device__ __forceinline__ uint2 pack_i8x8(const float (&c)[8]) {
-    uint32_t w[2] = {0u, 0u};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) w[i >> 2] |= ((uint32_t)((int32_t)c[i]) & 0xffu) << (8 * (i & 3));
-    return make_uint2(w[0], w[1]);
+    return make_uint2(pack_i8x4(c[0], c[1], c[2], c[3]), pack_i8x4(c[4], c[5], c[6], c[7]));
 }
 
 // The row stays in registers as its raw 16-byte vectors only: each pass
@@ -284,8 +280,7 @@ k_dispatch_quant(RouteDev ra, const uint4 *__restrict__ x, const float4 *__restr
                 if (j < H8) {
                     float v[8], c[8];
                     values(u, j, sm, v);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) c[i] = quant_code(v[i], sc, rs);
+                    quant_codes<8>(v, sc, rs, c);
                     const uint2 packed = pack_i8x8(c);
                     for (int dd = d0; dd < d1; ++dd) q[(int64_t)rows[dd] * H8 + j] = packed;
                 }
@@ -355,10 +350,10 @@ k_quant2(const float4 *__restrict__ g, const int32_t *__restrict__ offsets, int6
             for (int u = 0; u < kQ2Vec; ++u) {
                 const int64_t j = lane + 32 * u;
                 if (j < Nh4) {
-                    uint2 o;
-                    o.x = pack_half2(quant_code(v[u].x, s, rs), quant_code(v[u].y, s, rs));
-                    o.y = pack_half2(quant_code(v[u].z, s, rs), quant_code(v[u].w, s, rs));
-                    dst[j] = o;
+                    const float a[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                    float c[4];
+                    quant_codes<4>(a, s, rs, c);
+                    dst[j] = make_uint2(pack_half2(c[0], c[1]), pack_half2(c[2], c[3]));
                 }
             }
             if (lane == 0) s2[r] = s;
@@ -373,10 +368,10 @@ k_quant2(const float4 *__restrict__ g, const int32_t *__restrict__ offsets, int6
             const float rs = __frcp_rn(s);
             for (int64_t j = lane; j < Nh4; j += 32) {
                 const float4 v = src[j];
-                uint2 o;
-                o.x = pack_half2(quant_code(v.x, s, rs), quant_code(v.y, s, rs));
-                o.y = pack_half2(quant_code(v.z, s, rs), quant_code(v.w, s, rs));
-                dst[j] = o;
+                const float a[4] = {v.x, v.y, v.z, v.w};
+                float c[4];
+                quant_codes<4>(a, s, rs, c);
+                dst[j] = make_uint2(pack_half2(c[0], c[1]), pack_half2(c[2], c[3]));
             }
             if (lane == 0) s2[r] = s;
         }
