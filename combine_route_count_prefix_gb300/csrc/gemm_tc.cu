@@ -109,7 +109,17 @@ struct GemmDev {
     const float *scale2;
     const float *s2;
     int32_t *status;
+    int y_vec32;        // y rows start on 32-byte boundaries: 32-byte stores
 };
+
+// One 32-byte store (eight 32-bit words) to a 32-byte aligned global address.
+__device__ __forceinline__ void st_global_v8(void *p, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d, uint32_t e, uint32_t f, uint32_t g,
+                                             uint32_t h) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a),
+                 "r"(b), "r"(c), "r"(d), "r"(e), "r"(f), "r"(g), "r"(h)
+                 : "memory");
+}
 
 struct Tile {
     int e, row0, rows, nb;
@@ -201,22 +211,37 @@ __device__ __forceinline__ void epilogue_store(const GemmDev &p, const Tile &t, 
         const int c0 = t.nb * BN + hf * 128;
         const float s2 = p.s2[row];
         const float *sc = p.scale2 + (int64_t)t.e * p.Nout + c0;
-        uint4 *dst = reinterpret_cast<uint4 *>(p.y + (int64_t)row * p.Nout + c0);
+        __nv_bfloat16 *dst = p.y + (int64_t)row * p.Nout + c0;
+        // bf16 of (acc * scale2) * s2 for tile columns 8i .. 8i + 7, as four words
+        auto dequant8 = [&](int i, uint32_t (&w)[4]) {
+            const float4 sa = __ldg(reinterpret_cast<const float4 *>(sc) + 2 * i);
+            const float4 sb = __ldg(reinterpret_cast<const float4 *>(sc) + 2 * i + 1);
+            const float sv[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            if (c0 + 8 * i < p.Nout) {
-                const float4 sa = __ldg(reinterpret_cast<const float4 *>(sc) + 2 * i);
-                const float4 sb = __ldg(reinterpret_cast<const float4 *>(sc) + 2 * i + 1);
-                const float sv[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
-                uint32_t w[4];
+            for (int u = 0; u < 4; ++u) {
+                float lo = __fmul_rn(__fmul_rn(__int2float_rn(acc[8 * i + 2 * u]), sv[2 * u]), s2);
+                float hi = __fmul_rn(__fmul_rn(__int2float_rn(acc[8 * i + 2 * u + 1]), sv[2 * u + 1]), s2);
+                w[u] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+                       ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+            }
+        };
+        if (p.y_vec32 && c0 + 128 <= p.Nout) {
+            // y rows start on 32-byte boundaries and c0 is a multiple of 128
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    float lo = __fmul_rn(__fmul_rn(__int2float_rn(acc[8 * i + 2 * u]), sv[2 * u]), s2);
-                    float hi = __fmul_rn(__fmul_rn(__int2float_rn(acc[8 * i + 2 * u + 1]), sv[2 * u + 1]), s2);
-                    w[u] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
-                           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+            for (int i = 0; i < 16; i += 2) {
+                uint32_t a[4], b[4];
+                dequant8(i, a);
+                dequant8(i + 1, b);
+                st_global_v8(dst + 8 * i, a[0], a[1], a[2], a[3], b[0], b[1], b[2], b[3]);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                if (c0 + 8 * i < p.Nout) {
+                    uint32_t w[4];
+                    dequant8(i, w);
+                    reinterpret_cast<uint4 *>(dst)[i] = make_uint4(w[0], w[1], w[2], w[3]);
                 }
-                dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
             }
         }
     }
@@ -735,8 +760,13 @@ __device__ __forceinline__ PairTile decode_pair_tile(int64_t tile, int n_blocks,
 //               whole stage and no thread relays the peer's landing.
 //   warp 1      TMEM (pair allocation); CTA 0: MMA issuer
 //   warps 2..9  epilogue; their accumulator-free signal goes to CTA 0
-// Commits arrive on both CTAs' barriers (multicast).  Every wait is bounded;
-// both CTAs meet at a cluster barrier before either frees TMEM or exits.
+// Commits arrive on both CTAs' barriers (multicast).  Waits acquire at CTA
+// scope and the epilogue's accumulator-free arrivals release at CTA scope:
+// the barriers order tensor-memory and shared-memory use, which the tcgen05
+// fences and the copies' transaction counts cover, and a cluster-scope release
+// would stall each arrival behind the warp's outstanding output stores.  Every
+// wait is bounded; both CTAs meet at a cluster barrier before either frees
+// TMEM or exits.
 template <int EPI>
 __global__ void __launch_bounds__(THREADS, 1)
 k_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -822,7 +852,7 @@ k_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const PairTile t = decode_pair_tile(tile, p.n_blocks, p.E, s_psched, s_off, rank);
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     // freed by CTA 0's commit once the MMAs have read both halves
-                    if (!wait_bounded_cluster(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                    if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
                     uint8_t *sa = smem + (size_t)stage * P_STAGE_BYTES;
                     if (leader) {
                         mbar_arrive_expect_tx(&full[stage], 2 * P_STAGE_BYTES);
@@ -860,12 +890,12 @@ k_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             bool ok = true;
             for (int64_t tile = first; ok && tile < total_tiles; tile += step) {
                 for (int kb0 = 0; ok && kb0 < p.num_kb; kb0 += CHUNK_KB) {
-                    if (!wait_bounded_cluster(&acc_empty[accb], acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                    if (!wait_bounded(&acc_empty[accb], acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + (uint32_t)(accb * BN);
                     const int kb1 = min(kb0 + CHUNK_KB, p.num_kb);
                     for (int kb = kb0; kb < kb1; ++kb) {
-                        if (!wait_bounded_cluster(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+                        if (!wait_bounded(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
                         tc_fence_after();
                         const uint32_t a_addr = smem_u32(smem + (size_t)stage * P_STAGE_BYTES);
                         const uint32_t b_addr = a_addr + A_BYTES;
@@ -898,7 +928,7 @@ k_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             int32_t acc[128];
             bool ok = true;
             for (int c = 0; c < num_chunks; ++c) {
-                const bool w = wait_bounded_cluster(&acc_full[accb], acc_phase, abort_flag, p.status);
+                const bool w = wait_bounded(&acc_full[accb], acc_phase, abort_flag, p.status);
                 if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
                 tc_fence_after();
                 if (rows_here) {
@@ -918,7 +948,7 @@ k_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(&acc_empty[accb], 0);
+                if (lane == 0) mbar_arrive_remote(&acc_empty[accb], 0);
                 if (++accb == 2) { accb = 0; acc_phase ^= 1u; }
             }
             if (!ok) break;
@@ -1010,6 +1040,8 @@ GemmDev gemm_dev(const GemmArgs &a) {
     d.scale2 = a.scale2;
     d.s2 = a.s2;
     d.status = a.status;
+    // 32-byte stores need every y row to start on a 32-byte boundary
+    d.y_vec32 = a.y != nullptr && ((uintptr_t)a.y % 32) == 0 && ((a.Nout * 2) % 32) == 0;
     return d;
 }
 

@@ -47,25 +47,15 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
         : "memory");
     return ok != 0;
 }
-// The same with acquire at cluster scope, for barriers that threads of the
-// peer CTA arrive on.
-__device__ __forceinline__ bool mbar_try_wait_sleep_cluster(uint64_t *bar, uint32_t parity, uint32_t ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
-        : "memory");
-    return ok != 0;
-}
-// Arrive (release, cluster scope) on the barrier at the same shared-memory
-// offset in CTA `rank` of the cluster.
-__device__ __forceinline__ void mbar_arrive_cluster(uint64_t *bar, uint32_t rank) {
+// Arrive on the barrier at the same shared-memory offset in CTA `rank` of the
+// cluster, with the default (CTA-scope) release: the arrival orders nothing
+// but the thread's own shared-memory and tensor-memory work that the caller
+// has already completed and fenced, so it does not wait for the thread's
+// outstanding global stores the way a cluster-scope release does.
+__device__ __forceinline__ void mbar_arrive_remote(uint64_t *bar, uint32_t rank) {
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(bar)), "r"(rank));
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
 }
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
@@ -103,6 +93,12 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
         : "memory");
 }
 
+// Hint: bring `bytes` (a multiple of 16) at the 16-byte aligned global address
+// `src` into L2, without a destination in shared memory or a completion.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Waits for phase `parity` of `bar`.  Gives up when the CTA's abort flag is set
 // or after limit_ns (kTimeoutNs unless a caller passes a shorter limit),
 // setting the abort flag and the status bit.  The first test is inline; the
@@ -129,27 +125,4 @@ __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, vol
     if (mbar_try_wait(bar, parity)) return true;
     return wait_bounded_loop(bar, parity, abort_flag, status, honour_abort);
 }
-// wait_bounded for a barrier that the peer CTA of a cluster arrives on.
-static __device__ __noinline__ bool wait_bounded_cluster_loop(uint64_t *bar, uint32_t parity,
-                                                              volatile int *abort_flag,
-                                                              int32_t *status, bool honour_abort) {
-    const uint64_t t0 = globaltimer();
-    for (;;) {
-        if (mbar_try_wait_sleep_cluster(bar, parity, kWaitSliceNs)) return true;
-        if (honour_abort && *abort_flag) return false;
-        if (globaltimer() - t0 > kTimeoutNs) {
-            *abort_flag = 1;
-            if (status) atomicOr(status, MOE_DEV_TIMEOUT);
-            return false;
-        }
-    }
-}
-
-__device__ __forceinline__ bool wait_bounded_cluster(uint64_t *bar, uint32_t parity,
-                                                     volatile int *abort_flag, int32_t *status,
-                                                     bool honour_abort = true) {
-    if (mbar_try_wait_sleep_cluster(bar, parity, 0)) return true;
-    return wait_bounded_cluster_loop(bar, parity, abort_flag, status, honour_abort);
-}
-
 }  // namespace moe

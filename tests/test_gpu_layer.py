@@ -340,3 +340,25 @@ def test_layer_with_zero_and_copy_experts(B):
     assert ulp <= 2.0 and rel <= 1e-3, (ulp, rel)
     r = oracle.route(ids, E, P, zero_experts=Z, copy_experts=C)
     np.testing.assert_array_equal(B.stage_views(shape, ws)["route_row"].cpu().numpy(), r["route_row"])
+
+
+@pytest.mark.parametrize("path", ["large", "large_pair", "small"])
+def test_grouped_ffn_output_alignment(B, path):
+    """y rows that start on 16- but not 32-byte boundaries take the GEMM2
+    epilogue's 16-byte stores; the result is bit-identical to a 32-byte
+    aligned y."""
+    w = wl.custom(P=2, M=80, H=512, E=6, K=3, N=512)
+    T, P, H, E, K, N = (w.num_tokens, w.num_partitions, w.hidden, w.num_experts, w.topk, w.ffn)
+    inp = wl.make_inputs(w, seed=12)
+    W1, S1, W2, S2 = wl.all_expert_weights(w, seed=12)
+    shape = B.make_shape(T, P, H, E, K, N, ffn_path=path)
+    (o1, w1p), (o2, w2p) = _device_weights(B, shape, W1, W2)
+    d = B.dispatch(dev_bf16(inp["x"]), dev(inp["ids"]), E, P)
+    y_al, _ = B.grouped_ffn(shape, d["expand_x"], d["expert_offsets"], w1p, dev(S1), w2p, dev(S2))
+    buf = torch.empty(T * K * H + 8, dtype=torch.bfloat16, device="cuda")
+    y_off = buf[8:].view(T * K, H)
+    assert y_off.data_ptr() % 32 == 16
+    B.grouped_ffn(shape, d["expand_x"], d["expert_offsets"], w1p, dev(S1), w2p, dev(S2), y=y_off)
+    torch.cuda.synchronize()
+    R = int(d["expert_offsets"][-1].item())
+    np.testing.assert_array_equal(host_bits(y_al[:R]), host_bits(y_off[:R]))
