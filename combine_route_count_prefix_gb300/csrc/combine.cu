@@ -161,6 +161,7 @@ k_combine(CombineArgs a) {
         bool ok = true;
         int32_t rr[kMaxTopK];
         float pp[kMaxTopK];
+        const uint64_t read_once = l2_policy_evict_first();
         // metadata of the batch starting at tb, for token tb + lane, into registers
         auto load_meta = [&](int64_t ib) {
             const bool in = ib + lane < ntok;
@@ -254,15 +255,18 @@ k_combine(CombineArgs a) {
                         issued_phase[stage] = (int)phase;
                     }
                     __syncwarp();
+                    // every input is read once: evict-first keeps the rows still to
+                    // come (the row copy leaves the last tokens' rows in L2) in place
                     if (my_code >= 0)
-                        bulk_load(dst + (size_t)my_slot * a.seg_vecs * 16,
-                                  a.y + (int64_t)my_code * a.H8 + v0, bytes, &full[stage]);
+                        bulk_load_hint(dst + (size_t)my_slot * a.seg_vecs * 16,
+                                       a.y + (int64_t)my_code * a.H8 + v0, bytes, &full[stage],
+                                       read_once);
                     else if (lane == a.K && a.shared)
-                        bulk_load(dst + (size_t)a.K * a.seg_vecs * 16, a.shared + tt * a.H8 + v0,
-                                  bytes, &full[stage]);
+                        bulk_load_hint(dst + (size_t)a.K * a.seg_vecs * 16,
+                                       a.shared + tt * a.H8 + v0, bytes, &full[stage], read_once);
                     else if (lane == a.K + 1 && need_ori)
-                        bulk_load(dst + (size_t)(a.K + 1) * a.seg_vecs * 16,
-                                  a.ori_x + tt * a.H8 + v0, bytes, &full[stage]);
+                        bulk_load_hint(dst + (size_t)(a.K + 1) * a.seg_vecs * 16,
+                                       a.ori_x + tt * a.H8 + v0, bytes, &full[stage], read_once);
                     if (++stage == a.stages) { stage = 0; phase ^= 1u; }
                 }
             }

@@ -27,15 +27,21 @@ __device__ __forceinline__ uint32_t pack_i8x4(float a, float b, float c, float d
     return __byte_perm(ab, cd, 0x5410);
 }
 
-// Dynamic int8 quantisation codes of n values with scale s (s = amax / 127):
-// for each value the round-half-even integer of the IEEE quotient v/s, clamped
-// to [-127, 127]; all 0 when s == 0.  rs = 1/s rounded to nearest.
+// Dynamic int8 quantisation codes of n values with scale s (s = amax / 127,
+// amax the largest |v| of the row): for each value the round-half-even
+// integer of the IEEE quotient v/s, clamped to [-127, 127]; all 0 when s == 0.
+// rs = 1/s rounded to nearest.
 // Fast path: x = v * rs differs from the exact quotient by at most 2^-23
 // relatively, i.e. by less than 1.6e-5 for |v/s| <= 128, so rint(x) equals
-// rint(v/s) unless x lies within that distance of a half-integer.  Those rare
-// values (and non-finite x) take the IEEE division, so every code is the same
-// as rint(__fdiv_rn(v, s)).  The check covers all n values before the one
-// branch to the division, so the common case has no branch per value.
+// rint(v/s) unless x lies within that distance of a half-integer: the guard
+// below keeps every x whose distance d = |x - rint(x)| to its integer is at
+// most 0.5 - 3e-5.  For finite x, |x| <= 127 * (1 + 3 * 2^-24) < 127.5, so
+// rint(x) needs no clamp.  The rare values beyond the guard (and non-finite
+// x) take the IEEE division and the clamp, so every code is the same as
+// clamp(rint(__fdiv_rn(v, s))).  The guard is tested for all n values before
+// the one branch to the division, so the common case has no branch per value.
+constexpr float kTieGuard = 0.5f - 3.0e-5f;
+
 template <int n>
 __device__ __forceinline__ void quant_codes(const float (&v)[n], float s, float rs, float (&q)[n]) {
     if (s == 0.0f) {
@@ -43,20 +49,21 @@ __device__ __forceinline__ void quant_codes(const float (&v)[n], float s, float 
         for (int i = 0; i < n; ++i) q[i] = 0.0f;
         return;
     }
-    uint32_t slow = 0;
+    bool slow = false;
 #pragma unroll
     for (int i = 0; i < n; ++i) {
         const float x = __fmul_rn(v[i], rs);
         q[i] = rintf(x);
-        slow |= (uint32_t)(!(fabsf(fabsf(__fsub_rn(x, q[i])) - 0.5f) >= 3.0e-5f)) << i;
+        slow = slow || !(fabsf(__fsub_rn(x, q[i])) <= kTieGuard);
     }
     if (slow) {
 #pragma unroll
-        for (int i = 0; i < n; ++i)
-            if ((slow >> i) & 1u) q[i] = rintf(__fdiv_rn(v[i], s));
+        for (int i = 0; i < n; ++i) {
+            const float x = __fmul_rn(v[i], rs);
+            if (!(fabsf(__fsub_rn(x, q[i])) <= kTieGuard))
+                q[i] = fminf(fmaxf(rintf(__fdiv_rn(v[i], s)), -127.0f), 127.0f);
+        }
     }
-#pragma unroll
-    for (int i = 0; i < n; ++i) q[i] = fminf(fmaxf(q[i], -127.0f), 127.0f);
 }
 
 }  // namespace moe

@@ -6,6 +6,7 @@
 // (up to 8 x 16 B), and then writes it once per destination.  H is a multiple
 // of 8, so a 16-byte vector never straddles a row.
 #include "common.cuh"
+#include "ptx.cuh"
 #include "quant.cuh"
 
 namespace moe {
@@ -20,6 +21,12 @@ __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
     return v;
+}
+
+__device__ __forceinline__ void st_hint(uint4 *p, const uint4 &v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p), "r"(v.x),
+                 "r"(v.y), "r"(v.z), "r"(v.w), "l"(policy)
+                 : "memory");
 }
 
 __device__ __forceinline__ void unpack_bf16x8(const uint4 &v, float (&f)[8]) {
@@ -51,12 +58,17 @@ __device__ __forceinline__ float block_max(float v, float *scratch /*[32]*/) {
 
 // ---------------------------------------------------------------- dispatch copy
 // expand_x[route_row[t*K+k]] = x[t] for every active route of token t.
+// The rows of tokens t >= keep_from are stored with an L2 evict-last policy
+// and the others evict-first: the combine reads tokens from the last one
+// down, so the rows it reads first are still in L2 when it starts.
 __global__ void __launch_bounds__(kRowThreads)
 k_dispatch_rows(RouteDev ra, const uint4 *__restrict__ x, int32_t *__restrict__ route_row,
-                int32_t *__restrict__ assist, uint4 *__restrict__ expand_x, int64_t H8) {
+                int32_t *__restrict__ assist, uint4 *__restrict__ expand_x, int64_t H8,
+                int64_t keep_from) {
     __shared__ int32_t rows[kMaxTopK];
     const int64_t T = ra.T;
     const int K = (int)ra.K;
+    const uint64_t keep = l2_policy_evict_last(), pass = l2_policy_evict_first();
     uint4 v[kVec];
     auto load_row = [&](int64_t t, int64_t j0) {
 #pragma unroll
@@ -97,6 +109,7 @@ k_dispatch_rows(RouteDev ra, const uint4 *__restrict__ x, int32_t *__restrict__ 
         for (int64_t j0 = threadIdx.x; j0 < H8; j0 += (int64_t)kRowThreads * kVec) {
             if (!preloaded) load_row(t, j0);
             preloaded = false;
+            const uint64_t pol = t >= keep_from ? keep : pass;
             for (int k = 0; k < K; ++k) {
                 int32_t r = rows[k];
                 if (r < 0) continue;
@@ -104,7 +117,7 @@ k_dispatch_rows(RouteDev ra, const uint4 *__restrict__ x, int32_t *__restrict__ 
 #pragma unroll
                 for (int u = 0; u < kVec; ++u) {
                     int64_t j = j0 + (int64_t)u * kRowThreads;
-                    if (j < H8) dst[j] = v[u];
+                    if (j < H8) st_hint(dst + j, v[u], pol);
                 }
             }
         }
@@ -235,13 +248,9 @@ k_dispatch_quant(RouteDev ra, const uint4 *__restrict__ x, const float4 *__restr
             for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(v[i], m[i]);
         }
     };
-    load_row(blockIdx.x);
-    pdl_wait();
-    for (int64_t t = blockIdx.x; t < ra.T; t += gridDim.x) {
-        if (t != blockIdx.x) load_row(t);
-        __syncthreads();   // the previous token's rows are no longer read
+    // lane k resolves slot k of token t; the active rows are packed in slot order
+    auto resolve_rows = [&](int64_t t) {
         if (threadIdx.x < 32) {
-            // lane k resolves slot k; the active rows are packed in slot order
             const int k = threadIdx.x;
             const int32_t e = k < K ? ra.ids[t * K + k] : 0;
             const int32_t r = k < K ? resolve_route_row(ra, t, k, route_row, assist) : -1;
@@ -253,6 +262,66 @@ k_dispatch_quant(RouteDev ra, const uint4 *__restrict__ x, const float4 *__restr
             }
             if (k == 0) nrows = __popc(act);
         }
+    };
+    if constexpr (!kSmooth) {
+        // Every destination gets the token's own codes, which depend on x alone:
+        // the first token's scale and codes are computed before the wait on the
+        // routing kernel, so only its stores wait for the route rows.
+        uint2 codes[kVec];
+        float sc = 0.0f;
+        auto quantise_token = [&]() {
+            float amax = 0.0f;
+#pragma unroll
+            for (int u = 0; u < kVec; ++u) {
+                const int64_t j = threadIdx.x + (int64_t)u * kRowThreads;
+                if (j < H8) {
+                    float v[8];
+                    values(u, j, nullptr, v);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+                }
+            }
+            amax = block_max(amax, scratch);
+            sc = __fdiv_rn(amax, 127.0f);
+            const float rs = __frcp_rn(sc);
+#pragma unroll
+            for (int u = 0; u < kVec; ++u) {
+                float v[8], c[8];
+                values(u, 0, nullptr, v);
+                quant_codes<8>(v, sc, rs, c);
+                codes[u] = pack_i8x8(c);
+            }
+        };
+        load_row(blockIdx.x);
+        quantise_token();
+        pdl_wait();
+        for (int64_t t = blockIdx.x; t < ra.T; t += gridDim.x) {
+            if (t != blockIdx.x) {
+                load_row(t);
+                quantise_token();
+            }
+            __syncthreads();   // the previous token's rows are no longer read
+            resolve_rows(t);
+            __syncthreads();
+            const int n = nrows;
+            for (int d = 0; d < n; ++d) {
+                const int64_t r = rows[d];
+#pragma unroll
+                for (int u = 0; u < kVec; ++u) {
+                    const int64_t j = threadIdx.x + (int64_t)u * kRowThreads;
+                    if (j < H8) q[r * H8 + j] = codes[u];
+                }
+                if (threadIdx.x == 0) s_out[r] = sc;
+            }
+        }
+        return;
+    }
+    load_row(blockIdx.x);
+    pdl_wait();
+    for (int64_t t = blockIdx.x; t < ra.T; t += gridDim.x) {
+        if (t != blockIdx.x) load_row(t);
+        __syncthreads();   // the previous token's rows are no longer read
+        resolve_rows(t);
         __syncthreads();
         const int n = nrows;
         if (n == 0) continue;
@@ -477,11 +546,17 @@ int grid_for(int64_t items, int per_sm) {
 
 }  // namespace
 
+#ifndef MOE_ROWS_L2_KEEP_MB
+#define MOE_ROWS_L2_KEEP_MB 128
+#endif
 moe_status launch_dispatch_rows(const RouteDev &r, const void *x, int32_t *route_row,
                                 int32_t *assist, void *expand_x, int64_t H, cudaStream_t stream) {
     if (r.T == 0) return MOE_OK;
+    // the last tokens whose rows (K per token at most) fit the L2 budget
+    const int64_t keep_tokens = ((int64_t)MOE_ROWS_L2_KEEP_MB << 20) / (r.K * H * 2);
+    const int64_t keep_from = r.T > keep_tokens ? r.T - keep_tokens : 0;
     MOE_LAUNCH("dispatch_rows", k_dispatch_rows, grid_for(r.T, 16), kRowThreads, 0, stream, r,
-               (const uint4 *)x, route_row, assist, (uint4 *)expand_x, H / 8);
+               (const uint4 *)x, route_row, assist, (uint4 *)expand_x, H / 8, keep_from);
     return MOE_OK;
 }
 
