@@ -37,6 +37,23 @@ def test_dispatch_quant_parity(B, smooth, mask_kind):
     np.testing.assert_array_equal(d["dynamic_scales"][:R].cpu().numpy(), s)
 
 
+def test_dispatch_quant_many_tokens_per_cta(B):
+    """12288 tokens: about ten per resident CTA, so each CTA quantises its first
+    tokens before the wait on routing (codes staged in shared memory) and the
+    rest after it; both kinds must be exact."""
+    w = wl.custom(P=12, M=1024, H=520, E=64, K=4, mask_kind=1, mask_p=0.9)
+    inp = wl.make_inputs(w, seed=45)
+    E, P = w.num_experts, w.num_partitions
+    d = B.dispatch_quant(dev_bf16(inp["x"]), dev(inp["ids"]), E, P, mask=dev(inp["mask"]))
+    torch.cuda.synchronize()
+    r = oracle.route(inp["ids"], E, P, inp["mask"])
+    R = r["R"]
+    np.testing.assert_array_equal(d["route_row"].cpu().numpy(), r["route_row"])
+    q, s = oracle.dispatch_quant(inp["x"], inp["ids"], r["route_row"], R)
+    np.testing.assert_array_equal(d["expand_x"][:R].cpu().numpy(), q)
+    np.testing.assert_array_equal(d["dynamic_scales"][:R].cpu().numpy(), s)
+
+
 @pytest.mark.parametrize("path", ["large", "small"])
 def test_ffn_on_quantised_rows_equals_ffn_on_bf16_rows(B, path):
     w = wl.custom(P=2, M=96, H=512, E=6, K=3, N=512)
