@@ -33,9 +33,13 @@
  * Parity pins: every function below is checked by the CPU test suite against
  * something other than itself (library restatements, closed forms,
  * brute force, invariants, and small fixtures worked by hand from the cited
- * definitions).  The FFN's numeric conventions above are pinned
- * only by those readings, not by a value printed on the pages: for them
- * parity is "unpinned" in the sense that the pages print no number to match.
+ * definitions).  Where the pages leave a convention open (the readings
+ * above), the pins check the oracle against that reading; the pages print no
+ * value of the FFN's output to compare with.
+ *
+ * The threaded drivers at the end of the file add no arithmetic: they split
+ * tokens or rows into contiguous slices over pthreads and call the functions
+ * above on each slice.
  */
 #include <math.h>
 #include <pthread.h>
