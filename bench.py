@@ -21,7 +21,9 @@ captured once as a CUDA graph and replayed (flushed and hot), so that launch
 overhead shows separately; `dispatch_quant` times moe_dispatch_quant (int8 rows
 and per-row scales) on the same inputs.  `e2e` repeats the step through the same C ABI
 calls with pinned host inputs: host->device copies, the step, and the
-device->host copy of the output are inside the timed region.
+device->host copy of the output are inside the timed region.  The same copy
+loop is then timed without the kernels (`copies_only_ms_per_step`): the host
+link's own time for a step's bytes, which bounds the end-to-end rate.
 
 Under torchrun (N > 1) every rank runs the same workload on its own GPU with
 its own seed and no collective on the data path (weak scaling, replicas).
@@ -701,7 +703,7 @@ def run_ours(args, rank, world, dist):
     d2h = hout.numel() * hout.element_size()
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
-    def e2e_run(nsteps, start=None, end=None):
+    def e2e_run(nsteps, start=None, end=None, compute=True):
         ev_in = [torch.cuda.Event() for _ in range(nsteps)]
         ev_comp = [torch.cuda.Event() for _ in range(nsteps)]
         ev_out = [torch.cuda.Event() for _ in range(nsteps)]
@@ -720,9 +722,11 @@ def run_ours(args, rank, world, dist):
             stream.wait_event(ev_in[i])
             if i >= 2:
                 stream.wait_event(ev_out[i - 2])       # step i-2's output has been read back
-            flush.fill_(1)
-            path.step(b["x"].view(torch.bfloat16), b["ids"], b["probs"], b["mask"],
-                      None if b["shared"] is None else b["shared"].view(torch.bfloat16), out=b["out"])
+            if compute:
+                flush.fill_(1)
+                path.step(b["x"].view(torch.bfloat16), b["ids"], b["probs"], b["mask"],
+                          None if b["shared"] is None else b["shared"].view(torch.bfloat16),
+                          out=b["out"])
             ev_comp[i].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_comp[i])
@@ -737,6 +741,13 @@ def run_ours(args, rank, world, dist):
     e2e_run(args.steps, e0, e1)
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, dev)
+    # the same copies alone (same streams, bytes and ordering, no kernels): the
+    # host link's own time for a step's inputs and output
+    e2e_run(3, compute=False)
+    barrier()
+    e2e_run(args.steps, e0, e1, compute=False)
+    barrier()
+    link_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, dev)
 
     secondary = None
     if not args.no_layer and w.identity:
@@ -756,6 +767,7 @@ def run_ours(args, rank, world, dist):
         "roofline": roofline, "cpu_baseline": cpu,
         "e2e": {"value": whole_job_tokens_per_s(T, world, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "copies_only_ms_per_step": link_ms, "frac_of_copies_only": link_ms / e2e_ms,
                 "copies": "pinned host buffers; neighbouring steps' copies overlap compute on "
                           "their own streams (double-buffered device tensors)"},
         "gpu_launches": launches, "clocks": clk, "routed_rows": R,
