@@ -80,6 +80,9 @@ def parse():
     ap.add_argument("--soak", type=float, default=2.0,
                     help="seconds of untimed steps before the timed region (clock samples)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-full", action="store_true",
+                    help="one GPU step, then the oracle over the whole workload on every host "
+                         "core (timed) and every output token compared with it; one JSON line")
     ap.add_argument("--ffn-path", default="auto", choices=["auto", "large", "small", "large_pair", "fused"],
                     help="grouped-GEMM kernels of the layer workloads (auto: small-batch "
                          "kernels when T*K <= 32*E)")
@@ -292,6 +295,68 @@ def run_reference(args, rank, world):
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
+    print(json.dumps(line), flush=True)
+
+
+def bf16_errors(got_bits, ref_bits):
+    """Output errors in bf16 ulps taken at the oracle value's magnitude."""
+    g = wl.bf16_bits_to_f32(got_bits).astype(np.float64)
+    r = wl.bf16_bits_to_f32(ref_bits).astype(np.float64)
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(r), 2.0 ** -126))) - 7)
+    e = np.abs(g - r) / ulp
+    tok_max = e.max(axis=1) if e.size else np.zeros(0)
+    return {"tokens": int(got_bits.shape[0]), "max_ulp": float(e.max()) if e.size else 0.0,
+            "rel_l2": float(np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-30)),
+            "tokens_within_2_ulp": int((tok_max <= 2.0).sum()),
+            "tokens_bit_exact": int((got_bits == ref_bits).all(axis=1).sum())}
+
+
+def run_cpu_full(args):
+    """The oracle once over the whole workload on every host core, timed, and
+    every output token of one GPU step (the benchmark's launch configuration)
+    compared with it."""
+    import torch
+    import oracle
+    from combine_route_count_prefix_gb300 import binding as B
+    B.lib()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    w = select_workload(args)
+    T = w.num_tokens
+    inp = wl.make_inputs(w, seed=args.seed)
+    threads = host_cores()
+    oracle.build()
+    if w.identity:
+        path = IdentityPath(B, w, inp, dev)
+        path.step()
+        torch.cuda.synchronize()
+        got = path.out.view(torch.int16).cpu().numpy().view(np.uint16)
+        del path
+        t0 = time.perf_counter()
+        _, _, ref = oracle.dispatch_combine_identity(
+            inp["x"], inp["ids"], inp["probs"], w.num_experts, w.num_partitions,
+            mask=inp["mask"], shared=inp["shared"], threads=threads)
+        dt = time.perf_counter() - t0
+        what = "routing, row gather and combine"
+    else:
+        path = LayerPath(B, w, inp, dev, args.seed, args.ffn_path)
+        torch.cuda.synchronize()
+        status = B.read_device_status(path.ws)
+        got = path.out.view(torch.int16).cpu().numpy().view(np.uint16)
+        del path
+        torch.cuda.empty_cache()
+        W1, S1, W2, S2 = wl.all_expert_weights(w, seed=args.seed, threads=threads)
+        t0 = time.perf_counter()
+        ref, ovf = oracle.layer_tokens(inp["x"], inp["ids"], inp["probs"], W1, S1, W2, S2,
+                                       np.arange(T, dtype=np.int64), mask=inp["mask"],
+                                       shared=inp["shared"], threads=threads)
+        dt = time.perf_counter() - t0
+        assert not ovf and status == 0
+        what = f"every token through the whole layer ({w.topk} expert FFNs each, then combine)"
+    line = {"cpu_full": {"workload": w.name, "config": workload_config(w), "kind": "oracle",
+                         "value": T / dt, "unit": "tokens/s", "seconds": dt, "cores": threads,
+                         "nproc": host_cores(), "run": f"the whole workload once: {what}"},
+            "parity_full": bf16_errors(got, ref)}
     print(json.dumps(line), flush=True)
 
 
@@ -799,6 +864,9 @@ def main():
             dist = tdist
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif args.cpu_full:
+        if rank == 0 and world == 1:
+            run_cpu_full(args)
     else:
         run_ours(args, rank, world, dist)
     if dist is not None:
