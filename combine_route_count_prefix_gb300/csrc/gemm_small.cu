@@ -76,7 +76,7 @@ static_assert(A_COL0 + SA * A_STAGE_COLS <= TMEM_COLS, "TMEM budget");
 static_assert(2 * TB <= (int)ACC_COLS, "accumulators");
 static_assert(BK / 16 == 4 * ISSUERS, "k-steps split between the issuers");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert((2 * S8 + 3 * SA + 5) * 8 + 16 <= (int)kBarrierBytes, "barrier area");
+static_assert((2 * S8 + 2 * SA + 5) * 8 + 16 <= (int)kBarrierBytes, "barrier area");
 
 struct SmallDev {
     const int32_t *offsets;
@@ -179,12 +179,14 @@ k_gemm_small(const __grid_constant__ CUtensorMap tmRows, const __grid_constant__
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t *ringB = smem;                                   // SA x 16 KB fp16 rows
-    uint8_t *ring8 = ringB + (size_t)SA * B_BYTES;           // S8 x 8 KB biased int8 weights
+    uint8_t *ring8 = ringB + (size_t)SA * B_BYTES;           // S8 x 16 KB biased int8 weights
     uint64_t *w8_full = reinterpret_cast<uint64_t *>(smem + RING_BYTES);
     uint64_t *w8_empty = w8_full + S8;
-    uint64_t *a_full = w8_empty + S8;
-    uint64_t *b_full = a_full + SA;
-    uint64_t *ab_empty = b_full + SA;
+    // ab_full[s]: operand stage s is complete -- the four converter warps have
+    // written its A columns and the row producer's copies have landed (one
+    // barrier, so the issuers test one phase per k-block)
+    uint64_t *ab_full = w8_empty + S8;
+    uint64_t *ab_empty = ab_full + SA;
     uint64_t *acc_full = ab_empty + SA;
     uint64_t *acc_empty = acc_full + 2;
     uint64_t *drain = acc_empty + 2;
@@ -201,8 +203,7 @@ k_gemm_small(const __grid_constant__ CUtensorMap tmRows, const __grid_constant__
             mbar_init(&w8_empty[s], 4);
         }
         for (int s = 0; s < SA; ++s) {
-            mbar_init(&a_full[s], 4);
-            mbar_init(&b_full[s], 1);
+            mbar_init(&ab_full[s], 4 + 1);
             mbar_init(&ab_empty[s], ISSUERS);
         }
         for (int b = 0; b < 2; ++b) {
@@ -286,11 +287,11 @@ k_gemm_small(const __grid_constant__ CUtensorMap tmRows, const __grid_constant__
                 const int nbox = (t.rows + BOX_ROWS - 1) / BOX_ROWS;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!wait_bounded(&ab_empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&b_full[stage], (uint32_t)(2 * nbox * BOX_BYTES));
+                    mbar_arrive_expect_tx(&ab_full[stage], (uint32_t)(2 * nbox * BOX_BYTES));
                     uint8_t *dst = ringB + (size_t)stage * B_BYTES;
                     for (int h = 0; h < 2; ++h)
                         for (int i = 0; i < nbox; ++i)
-                            tma_load_2d(dst + h * B_HALF_BYTES + i * BOX_BYTES, &tmRows, &b_full[stage],
+                            tma_load_2d(dst + h * B_HALF_BYTES + i * BOX_BYTES, &tmRows, &ab_full[stage],
                                         kb * BK + h * BKH, t.row0 + i * BOX_ROWS);
                     issued_phase[stage] = (int)phase;
                     if (++stage == SA) { stage = 0; phase ^= 1u; }
@@ -298,7 +299,7 @@ k_gemm_small(const __grid_constant__ CUtensorMap tmRows, const __grid_constant__
             }
             for (int s = 0; s < SA; ++s)
                 if (issued_phase[s] >= 0)
-                    wait_bounded(&b_full[s], (uint32_t)issued_phase[s], abort_flag, p.status, false);
+                    wait_bounded(&ab_full[s], (uint32_t)issued_phase[s], abort_flag, p.status, false);
         }
     } else if (warp >= CONV_WARP0 && warp < CONV_WARP0 + 4) {
         // ---------------------------------------------------- converters
@@ -340,7 +341,7 @@ k_gemm_small(const __grid_constant__ CUtensorMap tmRows, const __grid_constant__
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&w8_empty[s8]);
-                    mbar_arrive(&a_full[sa]);
+                    mbar_arrive(&ab_full[sa]);
                 }
                 if (++s8 == S8) { s8 = 0; ph8 ^= 1u; }
                 if (++sa == SA) { sa = 0; pha ^= 1u; }
@@ -365,8 +366,7 @@ k_gemm_small(const __grid_constant__ CUtensorMap tmRows, const __grid_constant__
                     const uint32_t d_tmem = tmem_base + (uint32_t)(is * ACC_COLS + accb * TB);
                     const int kb1 = min(kb0 + CHUNK_KB, p.num_kb);
                     for (int kb = kb0; kb < kb1; ++kb) {
-                        if (!wait_bounded(&a_full[stage], phase, abort_flag, p.status) ||
-                            !wait_bounded(&b_full[stage], phase, abort_flag, p.status)) {
+                        if (!wait_bounded(&ab_full[stage], phase, abort_flag, p.status)) {
                             ok = false;
                             break;
                         }
