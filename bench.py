@@ -83,7 +83,7 @@ def parse():
     ap.add_argument("--cpu-full", action="store_true",
                     help="one GPU step, then the oracle over the whole workload on every host "
                          "core (timed) and every output token compared with it; one JSON line")
-    ap.add_argument("--ffn-path", default="auto", choices=["auto", "large", "small", "large_pair", "fused"],
+    ap.add_argument("--ffn-path", default="auto", choices=["auto", "large", "small", "large_pair"],
                     help="grouped-GEMM kernels of the layer workloads (auto: small-batch "
                          "kernels when T*K <= 32*E)")
     return ap.parse_args()
@@ -492,8 +492,6 @@ class LayerPath:
         w = self.w
         R = self.rows()
         H, N, Nh = w.hidden, w.ffn, w.ffn // 2
-        if "ffn_fused" in prof:
-            return self.roofline_fused(prof, pk)
         small = "gemm1_swiglu_small" in prof
         sfx = "_small" if small else ("_pair" if "gemm1_swiglu_pair" in prof else "")
         g1, g2 = "gemm1_swiglu" + sfx, "gemm2_dequant" + sfx
@@ -535,22 +533,6 @@ class LayerPath:
                     peak_source=pk["source"] + " bf16_tflops_sustained (cuBLAS bf16; the int8 "
                     "products run as exact fp16-image tcgen05 kind::f16 MMAs, whose dense rate "
                     "equals bf16's)"), step_bytes, extra
-
-    def roofline_fused(self, prof, pk):
-        """GMM1, the second quantisation and GMM2 in one kernel: its flops over
-        its duration, against the sustained bf16 peak."""
-        w = self.w
-        R = self.rows()
-        fl = 2.0 * R * w.hidden * w.ffn + 2.0 * R * (w.ffn // 2) * w.hidden
-        n, ms = prof["ffn_fused"]
-        achieved = fl / (ms / n * 1e-3) / 1e12
-        extra = {"ffn_path": "fused", "status": self.B.read_device_status(self.ws)}
-        return dict(bound="tensor", kernel="ffn_fused", achieved=achieved,
-                    peak=pk["bf16_tflops_sustained"], unit="TFLOP/s",
-                    frac=achieved / pk["bf16_tflops_sustained"], traffic=None,
-                    algorithmic_flops=fl,
-                    algorithmic_unit="2*R*H*N + 2*R*(N/2)*H flops per launch",
-                    peak_source=pk["source"] + " bf16_tflops_sustained"), None, extra
 
     def dtype(self):
         return "int8 GEMMs (exact, on fp16 images), fp32 epilogues, bf16 rows"

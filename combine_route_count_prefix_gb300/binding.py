@@ -55,9 +55,9 @@ class MoeShape(ctypes.Structure):
 
 
 # moe_shape.ffn_path: which grouped-GEMM kernels the FFN uses (same results)
-FFN_PATH_AUTO, FFN_PATH_LARGE, FFN_PATH_SMALL, FFN_PATH_LARGE_PAIR, FFN_PATH_FUSED = 0, 1, 2, 3, 4
+FFN_PATH_AUTO, FFN_PATH_LARGE, FFN_PATH_SMALL, FFN_PATH_LARGE_PAIR = 0, 1, 2, 3
 FFN_PATHS = {"auto": FFN_PATH_AUTO, "large": FFN_PATH_LARGE, "small": FFN_PATH_SMALL,
-             "large_pair": FFN_PATH_LARGE_PAIR, "fused": FFN_PATH_FUSED}
+             "large_pair": FFN_PATH_LARGE_PAIR}
 
 
 class StageViews(ctypes.Structure):

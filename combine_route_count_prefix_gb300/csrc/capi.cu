@@ -106,7 +106,7 @@ moe_status check_shape(const moe_shape *s, bool need_ffn) {
         s->num_experts + s->zero_experts + s->copy_experts > INT32_MAX)
         return MOE_ERR_SHAPE;
     if (s->has_shared != 0 && s->has_shared != 1) return MOE_ERR_PARAM_INVALID;
-    if (s->ffn_path < MOE_FFN_PATH_AUTO || s->ffn_path > MOE_FFN_PATH_FUSED || s->reserved != 0)
+    if (s->ffn_path < MOE_FFN_PATH_AUTO || s->ffn_path > MOE_FFN_PATH_LARGE_PAIR || s->reserved != 0)
         return MOE_ERR_PARAM_INVALID;
     const int64_t cap = s->num_tokens * s->topk;
     if (cap > INT32_MAX) return MOE_ERR_SHAPE;
@@ -117,12 +117,6 @@ moe_status check_shape(const moe_shape *s, bool need_ffn) {
         return MOE_ERR_SHAPE;
     }
     return MOE_OK;
-}
-
-// Upper bound on the FFN's 128-row m-blocks: sum over experts of
-// ceil(rows_e / 128) <= T*K / 128 + E.
-static int64_t mblock_flags(const moe_shape &s) {
-    return s.num_tokens * s.topk / kGemmBM + s.num_experts + 1;
 }
 
 Layout layout_for(const moe_shape &s, Op op) {
@@ -154,7 +148,6 @@ Layout layout_for(const moe_shape &s, Op op) {
         L.g = take((size_t)cap * Nh * sizeof(float));
         L.q2 = take((size_t)cap * Nh * 2);
         L.s2 = take((size_t)cap * sizeof(float));
-        L.mflags = take(2 * mblock_flags(s) * sizeof(int32_t));
     }
     if (op == Op::Layer) L.y = take((size_t)cap * H * 2);
     L.total = off;
@@ -386,8 +379,7 @@ static const void *packed_i8(const void *packed, int32_t path, int64_t E, int64_
 
 static bool use_small_path(int32_t path, int64_t rows, int64_t E) {
     if (path == MOE_FFN_PATH_SMALL) return true;
-    if (path == MOE_FFN_PATH_LARGE || path == MOE_FFN_PATH_LARGE_PAIR || path == MOE_FFN_PATH_FUSED)
-        return false;
+    if (path == MOE_FFN_PATH_LARGE || path == MOE_FFN_PATH_LARGE_PAIR) return false;
     return rows <= (int64_t)MOE_FFN_SMALL_ROWS_PER_EXPERT * E;
 }
 
@@ -456,12 +448,6 @@ static moe_status run_ffn_core(const moe_shape &s, const Layout &L, void *ws,
     g2.scale2 = scale2;
     g2.s2 = at<float>(ws, L.s2);
     g2.status = status;
-    if (!small && s.ffn_path == MOE_FFN_PATH_FUSED) {
-        const size_t nflags = (size_t)mblock_flags(s);
-        int32_t *flags = at<int32_t>(ws, L.mflags);
-        return launch_ffn_fused(g1, g2, at<void>(ws, L.q2), at<float>(ws, L.s2), flags,
-                                flags + nflags, nflags * sizeof(int32_t), stream);
-    }
     MOE_TRY(run_gemm(small, s.ffn_path, Epi::SwiGLU, g1, stream));
     MOE_TRY(launch_quant2(at<float>(ws, L.g), offsets, s.num_experts, at<void>(ws, L.q2),
                           at<float>(ws, L.s2), cap, Nh, stream));

@@ -133,7 +133,6 @@ struct Layout {
     size_t q2 = 0;            // fp16 [T*K, N/2] int8 values
     size_t s2 = 0;            // fp32 [T*K]
     size_t y = 0;             // bf16 [T*K, H]
-    size_t mflags = 0;        // int32 [2][m-blocks]: the fused FFN's per-m-block counters
     size_t a_img = 0;         // fp16 images for the plain grouped GEMM
     size_t w_img = 0;
     size_t total = 0;
@@ -312,9 +311,5 @@ moe_status launch_grouped_gemm(Epi epi, const GemmArgs &a, cudaStream_t stream,
 // side, only as many as present.  Kd % 16 == 0 (and Nout % 128 == 0 for the
 // SwiGLU epilogue).
 moe_status launch_grouped_gemm_small(Epi epi, const GemmArgs &a, cudaStream_t stream);
-// GMM1 + SwiGLU, the second quantisation (into q2 / s2) and GMM2 + dequant in
-// one persistent kernel; done1 / ready2: flag_bytes each, zeroed here.
-moe_status launch_ffn_fused(const GemmArgs &g1, const GemmArgs &g2, void *q2, float *s2,
-                           int32_t *done1, int32_t *ready2, size_t flag_bytes, cudaStream_t stream);
 
 }  // namespace moe

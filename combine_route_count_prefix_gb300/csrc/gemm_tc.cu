@@ -32,7 +32,6 @@
 // Every wait is bounded: after about two seconds a wait gives up, sets
 // MOE_DEV_TIMEOUT in the status word and the CTA drains and exits.
 #include "common.cuh"
-#include "quant.cuh"
 #include "tcgen05.cuh"
 
 #include <cuda.h>
@@ -124,24 +123,6 @@ __device__ __forceinline__ void st_global_v8(void *p, uint32_t a, uint32_t b, ui
 struct Tile {
     int e, row0, rows, nb;
 };
-
-// m-block-major order: tile = m-block * n_blocks + column block (the fused
-// FFN counts finished tiles per m-block in this order).
-__device__ __forceinline__ Tile decode_tile(int64_t tile, int n_blocks, int E, const int32_t *s_sched,
-                                            const int32_t *s_off) {
-    Tile t;
-    int mblk = (int)(tile / n_blocks);
-    t.nb = (int)(tile % n_blocks);
-    int lo = 0, hi = E - 1;
-    while (lo < hi) {   // last expert whose first m-block is <= mblk
-        int mid = (lo + hi + 1) >> 1;
-        if (s_sched[mid] <= mblk) lo = mid; else hi = mid - 1;
-    }
-    t.e = lo;
-    t.row0 = s_off[lo] + (mblk - s_sched[lo]) * BM;
-    t.rows = min(BM, s_off[lo + 1] - t.row0);
-    return t;
-}
 
 // Expert-major, then column-block-major order: expert e owns tiles
 // [blk[e] * n_blocks, blk[e + 1] * n_blocks), where blk[e] counts the row
@@ -402,322 +383,6 @@ k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             if (!ok) break;
             if (rloc < t.rows && (int64_t)t.row0 + rloc < p.cap_rows)
                 epilogue_store<EPI>(p, t, t.row0 + rloc, hf, acc);
-        }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
-}
-
-// ---------------------------------------------------------------- fused FFN
-// GMM1 + SwiGLU, the second quantisation and GMM2 + dequant in one persistent
-// kernel ("PTO MegaMoE ...", Overall Architecture: the SwiGLU / dynamic
-// quantisation segments overlap GMM2).  The tile list is every GMM1 tile
-// followed by every GMM2 tile, both m-block-major; CTA b takes tiles b, b + G,
-// ... as in k_grouped_gemm.  Each epilogue warp that has stored its part of
-// a GMM1 tile's g columns counts itself in done1[m-block]; two extra warps per
-// CTA quantise the m-blocks m = b, b + G, ... of CTA b once their count is
-// complete (q2, s2, exactly as k_quant2) and then set ready2[m-block].  A GMM2 tile's loads wait for
-// that flag, so GMM2 starts on the first m-blocks while GMM1's last tiles and
-// their quantisation are still running, and no kernel boundary separates the
-// stages.  Every CTA's GMM1 tiles precede its GMM2 tiles, so every flag is
-// eventually set whatever the scheduling; all CTAs are resident (one per SM,
-// cooperative launch) and every wait is bounded.
-struct FusedDev {
-    GemmDev g1;          // GMM1 with the SwiGLU epilogue
-    GemmDev g2;          // GMM2 with the dequant epilogue (same offsets, schedule, rows)
-    uint2 *q2;           // fp16 images of the second quantisation's codes, [cap, N/2]
-    float *s2;
-    int32_t *done1;      // [m-blocks] GMM1 tiles finished
-    int32_t *ready2;     // [m-blocks] 1 once q2 / s2 of the m-block are written
-    int Nh4;             // N/2 / 4
-};
-
-__device__ __forceinline__ bool wait_flag(const int32_t *flag, volatile int *abort_flag,
-                                          int32_t *status) {
-    const uint64_t t0 = globaltimer();
-    for (;;) {
-        int v;
-        asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
-        if (v != 0) return true;
-        if (*abort_flag) return false;
-        if (globaltimer() - t0 > kTimeoutNs) {
-            *abort_flag = 1;
-            atomicOr(status, MOE_DEV_TIMEOUT);
-            return false;
-        }
-        __nanosleep(256);
-    }
-}
-
-constexpr int Q2_WARPS = 2;                       // quantisation service warps per CTA
-constexpr int FUSED_THREADS = THREADS + 32 * Q2_WARPS;
-
-__device__ __forceinline__ bool wait_count(const int32_t *ctr, int target, volatile int *abort_flag,
-                                           int32_t *status) {
-    const uint64_t t0 = globaltimer();
-    for (;;) {
-        int v;
-        asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
-        if (v >= target) return true;
-        if (*abort_flag) return false;
-        if (globaltimer() - t0 > kTimeoutNs) {
-            *abort_flag = 1;
-            atomicOr(status, MOE_DEV_TIMEOUT);
-            return false;
-        }
-        __nanosleep(512);
-    }
-}
-
-// Row r of g -> its q2 codes and s2 (one warp, the arithmetic of k_quant2).
-// g was written by other CTAs: read through L2.
-__device__ __forceinline__ void quant2_row(const FusedDev &p, int64_t r, int lane) {
-    constexpr int kV = 16;
-    const float4 *src = reinterpret_cast<const float4 *>(p.g1.g) + r * p.Nh4;
-    uint2 *dst = p.q2 + r * p.Nh4;
-    float amax = 0.0f;
-    if (p.Nh4 <= 32 * kV) {
-        float4 v[kV];
-#pragma unroll
-        for (int u = 0; u < kV; ++u) {
-            const int j = lane + 32 * u;
-            v[u] = (j < p.Nh4) ? __ldcg(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int u = 0; u < kV; ++u)
-            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w))));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const float s = __fdiv_rn(amax, 127.0f);
-        const float rs = __frcp_rn(s);
-#pragma unroll
-        for (int u = 0; u < kV; ++u) {
-            const int j = lane + 32 * u;
-            if (j < p.Nh4) {
-                const float a[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-                float c[4];
-                quant_codes<4>(a, s, rs, c);
-                dst[j] = make_uint2(pack_half2(c[0], c[1]), pack_half2(c[2], c[3]));
-            }
-        }
-        if (lane == 0) p.s2[r] = s;
-    } else {
-        for (int j = lane; j < p.Nh4; j += 32) {
-            const float4 v = __ldcg(src + j);
-            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const float s = __fdiv_rn(amax, 127.0f);
-        const float rs = __frcp_rn(s);
-        for (int j = lane; j < p.Nh4; j += 32) {
-            const float4 v = __ldcg(src + j);
-            const float a[4] = {v.x, v.y, v.z, v.w};
-            float c[4];
-            quant_codes<4>(a, s, rs, c);
-            dst[j] = make_uint2(pack_half2(c[0], c[1]), pack_half2(c[2], c[3]));
-        }
-        if (lane == 0) p.s2[r] = s;
-    }
-}
-
-__global__ void __launch_bounds__(FUSED_THREADS, 1)
-k_ffn_fused(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
-            const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
-            FusedDev p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)STAGES * STAGE_BYTES);
-    uint64_t *empty = full + STAGES;
-    uint64_t *acc_full = empty + STAGES;
-    uint64_t *acc_empty = acc_full + 2;
-    uint64_t *drain = acc_empty + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    int32_t *s_sched = reinterpret_cast<int32_t *>(smem + (size_t)STAGES * STAGE_BYTES + kBarrierBytes);
-    int32_t *s_off = s_sched + (kMaxExperts + 1);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const GemmDev &q1 = p.g1;
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], EPI_WARPS);
-        }
-        mbar_init(drain, 1);
-        *abort_flag = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    if (warp == 0 && lane == 0) {
-        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA1) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB1) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA2) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB2) : "memory");
-    }
-    for (int i = threadIdx.x; i <= q1.E; i += blockDim.x) {
-        s_sched[i] = q1.sched[i];
-        s_off[i] = q1.offsets[i];
-    }
-    if (warp == 1) {
-        tmem_alloc(tmem_slot, TMEM_COLS);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
-    const int64_t mblocks = s_sched[q1.E];
-    const int64_t t1 = mblocks * q1.n_blocks;                  // GMM1 tiles
-    const int64_t total_tiles = t1 + mblocks * p.g2.n_blocks;  // then GMM2 tiles
-    // tile -> (stage 1 or 2, its Tile); the GMM2 part counts from t1
-    auto decode = [&](int64_t tile, bool &second) -> Tile {
-        second = tile >= t1;
-        return second ? decode_tile(tile - t1, p.g2.n_blocks, q1.E, s_sched, s_off)
-                      : decode_tile(tile, q1.n_blocks, q1.E, s_sched, s_off);
-    };
-
-    if (warp == 0) {
-        if (lane == 0) {
-            // ------------------------------------------------ TMA producer
-            int stage = 0;
-            uint32_t phase = 0;
-            int issued_phase[STAGES];
-#pragma unroll
-            for (int s = 0; s < STAGES; ++s) issued_phase[s] = -1;
-            bool ok = true;
-            for (int64_t tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-                bool second;
-                const Tile t = decode(tile, second);
-                if (second) {
-                    // the m-block's q2 rows must be complete before they are loaded
-                    const int64_t mb = (tile - t1) / p.g2.n_blocks;
-                    if (!wait_flag(p.ready2 + mb, abort_flag, q1.status)) { ok = false; break; }
-                    asm volatile("fence.proxy.async.global;" ::: "memory");
-                }
-                const CUtensorMap *ma = second ? &tmA2 : &tmA1;
-                const CUtensorMap *mb = second ? &tmB2 : &tmB1;
-                const int nkb = second ? p.g2.num_kb : q1.num_kb;
-                for (int kb = 0; kb < nkb; ++kb) {
-                    if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, q1.status)) { ok = false; break; }
-                    uint8_t *sa = smem + (size_t)stage * STAGE_BYTES;
-                    mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-                    tma_load_2d(sa, ma, &full[stage], kb * BK, t.row0);
-                    tma_load_3d(sa + A_BYTES, mb, &full[stage], kb * BK, t.nb * BN, t.e);
-                    issued_phase[stage] = (int)phase;
-                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-                }
-            }
-            for (int s = 0; s < STAGES; ++s)
-                if (issued_phase[s] >= 0)
-                    wait_bounded(&full[s], (uint32_t)issued_phase[s], abort_flag, q1.status, false);
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------ MMA issuer
-            constexpr uint32_t idesc = idesc_f16(BM, BN);
-            int stage = 0;
-            uint32_t phase = 0;
-            int accb = 0;
-            uint32_t acc_phase = 0;
-            bool ok = true;
-            for (int64_t tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-                const int nkb = tile >= t1 ? p.g2.num_kb : q1.num_kb;
-                for (int kb0 = 0; ok && kb0 < nkb; kb0 += CHUNK_KB) {
-                    if (!wait_bounded(&acc_empty[accb], acc_phase ^ 1u, abort_flag, q1.status)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + (uint32_t)(accb * BN);
-                    const int kb1 = min(kb0 + CHUNK_KB, nkb);
-                    for (int kb = kb0; kb < kb1; ++kb) {
-                        if (!wait_bounded(&full[stage], phase, abort_flag, q1.status)) { ok = false; break; }
-                        tc_fence_after();
-                        const uint32_t a_addr = smem_u32(smem + (size_t)stage * STAGE_BYTES);
-                        const uint32_t b_addr = a_addr + A_BYTES;
-#pragma unroll
-                        for (int k = 0; k < BK / 16; ++k)
-                            mma_f16(d_tmem, desc_k(a_addr + 32 * k), desc_k(b_addr + 32 * k),
-                                    idesc, (kb > kb0 || k > 0) ? 1u : 0u);
-                        mma_commit(&empty[stage]);
-                        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-                    }
-                    if (!ok) break;
-                    mma_commit(&acc_full[accb]);
-                    if (++accb == 2) { accb = 0; acc_phase ^= 1u; }
-                }
-            }
-            mma_commit(drain);
-            wait_bounded(drain, 0, abort_flag, q1.status, false);
-        }
-    } else if (warp < 2 + EPI_WARPS) {
-        // ---------------------------------------------------- epilogue warps
-        const int q = warp & 3;
-        const int hf = (warp - 2) >> 2;
-        const int rloc = q * 32 + lane;
-        int accb = 0;
-        uint32_t acc_phase = 0;
-        for (int64_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-            bool second;
-            const Tile t = decode(tile, second);
-            const int nchunks = ((second ? p.g2.num_kb : q1.num_kb) + CHUNK_KB - 1) / CHUNK_KB;
-            int32_t acc[128];
-            bool ok = true;
-            for (int c = 0; c < nchunks; ++c) {
-                bool w = wait_bounded(&acc_full[accb], acc_phase, abort_flag, q1.status);
-                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) +
-                                       (uint32_t)(accb * BN + hf * 128);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint32_t r[32];
-                    tmem_ld32(taddr + 32 * j, r);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int v = __float2int_rn(__uint_as_float(r[i]));
-                        acc[32 * j + i] = (c == 0) ? v : acc[32 * j + i] + v;
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&acc_empty[accb]);
-                if (++accb == 2) { accb = 0; acc_phase ^= 1u; }
-            }
-            if (!ok) break;
-            const bool mine = rloc < t.rows && (int64_t)t.row0 + rloc < q1.cap_rows;
-            if (second) {
-                if (mine) epilogue_store<(int)Epi::DequantBF16>(p.g2, t, t.row0 + rloc, hf, acc);
-                continue;
-            }
-            if (mine) epilogue_store<(int)Epi::SwiGLU>(q1, t, t.row0 + rloc, hf, acc);
-            // count this warp's part of the tile in its m-block
-            __threadfence();   // this thread's g columns, before the count
-            __syncwarp();
-            if (lane == 0) atomicAdd(p.done1 + tile / q1.n_blocks, 1);
-        }
-    } else {
-        // ---------------------------------------------------- quantisation service
-        const int sw = warp - 2 - EPI_WARPS;   // 0 .. Q2_WARPS - 1
-        for (int64_t mb = blockIdx.x; mb < mblocks; mb += gridDim.x) {
-            // the m-block's GMM1 tiles, each counted by its 8 epilogue warps
-            bool w = true;
-            if (lane == 0) w = wait_count(p.done1 + mb, EPI_WARPS * q1.n_blocks, abort_flag, q1.status);
-            if (!__shfl_sync(0xffffffffu, w, 0)) break;
-            __threadfence();
-            const Tile t = decode_tile(mb * q1.n_blocks, q1.n_blocks, q1.E, s_sched, s_off);
-            for (int r = sw; r < t.rows; r += Q2_WARPS)
-                if ((int64_t)t.row0 + r < q1.cap_rows) quant2_row(p, (int64_t)t.row0 + r, lane);
-            __threadfence();   // this thread's q2 / s2, before the flag
-            asm volatile("bar.sync 2, %0;" ::"n"(32 * Q2_WARPS) : "memory");
-            if (sw == 0 && lane == 0)
-                asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p.ready2 + mb), "r"(1) : "memory");
         }
     }
 
@@ -1089,58 +754,6 @@ moe_status launch_pair_or_single(const GemmArgs &a, cudaStream_t stream, bool pa
     const GemmDev d = gemm_dev(a);
     if (clusters > 0) return launch_epi_pair<EPI>(ma, mb, d, clusters, stream);
     return launch_epi<EPI>(ma, mb, d, stream);
-}
-
-moe_status launch_ffn_fused(const GemmArgs &g1, const GemmArgs &g2, void *q2, float *s2,
-                           int32_t *done1, int32_t *ready2, size_t flag_bytes, cudaStream_t stream) {
-    if (g1.cap_rows <= 0 || g1.E <= 0) return MOE_OK;
-    CUtensorMap ma1, mb1, ma2, mb2;
-    const uint32_t abox[2] = {BK, BM};
-    const uint32_t bbox[3] = {BK, BN, 1};
-    const uint64_t a1dims[2] = {(uint64_t)g1.Kd, (uint64_t)g1.cap_rows};
-    const uint64_t a1str[1] = {(uint64_t)g1.Kd * 2};
-    const uint64_t b1dims[3] = {(uint64_t)g1.Kd, (uint64_t)g1.Nout, (uint64_t)g1.E};
-    const uint64_t b1str[2] = {(uint64_t)g1.Kd * 2, (uint64_t)g1.Kd * g1.Nout * 2};
-    const uint64_t a2dims[2] = {(uint64_t)g2.Kd, (uint64_t)g2.cap_rows};
-    const uint64_t a2str[1] = {(uint64_t)g2.Kd * 2};
-    const uint64_t b2dims[3] = {(uint64_t)g2.Kd, (uint64_t)g2.Nout, (uint64_t)g2.E};
-    const uint64_t b2str[2] = {(uint64_t)g2.Kd * 2, (uint64_t)g2.Kd * g2.Nout * 2};
-    const auto f16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    const auto sw = kTileSwizzle;
-    if (!make_tensor_map(&ma1, f16, sw, g1.a_img, 2, a1dims, a1str, abox) ||
-        !make_tensor_map(&mb1, f16, sw, g1.b_img, 3, b1dims, b1str, bbox) ||
-        !make_tensor_map(&ma2, f16, sw, g2.a_img, 2, a2dims, a2str, abox) ||
-        !make_tensor_map(&mb2, f16, sw, g2.b_img, 3, b2dims, b2str, bbox))
-        return MOE_ERR_CUDA;
-    FusedDev d;
-    d.g1 = gemm_dev(g1);
-    d.g2 = gemm_dev(g2);
-    d.q2 = static_cast<uint2 *>(q2);
-    d.s2 = s2;
-    d.done1 = done1;
-    d.ready2 = ready2;
-    d.Nh4 = (int)(g2.Kd / 4);
-    if (!set_smem_limit((const void *)k_ffn_fused, SMEM_BYTES)) return MOE_ERR_CUDA;
-    if (cudaMemsetAsync(done1, 0, flag_bytes, stream) != cudaSuccess ||
-        cudaMemsetAsync(ready2, 0, flag_bytes, stream) != cudaSuccess)
-        return MOE_ERR_CUDA;
-    // one CTA per SM, all resident at once: the GMM2 tiles wait on flags that
-    // other CTAs set
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)num_sms());
-    cfg.blockDim = dim3(FUSED_THREADS);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const int tok = launch_begin("ffn_fused", stream, cfg.gridDim.x);
-    cudaError_t err = cudaLaunchKernelEx(&cfg, k_ffn_fused, ma1, mb1, ma2, mb2, d);
-    if (err == cudaSuccess) err = cudaGetLastError();
-    launch_end(tok, stream);
-    return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 moe_status launch_grouped_gemm(Epi epi, const GemmArgs &a, cudaStream_t stream, bool pair) {

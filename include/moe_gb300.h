@@ -106,11 +106,6 @@ typedef struct moe_shape {
  *          of the rows and half of the weight channels, so a k-step moves a
  *          third less data per SM than LARGE).  Falls back to LARGE's kernel
  *          where no pair cluster fits.
- *   FUSED: LARGE's tiles with GMM1, the second quantisation and GMM2 in one
- *          persistent kernel; GMM2 starts on an m-block as soon as its rows
- *          are quantised ("PTO MegaMoE ...", the quantisation overlapping GMM2).
- *          Same results; measured slightly slower than LARGE, kept as an
- *          option.
  *   SMALL: the weights read as int8 (half the bytes), widened on chip into
  *          tensor memory as the MMA's 128-row side, against the expert's rows
  *          (only those present); for few rows per expert, where reading the
@@ -124,7 +119,7 @@ typedef struct moe_shape {
 #define MOE_FFN_PATH_LARGE 1
 #define MOE_FFN_PATH_SMALL 2
 #define MOE_FFN_PATH_LARGE_PAIR 3
-#define MOE_FFN_PATH_FUSED 4
+/* Any other ffn_path value returns MOE_ERR_PARAM_INVALID. */
 #define MOE_FFN_SMALL_ROWS_PER_EXPERT 32
 
 /* ------------------------------------------------------------------------
@@ -214,7 +209,7 @@ moe_status moe_combine(const moe_shape *shape, const void *expand_x, const int32
  *   w1 int8 [E, N, H]   (row n = GMM1 output channel n, H contiguous)
  *   w2 int8 [E, H, N/2] (row c = GMM2 output channel c, N/2 contiguous)
  * Packing, done once per model, writes the operand format(s) of shape->ffn_path:
- *   LARGE, LARGE_PAIR, FUSED: fp16 images of the int8 values (exact), 2 bytes
+ *   LARGE, LARGE_PAIR: fp16 images of the int8 values (exact), 2 bytes
  *          per weight (E*N*H*2 and E*H*(N/2)*2 bytes);
  *   SMALL: the values as bytes biased by +128, 1 byte per weight;
  *   AUTO:  both, the bytes after the images, 3 bytes per weight.

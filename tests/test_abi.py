@@ -48,7 +48,7 @@ def test_workspace_sizes_and_shape_checks(B):
     a, b = B.packed_weight_bytes(s)
     # AUTO: fp16 images for the large-tile GEMMs + biased bytes for the small-batch GEMM
     assert a == 128 * 4096 * 7168 * 3 and b == 128 * 7168 * 2048 * 3
-    for path, per in (("large", 2), ("large_pair", 2), ("fused", 2), ("small", 1)):
+    for path, per in (("large", 2), ("large_pair", 2), ("small", 1)):
         sp = B.make_shape(16384, 8, 7168, 128, 8, 4096, ffn_path=path)
         assert B.packed_weight_bytes(sp) == (128 * 4096 * 7168 * per, 128 * 7168 * 2048 * per)
     # the large prefill workload's weights on the large-tile path: 2 bytes per weight
@@ -61,7 +61,7 @@ def test_workspace_sizes_and_shape_checks(B):
                 B.make_shape(16, 2, 128, 8, 2, 300),   # N % 256
                 B.make_shape(16, 2, 128, 8, 2, 256, ffn_path="large")]:
         if bad.ffn_path:
-            bad.ffn_path = 5                           # no such kernel choice
+            bad.ffn_path = 4                           # no such kernel choice
         with pytest.raises(B.MoeError):
             B.layer_workspace_size(bad) if bad.ffn else B.dispatch_workspace_size(bad)
 

@@ -9,8 +9,7 @@ Bars (the oracle computes each stage from its own inputs only):
   out: max 2 bf16 ulp and rel-L2 <= 1e-3.
 Each check runs on every grouped-GEMM kernel ("large": fp16 weight images in
 128 x 256 tiles, one SM each; "large_pair": 256 x 256 tiles on SM pairs;
-"small": int8 weights widened on chip; "fused": large tiles with GMM1, the
-second quantisation and GMM2 in one kernel), and they must agree bit for bit.
+"small": int8 weights widened on chip), and they must agree bit for bit.
 """
 import numpy as np
 import pytest
@@ -33,7 +32,7 @@ def _device_weights(B, shape, W1, W2):
     return B.pack_weights(shape, dev(W1), dev(W2))
 
 
-PATHS = ["large", "large_pair", "small", "fused"]
+PATHS = ["large", "large_pair", "small"]
 
 
 def _stage_check(B, w, seed, path="auto"):
@@ -150,7 +149,7 @@ def test_layer_paths_agree_bit_for_bit(B):
 
 def test_grouped_ffn_entry_on_dispatched_rows(B):
     """moe_grouped_ffn on the bf16 rows of moe_dispatch gives the same y as the
-    fused layer (quantising each dispatched copy equals quantising the token)."""
+    whole-layer call (quantising each dispatched copy equals quantising the token)."""
     w = wl.custom(P=2, M=96, H=256, E=6, K=3, N=512)
     T, P, H, E, K, N = (w.num_tokens, w.num_partitions, w.hidden, w.num_experts, w.topk, w.ffn)
     inp = wl.make_inputs(w, seed=4)
