@@ -142,17 +142,18 @@ k_quant_bf16_rows(RouteDev ra, const uint4 *__restrict__ src, int32_t *__restric
     const int64_t n_items = kFromRouteTable ? T : min((int64_t)offsets[E], T);
     for (int64_t it = blockIdx.x; it < n_items; it += gridDim.x) {
         __syncthreads();
-        if (threadIdx.x == 0) {
-            int n = 0;
-            if (kFromRouteTable) {
-                for (int k = 0; k < K; ++k) {
-                    int32_t r = resolve_route_row(ra, it, k, route_row, assist);
-                    if (r >= 0) rows[n++] = r;
-                }
-            } else {
-                rows[n++] = (int32_t)it;
+        if (kFromRouteTable) {
+            // lane k resolves slot k; the active rows are packed in slot order
+            if (threadIdx.x < 32) {
+                const int k = threadIdx.x;
+                const int32_t r = k < K ? resolve_route_row(ra, it, k, route_row, assist) : -1;
+                const uint32_t act = __ballot_sync(kFull, r >= 0);
+                if (r >= 0) rows[__popc(act & lanemask_lt())] = r;
+                if (k == 0) nrows = __popc(act);
             }
-            nrows = n;
+        } else if (threadIdx.x == 0) {
+            rows[0] = (int32_t)it;
+            nrows = 1;
         }
         __syncthreads();
         const int n = nrows;
