@@ -78,3 +78,19 @@ def test_workload_config_names_the_workload():
     c = bench.workload_config(w)
     assert c["workload"] == "decode_dispatch_combine" and c["tokens"] == 2048
     assert c["mask"] == "per-token" and c["shared_expert"] is True
+
+
+def test_bf16_errors_in_ulps_of_the_reference():
+    # bf16 spacing at 1.0 is 2^-7 and at 100 it is 0.5; a one-step change in the
+    # last bit is one ulp, and the counts are per token (row)
+    ref = wl.f32_to_bf16_bits(np.array([[1.0, -3.0, 100.0], [0.25, 7.0, -0.5]], np.float32))
+    got = ref.copy()
+    got[0, 2] += 2                                   # 100 -> 101: two ulps
+    e = bench.bf16_errors(got, ref)
+    assert e["tokens"] == 2 and e["max_ulp"] == 2.0
+    assert e["tokens_within_2_ulp"] == 2 and e["tokens_bit_exact"] == 1
+    got[1, 1] += 3                                   # three ulps at 7.0
+    e = bench.bf16_errors(got, ref)
+    assert e["max_ulp"] == 3.0 and e["tokens_within_2_ulp"] == 1 and e["tokens_bit_exact"] == 0
+    assert bench.bf16_errors(ref, ref) == {"tokens": 2, "max_ulp": 0.0, "rel_l2": 0.0,
+                                           "tokens_within_2_ulp": 2, "tokens_bit_exact": 2}
