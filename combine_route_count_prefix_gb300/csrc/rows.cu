@@ -38,11 +38,6 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 &v, float (&f)[8]) {
     }
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    __nv_bfloat16 a = __float2bfloat16_rn(lo), b = __float2bfloat16_rn(hi);
-    return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
-}
-
 
 __device__ __forceinline__ float block_max(float v, float *scratch /*[32]*/) {
 #pragma unroll
