@@ -176,3 +176,20 @@ def test_noalloc_dispatch_alignment_checks_before_launch(B):
     rc = L.moe_dispatch_noalloc(ctypes.byref(big), A, ODD8, None, A2, ODD8, A, ODD8, ODD8,
                                 ODD8, None)
     assert rc == 561007
+
+
+def test_missing_library_fails_loudly():
+    """No CPU fallback: without the CUDA library every call raises."""
+    import subprocess
+    import sys
+    code = (
+        "import sys; sys.path.insert(0, %r)\n"
+        "from combine_route_count_prefix_gb300 import binding as B\n"
+        "B.LIB_PATH = '/nonexistent/libmoe_gb300.so'\n"
+        "try:\n"
+        "    B.make_shape(16, 2, 128, 8, 2); B.dispatch_workspace_size(B.make_shape(16, 2, 128, 8, 2))\n"
+        "except RuntimeError as e:\n"
+        "    print('raised', 'missing' in str(e)); sys.exit(0)\n"
+        "print('no error'); sys.exit(1)\n" % ROOT)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True)
+    assert r.returncode == 0 and "raised True" in r.stdout, (r.stdout, r.stderr)
