@@ -299,9 +299,9 @@ moe_status moe_stage_views_get(const moe_shape *shape, int for_layer, void *work
  * rows r in [offsets[e], offsets[e+1]).
  *   A int8 [rows, Kd]; W int8 [E, N, Kd]; C int32 [rows, N]; rows >= offsets[E].
  *   N % 8 == 0, Kd % 8 == 0 (Kd % 16 == 0 for the SMALL kernel).
- * path: MOE_FFN_PATH_* (AUTO: SMALL when rows <= 32 * E and Kd % 16 == 0, else LARGE).
- * A is first converted into fp16 images in the workspace, and W into fp16
- * images (LARGE) or biased bytes (SMALL).
+ * path: MOE_FFN_PATH_* (AUTO: SMALL when rows <= 32 * E and Kd % 16 == 0, else
+ * LARGE_PAIR).  A is first converted into fp16 images in the workspace, and W
+ * into fp16 images (LARGE, LARGE_PAIR) or biased bytes (SMALL).
  * ------------------------------------------------------------------------ */
 moe_status moe_grouped_gemm_s32_workspace_size(int64_t rows, int64_t E, int64_t N, int64_t Kd,
                                                size_t *bytes);
@@ -368,8 +368,9 @@ moe_status moe_wait_selftest(void *workspace, size_t workspace_bytes, uint64_t l
  * process so far.
  * moe_profile_enable(1) makes every later launch record a CUDA event pair
  * on its own stream; moe_profile_report (after the streams are synchronised)
- * writes one line per kernel name: "name launches total_ms" into buf and
- * clears the records.  moe_profile_enable(0) stops recording.
+ * writes one line per kernel name: "name launches total_ms grid" (grid: the
+ * CTAs of its last launch) into buf and clears the records.
+ * moe_profile_enable(0) stops recording.
  * ------------------------------------------------------------------------ */
 uint64_t moe_launch_count(void);
 moe_status moe_profile_enable(int on);
