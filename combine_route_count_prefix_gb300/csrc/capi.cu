@@ -9,6 +9,7 @@
 #include <vector>
 #include <map>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 
 namespace moe {
@@ -39,8 +40,22 @@ cudaEvent_t take_event() {
 }
 }  // namespace
 
+int log_level() {
+    static const int level = [] {
+        const char *e = getenv("MOE_LOG");
+        return e ? atoi(e) : 0;
+    }();
+    return level;
+}
+
+moe_status log_failure(const char *where, moe_status s) {
+    if (log_level() > 0) fprintf(stderr, "moe: %s: %s (%d)\n", where, moe_status_string(s), (int)s);
+    return s;
+}
+
 int launch_begin(const char *name, cudaStream_t stream, unsigned grid) {
     g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (log_level() >= 2) fprintf(stderr, "moe: launch %s, %u CTAs\n", name, grid);
     if (!g_profile.load(std::memory_order_relaxed)) return -1;
     std::lock_guard<std::mutex> lk(g_prof_mu);
     ProfRecord r{name, take_event(), take_event(), grid};
@@ -95,26 +110,26 @@ int64_t route_chunks(const moe_shape &s) {
 }
 
 moe_status check_shape(const moe_shape *s, bool need_ffn) {
-    if (!s) return MOE_ERR_NULLPTR;
+    if (!s) return MOE_FAIL(MOE_ERR_NULLPTR);
     if (s->num_tokens < 0 || s->num_partitions < 1 || s->num_tokens % s->num_partitions != 0)
-        return MOE_ERR_SHAPE;
-    if (s->hidden < 8 || s->hidden % 8 != 0) return MOE_ERR_SHAPE;
-    if (s->num_experts < 1 || s->num_experts > kMaxExperts) return MOE_ERR_SHAPE;
-    if (s->topk < 1 || s->topk > kMaxTopK) return MOE_ERR_SHAPE;
-    if (s->mask_kind < 0 || s->mask_kind > 2) return MOE_ERR_PARAM_INVALID;
+        return MOE_FAIL(MOE_ERR_SHAPE);
+    if (s->hidden < 8 || s->hidden % 8 != 0) return MOE_FAIL(MOE_ERR_SHAPE);
+    if (s->num_experts < 1 || s->num_experts > kMaxExperts) return MOE_FAIL(MOE_ERR_SHAPE);
+    if (s->topk < 1 || s->topk > kMaxTopK) return MOE_FAIL(MOE_ERR_SHAPE);
+    if (s->mask_kind < 0 || s->mask_kind > 2) return MOE_FAIL(MOE_ERR_PARAM_INVALID);
     if (s->zero_experts < 0 || s->copy_experts < 0 ||
         s->num_experts + s->zero_experts + s->copy_experts > INT32_MAX)
-        return MOE_ERR_SHAPE;
-    if (s->has_shared != 0 && s->has_shared != 1) return MOE_ERR_PARAM_INVALID;
+        return MOE_FAIL(MOE_ERR_SHAPE);
+    if (s->has_shared != 0 && s->has_shared != 1) return MOE_FAIL(MOE_ERR_PARAM_INVALID);
     if (s->ffn_path < MOE_FFN_PATH_AUTO || s->ffn_path > MOE_FFN_PATH_LARGE_PAIR || s->reserved != 0)
-        return MOE_ERR_PARAM_INVALID;
+        return MOE_FAIL(MOE_ERR_PARAM_INVALID);
     const int64_t cap = s->num_tokens * s->topk;
-    if (cap > INT32_MAX) return MOE_ERR_SHAPE;
+    if (cap > INT32_MAX) return MOE_FAIL(MOE_ERR_SHAPE);
     if (need_ffn) {
-        if (s->ffn <= 0 || s->ffn % 256 != 0 || s->ffn > 8192) return MOE_ERR_SHAPE;
-        if (s->hidden % 16 != 0 || s->hidden > 8192) return MOE_ERR_SHAPE;
+        if (s->ffn <= 0 || s->ffn % 256 != 0 || s->ffn > 8192) return MOE_FAIL(MOE_ERR_SHAPE);
+        if (s->hidden % 16 != 0 || s->hidden > 8192) return MOE_FAIL(MOE_ERR_SHAPE);
     } else if (s->ffn < 0) {
-        return MOE_ERR_SHAPE;
+        return MOE_FAIL(MOE_ERR_SHAPE);
     }
     return MOE_OK;
 }
@@ -215,7 +230,7 @@ moe_status moe_profile_enable(int on) {
 }
 
 moe_status moe_profile_report(char *buf, size_t bytes) {
-    if (!buf || bytes == 0) return MOE_ERR_NULLPTR;
+    if (!buf || bytes == 0) return MOE_FAIL(MOE_ERR_NULLPTR);
     std::lock_guard<std::mutex> lk(g_prof_mu);
     std::map<std::string, std::pair<int, double>> agg;
     std::map<std::string, unsigned> grid;
@@ -243,19 +258,20 @@ moe_status moe_profile_report(char *buf, size_t bytes) {
         snprintf(line, sizeof line, "%s %d %.6f %u\n", n.c_str(), agg[n].first, agg[n].second, grid[n]);
         out += line;
     }
-    if (out.size() + 1 > bytes) return MOE_ERR_PARAM_INVALID;
+    if (out.size() + 1 > bytes) return MOE_FAIL(MOE_ERR_PARAM_INVALID);
     memcpy(buf, out.c_str(), out.size() + 1);
     return MOE_OK;
 }
 
 moe_status moe_read_device_status(void *workspace, cudaStream_t stream, int32_t *status_host) {
-    if (!workspace || !status_host) return MOE_ERR_NULLPTR;
+    if (!workspace || !status_host) return MOE_FAIL(MOE_ERR_NULLPTR);
     int32_t v = 0;
     if (cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
-        return MOE_ERR_CUDA;
-    if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
-    if (cudaMemsetAsync(workspace, 0, sizeof v, stream) != cudaSuccess) return MOE_ERR_CUDA;
-    if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+        return MOE_FAIL(MOE_ERR_CUDA);
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_FAIL(MOE_ERR_CUDA);
+    if (cudaMemsetAsync(workspace, 0, sizeof v, stream) != cudaSuccess) return MOE_FAIL(MOE_ERR_CUDA);
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_FAIL(MOE_ERR_CUDA);
+    if (v != 0 && log_level() > 0) fprintf(stderr, "moe: device status word 0x%x\n", (unsigned)v);
     *status_host = v;
     return MOE_OK;
 }
@@ -263,7 +279,7 @@ moe_status moe_read_device_status(void *workspace, cudaStream_t stream, int32_t 
 // ---------------------------------------------------------------- dispatch
 moe_status moe_dispatch_workspace_size(const moe_shape *shape, size_t *bytes) {
     MOE_TRY(check_shape(shape, false));
-    if (!bytes) return MOE_ERR_NULLPTR;
+    if (!bytes) return MOE_FAIL(MOE_ERR_NULLPTR);
     *bytes = layout_for(*shape, Op::Dispatch).total;
     return MOE_OK;
 }
@@ -278,18 +294,18 @@ moe_status moe_dispatch(const moe_shape *shape, const void *x, const int32_t *ex
     // with T == 0 the per-token and per-route arrays are empty and may be NULL
     const bool empty = s.num_tokens == 0;
     if (!expert_token_nums || !expert_offsets || !ep_recv_counts || !workspace)
-        return MOE_ERR_NULLPTR;
-    if (!empty && (!expert_ids || !assist || !route_row)) return MOE_ERR_NULLPTR;
-    if (!empty && expand_x && !x) return MOE_ERR_NULLPTR;
-    if (!empty && s.mask_kind != 0 && !x_active_mask) return MOE_ERR_NULLPTR;
-    if (s.mask_kind == 0 && x_active_mask) return MOE_ERR_PARAM_INVALID;
+        return MOE_FAIL(MOE_ERR_NULLPTR);
+    if (!empty && (!expert_ids || !assist || !route_row)) return MOE_FAIL(MOE_ERR_NULLPTR);
+    if (!empty && expand_x && !x) return MOE_FAIL(MOE_ERR_NULLPTR);
+    if (!empty && s.mask_kind != 0 && !x_active_mask) return MOE_FAIL(MOE_ERR_NULLPTR);
+    if (s.mask_kind == 0 && x_active_mask) return MOE_FAIL(MOE_ERR_PARAM_INVALID);
     if ((expand_x && (!aligned(x, 16) || !aligned(expand_x, 16))) || !aligned(workspace, kAlign))
-        return MOE_ERR_ALIGNMENT;
+        return MOE_FAIL(MOE_ERR_ALIGNMENT);
     if (!aligned(expert_ids, 4) || !aligned(assist, 4) || !aligned(expert_token_nums, 8) ||
         !aligned(expert_offsets, 4) || !aligned(ep_recv_counts, 4) || !aligned(route_row, 4))
-        return MOE_ERR_ALIGNMENT;
+        return MOE_FAIL(MOE_ERR_ALIGNMENT);
     const Layout L = layout_for(s, Op::Dispatch);
-    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+    if (workspace_bytes < L.total) return MOE_FAIL(MOE_ERR_WORKSPACE);
     RouteDev r = route_dev(s, expert_ids, x_active_mask, workspace, L);
     MOE_TRY(launch_route_fused(r, route_chunks(s), expert_token_nums, expert_offsets,
                                ep_recv_counts, nullptr, route_row, stream));
@@ -306,17 +322,17 @@ moe_status moe_dispatch_quant(const moe_shape *shape, const void *x, const int32
     MOE_TRY(check_shape(shape, false));
     const moe_shape &s = *shape;
     const bool empty = s.num_tokens == 0;
-    if (s.hidden > 8192) return MOE_ERR_SHAPE;
-    if (!expert_token_nums || !expert_offsets || !ep_recv_counts || !workspace) return MOE_ERR_NULLPTR;
+    if (s.hidden > 8192) return MOE_FAIL(MOE_ERR_SHAPE);
+    if (!expert_token_nums || !expert_offsets || !ep_recv_counts || !workspace) return MOE_FAIL(MOE_ERR_NULLPTR);
     if (!empty && (!x || !expert_ids || !assist || !route_row || !expand_x || !dynamic_scales))
-        return MOE_ERR_NULLPTR;
-    if (!empty && s.mask_kind != 0 && !x_active_mask) return MOE_ERR_NULLPTR;
-    if (s.mask_kind == 0 && x_active_mask) return MOE_ERR_PARAM_INVALID;
+        return MOE_FAIL(MOE_ERR_NULLPTR);
+    if (!empty && s.mask_kind != 0 && !x_active_mask) return MOE_FAIL(MOE_ERR_NULLPTR);
+    if (s.mask_kind == 0 && x_active_mask) return MOE_FAIL(MOE_ERR_PARAM_INVALID);
     if (!aligned(x, 16) || !aligned(expand_x, 16) || !aligned(smooth_scales, 16) ||
         !aligned(workspace, kAlign) || !aligned(dynamic_scales, 4))
-        return MOE_ERR_ALIGNMENT;
+        return MOE_FAIL(MOE_ERR_ALIGNMENT);
     const Layout L = layout_for(s, Op::Dispatch);
-    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+    if (workspace_bytes < L.total) return MOE_FAIL(MOE_ERR_WORKSPACE);
     RouteDev r = route_dev(s, expert_ids, x_active_mask, workspace, L);
     MOE_TRY(launch_route_fused(r, route_chunks(s), expert_token_nums, expert_offsets,
                                ep_recv_counts, nullptr, route_row, stream));
@@ -332,17 +348,17 @@ moe_status moe_combine(const moe_shape *shape, const void *expand_x, const int32
     MOE_TRY(check_shape(shape, false));
     const moe_shape &s = *shape;
     if (s.num_tokens == 0) return MOE_OK;
-    if (!expand_x || !route_row || !expert_scales || !x_out) return MOE_ERR_NULLPTR;
-    if (s.copy_experts > 0 && !ori_x) return MOE_ERR_NULLPTR;
-    if (ori_x && !aligned(ori_x, 16)) return MOE_ERR_ALIGNMENT;
-    if (s.has_shared && !shared_expert_x) return MOE_ERR_NULLPTR;
-    if (!s.has_shared && shared_expert_x) return MOE_ERR_PARAM_INVALID;
-    if (s.mask_kind != 0 && !x_active_mask) return MOE_ERR_NULLPTR;
-    if (s.mask_kind == 0 && x_active_mask) return MOE_ERR_PARAM_INVALID;
+    if (!expand_x || !route_row || !expert_scales || !x_out) return MOE_FAIL(MOE_ERR_NULLPTR);
+    if (s.copy_experts > 0 && !ori_x) return MOE_FAIL(MOE_ERR_NULLPTR);
+    if (ori_x && !aligned(ori_x, 16)) return MOE_FAIL(MOE_ERR_ALIGNMENT);
+    if (s.has_shared && !shared_expert_x) return MOE_FAIL(MOE_ERR_NULLPTR);
+    if (!s.has_shared && shared_expert_x) return MOE_FAIL(MOE_ERR_PARAM_INVALID);
+    if (s.mask_kind != 0 && !x_active_mask) return MOE_FAIL(MOE_ERR_NULLPTR);
+    if (s.mask_kind == 0 && x_active_mask) return MOE_FAIL(MOE_ERR_PARAM_INVALID);
     if (!aligned(expand_x, 16) || !aligned(x_out, 16) ||
         (shared_expert_x && !aligned(shared_expert_x, 16)) || !aligned(route_row, 4) ||
         !aligned(expert_scales, 4))
-        return MOE_ERR_ALIGNMENT;
+        return MOE_FAIL(MOE_ERR_ALIGNMENT);
     return launch_combine(expand_x, route_row, expert_scales, x_active_mask, s.mask_kind,
                           shared_expert_x, s.copy_experts > 0 ? ori_x : nullptr,
                           s.zero_experts + s.copy_experts > 0, x_out, s.num_tokens, s.topk,
@@ -361,7 +377,7 @@ static bool packs_i8(int32_t path) {
 
 moe_status moe_packed_weight_bytes(const moe_shape *shape, size_t *w1_bytes, size_t *w2_bytes) {
     MOE_TRY(check_shape(shape, true));
-    if (!w1_bytes || !w2_bytes) return MOE_ERR_NULLPTR;
+    if (!w1_bytes || !w2_bytes) return MOE_FAIL(MOE_ERR_NULLPTR);
     const moe_shape &s = *shape;
     const size_t per = (packs_f16(s.ffn_path) ? 2 : 0) + (packs_i8(s.ffn_path) ? 1 : 0);
     *w1_bytes = (size_t)s.num_experts * s.ffn * s.hidden * per;
@@ -395,10 +411,10 @@ moe_status moe_pack_weights(const moe_shape *shape, const int8_t *w1, const int8
                             void *w1_packed, void *w2_packed, cudaStream_t stream) {
     MOE_TRY(check_shape(shape, true));
     const moe_shape &s = *shape;
-    if (!w1 || !w2 || !w1_packed || !w2_packed) return MOE_ERR_NULLPTR;
+    if (!w1 || !w2 || !w1_packed || !w2_packed) return MOE_FAIL(MOE_ERR_NULLPTR);
     if (!aligned(w1, 16) || !aligned(w2, 16) || !aligned(w1_packed, kAlign) ||
         !aligned(w2_packed, kAlign))
-        return MOE_ERR_ALIGNMENT;
+        return MOE_FAIL(MOE_ERR_ALIGNMENT);
     const int64_t E = s.num_experts, N = s.ffn, H = s.hidden, Nh = s.ffn / 2;
     const int32_t path = s.ffn_path;
     if (packs_f16(path)) {
@@ -456,7 +472,7 @@ static moe_status run_ffn_core(const moe_shape &s, const Layout &L, void *ws,
 
 moe_status moe_grouped_ffn_workspace_size(const moe_shape *shape, size_t *bytes) {
     MOE_TRY(check_shape(shape, true));
-    if (!bytes) return MOE_ERR_NULLPTR;
+    if (!bytes) return MOE_FAIL(MOE_ERR_NULLPTR);
     *bytes = layout_for(*shape, Op::Ffn).total;
     return MOE_OK;
 }
@@ -471,13 +487,13 @@ moe_status moe_grouped_ffn(const moe_shape *shape, const void *expand_x,
     // with T == 0 the per-row arrays are empty and may be NULL
     const bool empty = s.num_tokens == 0;
     if (!expert_offsets || !w1_packed || !scale1 || !w2_packed || !scale2 || !workspace)
-        return MOE_ERR_NULLPTR;
-    if (!empty && (!expand_x || !y)) return MOE_ERR_NULLPTR;
+        return MOE_FAIL(MOE_ERR_NULLPTR);
+    if (!empty && (!expand_x || !y)) return MOE_FAIL(MOE_ERR_NULLPTR);
     if (!aligned(expand_x, 16) || !aligned(y, 16) || !aligned(scale1, 16) || !aligned(scale2, 16) ||
         !aligned(w1_packed, kAlign) || !aligned(w2_packed, kAlign) || !aligned(workspace, kAlign))
-        return MOE_ERR_ALIGNMENT;
+        return MOE_FAIL(MOE_ERR_ALIGNMENT);
     const Layout L = layout_for(s, Op::Ffn);
-    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+    if (workspace_bytes < L.total) return MOE_FAIL(MOE_ERR_WORKSPACE);
     if (s.num_tokens == 0) return MOE_OK;
     const int64_t cap = s.num_tokens * s.topk;
     MOE_TRY(launch_sched(expert_offsets, s.num_experts, at<int32_t>(workspace, L.sched),
@@ -497,13 +513,13 @@ moe_status moe_grouped_ffn_q(const moe_shape *shape, const int8_t *expand_x,
     const moe_shape &s = *shape;
     const bool empty = s.num_tokens == 0;   // the per-row arrays may then be NULL
     if (!expert_offsets || !w1_packed || !scale1 || !w2_packed || !scale2 || !workspace)
-        return MOE_ERR_NULLPTR;
-    if (!empty && (!expand_x || !dynamic_scales || !y)) return MOE_ERR_NULLPTR;
+        return MOE_FAIL(MOE_ERR_NULLPTR);
+    if (!empty && (!expand_x || !dynamic_scales || !y)) return MOE_FAIL(MOE_ERR_NULLPTR);
     if (!aligned(expand_x, 16) || !aligned(y, 16) || !aligned(scale1, 16) || !aligned(scale2, 16) ||
         !aligned(w1_packed, kAlign) || !aligned(w2_packed, kAlign) || !aligned(workspace, kAlign))
-        return MOE_ERR_ALIGNMENT;
+        return MOE_FAIL(MOE_ERR_ALIGNMENT);
     const Layout L = layout_for(s, Op::Ffn);
-    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+    if (workspace_bytes < L.total) return MOE_FAIL(MOE_ERR_WORKSPACE);
     if (s.num_tokens == 0) return MOE_OK;
     const int64_t cap = s.num_tokens * s.topk;
     MOE_TRY(launch_sched(expert_offsets, s.num_experts, at<int32_t>(workspace, L.sched),
@@ -518,7 +534,7 @@ moe_status moe_grouped_ffn_q(const moe_shape *shape, const int8_t *expand_x,
 // ---------------------------------------------------------------- whole layer
 moe_status moe_layer_workspace_size(const moe_shape *shape, size_t *bytes) {
     MOE_TRY(check_shape(shape, true));
-    if (!bytes) return MOE_ERR_NULLPTR;
+    if (!bytes) return MOE_FAIL(MOE_ERR_NULLPTR);
     *bytes = layout_for(*shape, Op::Layer).total;
     return MOE_OK;
 }
@@ -532,19 +548,19 @@ moe_status moe_layer(const moe_shape *shape, const void *x, const int32_t *exper
     const moe_shape &s = *shape;
     // with T == 0 the per-token and per-route arrays are empty and may be NULL
     const bool empty = s.num_tokens == 0;
-    if (!w1_packed || !scale1 || !w2_packed || !scale2 || !workspace) return MOE_ERR_NULLPTR;
-    if (!empty && (!x || !expert_ids || !expert_scales || !x_out)) return MOE_ERR_NULLPTR;
-    if (!empty && s.has_shared && !shared_expert_x) return MOE_ERR_NULLPTR;
-    if (!s.has_shared && shared_expert_x) return MOE_ERR_PARAM_INVALID;
-    if (!empty && s.mask_kind != 0 && !x_active_mask) return MOE_ERR_NULLPTR;
-    if (s.mask_kind == 0 && x_active_mask) return MOE_ERR_PARAM_INVALID;
+    if (!w1_packed || !scale1 || !w2_packed || !scale2 || !workspace) return MOE_FAIL(MOE_ERR_NULLPTR);
+    if (!empty && (!x || !expert_ids || !expert_scales || !x_out)) return MOE_FAIL(MOE_ERR_NULLPTR);
+    if (!empty && s.has_shared && !shared_expert_x) return MOE_FAIL(MOE_ERR_NULLPTR);
+    if (!s.has_shared && shared_expert_x) return MOE_FAIL(MOE_ERR_PARAM_INVALID);
+    if (!empty && s.mask_kind != 0 && !x_active_mask) return MOE_FAIL(MOE_ERR_NULLPTR);
+    if (s.mask_kind == 0 && x_active_mask) return MOE_FAIL(MOE_ERR_PARAM_INVALID);
     if (!aligned(x, 16) || !aligned(x_out, 16) || !aligned(scale1, 16) || !aligned(scale2, 16) ||
         (shared_expert_x && !aligned(shared_expert_x, 16)) || !aligned(w1_packed, kAlign) ||
         !aligned(w2_packed, kAlign) || !aligned(workspace, kAlign) || !aligned(expert_ids, 4) ||
         !aligned(expert_scales, 4))
-        return MOE_ERR_ALIGNMENT;
+        return MOE_FAIL(MOE_ERR_ALIGNMENT);
     const Layout L = layout_for(s, Op::Layer);
-    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+    if (workspace_bytes < L.total) return MOE_FAIL(MOE_ERR_WORKSPACE);
     const int64_t cap = s.num_tokens * s.topk;
     RouteDev r = route_dev(s, expert_ids, x_active_mask, workspace, L);
     int32_t *route_row = at<int32_t>(workspace, L.route_row);
@@ -567,9 +583,9 @@ moe_status moe_layer(const moe_shape *shape, const void *x, const int32_t *exper
 moe_status moe_stage_views_get(const moe_shape *shape, int for_layer, void *workspace,
                                size_t workspace_bytes, moe_stage_views *v) {
     MOE_TRY(check_shape(shape, true));
-    if (!workspace || !v) return MOE_ERR_NULLPTR;
+    if (!workspace || !v) return MOE_FAIL(MOE_ERR_NULLPTR);
     const Layout L = layout_for(*shape, for_layer ? Op::Layer : Op::Ffn);
-    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+    if (workspace_bytes < L.total) return MOE_FAIL(MOE_ERR_WORKSPACE);
     memset(v, 0, sizeof *v);
     if (for_layer) {
         v->route_row = at<int32_t>(workspace, L.route_row);
@@ -606,10 +622,10 @@ static Layout gemm_layout(int64_t rows, int64_t E, int64_t N, int64_t Kd) {
 
 moe_status moe_grouped_gemm_s32_workspace_size(int64_t rows, int64_t E, int64_t N, int64_t Kd,
                                                size_t *bytes) {
-    if (!bytes) return MOE_ERR_NULLPTR;
+    if (!bytes) return MOE_FAIL(MOE_ERR_NULLPTR);
     if (rows < 0 || rows > INT32_MAX || E < 1 || E > kMaxExperts || N < 8 || N % 8 != 0 || Kd < 8 ||
         Kd % 8 != 0 || N > (1 << 20) || Kd > 131072)
-        return MOE_ERR_SHAPE;
+        return MOE_FAIL(MOE_ERR_SHAPE);
     *bytes = gemm_layout(rows, E, N, Kd).total;
     return MOE_OK;
 }
@@ -620,12 +636,12 @@ moe_status moe_grouped_gemm_s32(int64_t rows, int64_t E, int64_t N, int64_t Kd,
                                 cudaStream_t stream) {
     size_t need = 0;
     MOE_TRY(moe_grouped_gemm_s32_workspace_size(rows, E, N, Kd, &need));
-    if (!expert_offsets || !A || !W || !C || !workspace) return MOE_ERR_NULLPTR;
+    if (!expert_offsets || !A || !W || !C || !workspace) return MOE_FAIL(MOE_ERR_NULLPTR);
     if (!aligned(A, 16) || !aligned(W, 16) || !aligned(C, 16) || !aligned(workspace, kAlign))
-        return MOE_ERR_ALIGNMENT;
-    if (workspace_bytes < need) return MOE_ERR_WORKSPACE;
-    if (path < MOE_FFN_PATH_AUTO || path > MOE_FFN_PATH_LARGE_PAIR) return MOE_ERR_PARAM_INVALID;
-    if (path == MOE_FFN_PATH_SMALL && Kd % 16 != 0) return MOE_ERR_SHAPE;
+        return MOE_FAIL(MOE_ERR_ALIGNMENT);
+    if (workspace_bytes < need) return MOE_FAIL(MOE_ERR_WORKSPACE);
+    if (path < MOE_FFN_PATH_AUTO || path > MOE_FFN_PATH_LARGE_PAIR) return MOE_FAIL(MOE_ERR_PARAM_INVALID);
+    if (path == MOE_FFN_PATH_SMALL && Kd % 16 != 0) return MOE_FAIL(MOE_ERR_SHAPE);
     const bool small = Kd % 16 == 0 && use_small_path(path, rows, E);
     if (rows == 0) return MOE_OK;
     const Layout L = gemm_layout(rows, E, N, Kd);

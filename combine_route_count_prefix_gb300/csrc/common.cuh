@@ -109,10 +109,18 @@ __device__ __forceinline__ void pdl_wait() {
         if (_err != cudaSuccess) return MOE_ERR_CUDA;                                     \
     } while (0)
 
+// Optional log on stderr, set by the environment variable MOE_LOG (read
+// once): 1 reports every error status on its way out of the library (where it
+// arose: the function, or the failing call for MOE_TRY) and every non-zero
+// device status word read back; 2 also every kernel launch.  0 (the default)
+// prints nothing.
+int log_level();
+moe_status log_failure(const char *where, moe_status s);   // logs if enabled; returns s
+#define MOE_FAIL(s) ::moe::log_failure(__func__, (s))
 #define MOE_TRY(expr)                                                         \
     do {                                                                      \
         moe_status _s = (expr);                                               \
-        if (_s != MOE_OK) return _s;                                          \
+        if (_s != MOE_OK) return ::moe::log_failure(#expr, _s);               \
     } while (0)
 
 // ---------------------------------------------------------------- workspace

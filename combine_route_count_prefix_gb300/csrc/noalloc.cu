@@ -45,13 +45,13 @@ void *g_noalloc_addr[kMaxDevices] = {nullptr};
 // first call per device).
 moe_status noalloc_scratch(uint8_t **out) {
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_FAIL(MOE_ERR_CUDA);
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
     if (!g_noalloc_addr[dev]) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
             cudaGetLastError();
-            return MOE_ERR_CUDA;
+            return MOE_FAIL(MOE_ERR_CUDA);
         }
         g_noalloc_addr[dev] = p;
     }
@@ -76,21 +76,21 @@ moe_status moe_dispatch_noalloc(const moe_shape *shape, const void *x, const int
     MOE_TRY(check_shape(shape, false));
     const moe_shape &s = *shape;
     const bool empty = s.num_tokens == 0;
-    if (!expert_token_nums || !expert_offsets || !ep_recv_counts) return MOE_ERR_NULLPTR;
-    if (!empty && (!expert_ids || !assist || !route_row)) return MOE_ERR_NULLPTR;
-    if (!empty && expand_x && !x) return MOE_ERR_NULLPTR;
-    if (!empty && s.mask_kind != 0 && !x_active_mask) return MOE_ERR_NULLPTR;
-    if (s.mask_kind == 0 && x_active_mask) return MOE_ERR_PARAM_INVALID;
+    if (!expert_token_nums || !expert_offsets || !ep_recv_counts) return MOE_FAIL(MOE_ERR_NULLPTR);
+    if (!empty && (!expert_ids || !assist || !route_row)) return MOE_FAIL(MOE_ERR_NULLPTR);
+    if (!empty && expand_x && !x) return MOE_FAIL(MOE_ERR_NULLPTR);
+    if (!empty && s.mask_kind != 0 && !x_active_mask) return MOE_FAIL(MOE_ERR_NULLPTR);
+    if (s.mask_kind == 0 && x_active_mask) return MOE_FAIL(MOE_ERR_PARAM_INVALID);
     // the same alignment rules as moe_dispatch: 16-byte row vectors, 8-byte
     // counts, 4-byte indices
     auto misaligned = [](const void *ptr, uintptr_t a) { return ((uintptr_t)ptr % a) != 0; };
-    if (expand_x && (misaligned(x, 16) || misaligned(expand_x, 16))) return MOE_ERR_ALIGNMENT;
+    if (expand_x && (misaligned(x, 16) || misaligned(expand_x, 16))) return MOE_FAIL(MOE_ERR_ALIGNMENT);
     if (misaligned(expert_ids, 4) || misaligned(assist, 4) || misaligned(expert_token_nums, 8) ||
         misaligned(expert_offsets, 4) || misaligned(ep_recv_counts, 4) || misaligned(route_row, 4))
-        return MOE_ERR_ALIGNMENT;
+        return MOE_FAIL(MOE_ERR_ALIGNMENT);
     const int64_t chunks = route_chunks(s);
     const size_t entries = (size_t)(chunks * s.num_experts + chunks);
-    if (entries > kNoAllocScratchEntries) return MOE_ERR_TOO_LARGE;
+    if (entries > kNoAllocScratchEntries) return MOE_FAIL(MOE_ERR_TOO_LARGE);
 
     uint8_t *scratch = nullptr;
     MOE_TRY(noalloc_scratch(&scratch));

@@ -41,10 +41,10 @@ extern "C" {
 
 moe_status moe_wait_selftest(void *workspace, size_t workspace_bytes, uint64_t limit_ns,
                              cudaStream_t stream) {
-    if (!workspace) return MOE_ERR_NULLPTR;
-    if (((uintptr_t)workspace % kAlign) != 0) return MOE_ERR_ALIGNMENT;
-    if (workspace_bytes < 16) return MOE_ERR_WORKSPACE;
-    if (limit_ns == 0 || limit_ns > kTimeoutNs) return MOE_ERR_PARAM_INVALID;
+    if (!workspace) return MOE_FAIL(MOE_ERR_NULLPTR);
+    if (((uintptr_t)workspace % kAlign) != 0) return MOE_FAIL(MOE_ERR_ALIGNMENT);
+    if (workspace_bytes < 16) return MOE_FAIL(MOE_ERR_WORKSPACE);
+    if (limit_ns == 0 || limit_ns > kTimeoutNs) return MOE_FAIL(MOE_ERR_PARAM_INVALID);
     MOE_LAUNCH("wait_selftest", k_wait_selftest, 1, 32, 0, stream,
                static_cast<int32_t *>(workspace), (unsigned long long)limit_ns);
     return MOE_OK;

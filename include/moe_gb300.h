@@ -34,6 +34,11 @@
  *     Computation).
  *   - bf16 is IEEE binary32's upper half (stored as 2-byte words).
  *   - Concurrent calls that share a workspace race; give each stream its own.
+ *   - Optional log on stderr, set by the environment variable MOE_LOG (read
+ *     once per process): 1 reports every error status as it leaves the
+ *     library (the function or failing internal call, and the status) and
+ *     every non-zero device status word moe_read_device_status reads; 2 also
+ *     every kernel launch (name and CTA count).  Unset or 0: nothing printed.
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H

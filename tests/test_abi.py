@@ -193,3 +193,24 @@ def test_missing_library_fails_loudly():
         "print('no error'); sys.exit(1)\n" % ROOT)
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True)
     assert r.returncode == 0 and "raised True" in r.stdout, (r.stdout, r.stderr)
+
+
+def test_error_log_on_request():
+    """MOE_LOG=1 reports a rejected call on stderr; without it nothing is printed."""
+    import subprocess
+    import sys
+    code = (
+        "import sys; sys.path.insert(0, %r)\n"
+        "from combine_route_count_prefix_gb300 import binding as B\n"
+        "try:\n"
+        "    B.dispatch_workspace_size(B.make_shape(10, 3, 128, 8, 2))\n"
+        "except B.MoeError as e:\n"
+        "    print('code', e.code)\n" % ROOT)
+    env = dict(os.environ)
+    env.pop("MOE_LOG", None)
+    quiet = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
+    assert "code 561002" in quiet.stdout and "moe:" not in quiet.stderr, quiet.stderr
+    env["MOE_LOG"] = "1"
+    loud = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
+    assert "code 561002" in loud.stdout
+    assert "moe:" in loud.stderr and "561002" in loud.stderr, loud.stderr
