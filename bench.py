@@ -1,7 +1,7 @@
 """Benchmark of the single-GPU MoE dispatch / grouped FFN / combine path.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--no-layer]
+                    [--workload NAME | --config 1..5] [--no-layer] [--cpu-full]
 
 One step is one pass of the hot path over one batch: for the identity-expert
 workloads (decode_dispatch_combine, skewed_dispatch_combine) that is
@@ -70,6 +70,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode_dispatch_combine", choices=list(wl.WORKLOADS))
+    ap.add_argument("--config", type=int, choices=sorted(wl.CONFIGS), default=None,
+                    help="the benchmark configuration by number (1-5); overrides --workload")
     ap.add_argument("--no-layer", action="store_true",
                     help="skip the full layer workload (full_layer) that the identity-expert "
                          "workloads report as a secondary line item")
@@ -86,7 +88,10 @@ def parse():
     ap.add_argument("--ffn-path", default="auto", choices=["auto", "large", "small", "large_pair"],
                     help="grouped-GEMM kernels of the layer workloads (auto: small-batch "
                          "kernels when T*K <= 32*E)")
-    return ap.parse_args()
+    args = ap.parse_args()
+    if args.config is not None:
+        args.workload = wl.CONFIGS[args.config]
+    return args
 
 
 def peaks():

@@ -85,6 +85,12 @@ WORKLOADS = {
 }
 
 
+# The five benchmark configurations by number (1: tiny layer, 2: decode
+# dispatch + combine, 3: full layer, 4: skewed routing, 5: large prefill).
+CONFIGS = {1: "tiny_layer", 2: "decode_dispatch_combine", 3: "full_layer",
+           4: "skewed_dispatch_combine", 5: "large_prefill"}
+
+
 def rng_for(seed: int, kind: str, *sub: int) -> np.random.Generator:
     return np.random.Generator(np.random.PCG64(
         np.random.SeedSequence(seed, spawn_key=(_STREAM[kind],) + tuple(sub))))

@@ -81,3 +81,9 @@ def test_expert_weights_ranges():
     assert w1.shape == (32, 64) and w2.shape == (64, 16)
     assert w1.min() >= -127 and w1.max() <= 127 and w2.min() >= -127 and w2.max() <= 127
     assert s1.min() >= 1e-3 and s1.max() <= 1e-2 and s2.min() >= 1e-3 and s2.max() <= 1e-2
+
+
+def test_configs_by_number_name_existing_workloads():
+    assert sorted(wl.CONFIGS) == [1, 2, 3, 4, 5]
+    assert all(name in wl.WORKLOADS for name in wl.CONFIGS.values())
+    assert wl.CONFIGS[2] == "decode_dispatch_combine" and wl.CONFIGS[3] == "full_layer"
