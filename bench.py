@@ -82,6 +82,9 @@ def parse():
     ap.add_argument("--soak", type=float, default=2.0,
                     help="seconds of untimed steps before the timed region (clock samples)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--peak-probes", action="store_true",
+                    help="build and run the instruction-rate probes (mma.sync int8, HBM copy) and "
+                         "print them beside the measured peaks; one JSON line")
     ap.add_argument("--cpu-full", action="store_true",
                     help="one GPU step, then the oracle over the whole workload on every host "
                          "core (timed) and every output token compared with it; one JSON line")
@@ -314,6 +317,30 @@ def bf16_errors(got_bits, ref_bits):
             "rel_l2": float(np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-30)),
             "tokens_within_2_ulp": int((tok_max <= 2.0).sum()),
             "tokens_bit_exact": int((got_bits == ref_bits).all(axis=1).sum())}
+
+
+def run_peak_probes():
+    """The legacy int8 tensor instruction (mma.sync m16n8k32 s8, exact int32
+    accumulation) and a streaming copy, measured on this GPU, beside the
+    measured bf16 and HBM peaks the rooflines use."""
+    import subprocess
+    from combine_route_count_prefix_gb300 import build as bld
+    src = os.path.join(ROOT, "combine_route_count_prefix_gb300", "probes", "peak_probes.cu")
+    exe = os.path.join(bld.BUILD, "peak_probes")
+    os.makedirs(bld.BUILD, exist_ok=True)
+    r = subprocess.run([bld.nvcc(), *bld.ARCH, "-O3", "-std=c++17", "-o", exe, src],
+                       capture_output=True, text=True)
+    if r.returncode:
+        raise RuntimeError(r.stderr[-2000:])
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=300)
+    if r.returncode:
+        raise RuntimeError(r.stderr[-2000:])
+    probe = json.loads(r.stdout.strip().splitlines()[-1])
+    pk = peaks()
+    line = {"peak_probes": probe, "measured_peaks": pk,
+            "mma_sync_s8_vs_bf16_peak": probe["mma_sync_s8_tops"] / pk["bf16_tflops"],
+            "copy_vs_hbm_peak": probe["copy_gbs"] / pk["hbm_gbs"]}
+    print(json.dumps(line), flush=True)
 
 
 def run_cpu_full(args):
@@ -872,6 +899,9 @@ def main():
     elif args.cpu_full:
         if rank == 0 and world == 1:
             run_cpu_full(args)
+    elif args.peak_probes:
+        if rank == 0:
+            run_peak_probes()
     else:
         run_ours(args, rank, world, dist)
     if dist is not None:
