@@ -214,3 +214,45 @@ def test_error_log_on_request():
     loud = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
     assert "code 561002" in loud.stdout
     assert "moe:" in loud.stderr and "561002" in loud.stderr, loud.stderr
+
+
+def test_header_compiles_as_c_and_links(B, tmp_path):
+    """The header is plain C: a C99 program compiles against it with gcc, links
+    to the library and calls a host-only entry point, whose answer matches the
+    Python binding's."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no gcc")
+    cuda_inc = None
+    for cand in ("/usr/local/cuda/include", os.path.join(os.environ.get("CUDA_HOME", ""), "include")):
+        if cand and os.path.exists(os.path.join(cand, "cuda_runtime_api.h")):
+            cuda_inc = cand
+            break
+    if cuda_inc is None:
+        pytest.skip("no CUDA headers")
+    src = tmp_path / "use_abi.c"
+    src.write_text(
+        '#include "moe_gb300.h"\n'
+        "#include <stdio.h>\n"
+        "int main(void) {\n"
+        "    moe_shape s = {.num_tokens = 2048, .num_partitions = 16, .hidden = 7168,\n"
+        "                   .num_experts = 256, .topk = 8, .mask_kind = 1,\n"
+        "                   .ffn_path = MOE_FFN_PATH_AUTO};\n"
+        "    size_t ws = 0;\n"
+        "    moe_status st = moe_dispatch_workspace_size(&s, &ws);\n"
+        "    printf(\"%s %zu\\n\", moe_status_string(st), ws);\n"
+        "    return st == MOE_OK ? 0 : 1;\n"
+        "}\n")
+    exe = tmp_path / "use_abi"
+    lib_dir = os.path.dirname(B.LIB_PATH)
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        "-I", cuda_inc, str(src), "-o", str(exe), "-L", lib_dir, "-lmoe_gb300",
+                        "-Wl,-rpath," + lib_dir],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert run.returncode == 0, (run.stdout, run.stderr)
+    want = B.dispatch_workspace_size(B.make_shape(2048, 16, 7168, 256, 8, mask_kind=1))
+    assert run.stdout.split() == ["ok", str(want)]
