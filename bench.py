@@ -83,7 +83,7 @@ def parse():
                     help="seconds of untimed steps before the timed region (clock samples)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--peak-probes", action="store_true",
-                    help="build and run the instruction-rate probes (mma.sync int8, HBM copy) and "
+                    help="build and run the probes (mma.sync int8, HBM copy, host link) and "
                          "print them beside the measured peaks; one JSON line")
     ap.add_argument("--cpu-full", action="store_true",
                     help="one GPU step, then the oracle over the whole workload on every host "
@@ -321,8 +321,9 @@ def bf16_errors(got_bits, ref_bits):
 
 def run_peak_probes():
     """The legacy int8 tensor instruction (mma.sync m16n8k32 s8, exact int32
-    accumulation) and a streaming copy, measured on this GPU, beside the
-    measured bf16 and HBM peaks the rooflines use."""
+    accumulation), a streaming copy and the host link (DMA in, out and both
+    ways, and a kernel reading pinned host memory), measured on this GPU,
+    beside the measured bf16 and HBM peaks the rooflines use."""
     import subprocess
     from combine_route_count_prefix_gb300 import build as bld
     src = os.path.join(ROOT, "combine_route_count_prefix_gb300", "probes", "peak_probes.cu")

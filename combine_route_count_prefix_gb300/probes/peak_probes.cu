@@ -9,6 +9,11 @@
 //            the instruction's own.
 //   copy     a streaming device-to-device copy (16-byte vectors, grid-stride),
 //            to set beside the measured HBM peak.
+//   link     the host link with pinned (mapped) host memory, one 29.4 MB tensor
+//            (2048 x 7168 bf16) per copy: DMA host-to-device, device-to-host and
+//            both at once on two streams, and the same copy kernel reading the
+//            host buffer directly, the bound of a step whose inputs start on the
+//            host.
 //
 // Prints one JSON object on stdout.
 #include <cstdint>
@@ -111,12 +116,65 @@ int main() {
         if (ms < copy_ms) copy_ms = ms;
     }
     const double copy_gbs = 2.0 * bytes / (copy_ms * 1e-3) / 1e9;
-
-    printf("{\"sms\": %d, \"mma_sync_s8_tops\": %.1f, \"mma_sync_s8_ms\": %.3f, "
-           "\"copy_gbs\": %.1f, \"copy_ms\": %.3f}\n",
-           sms, mma_tops, best_ms, copy_gbs, copy_ms);
-    CK(cudaFree(out));
     CK(cudaFree(src));
     CK(cudaFree(dst));
+
+    // ---- host link
+    const size_t lb = (size_t)2048 * 7168 * 2;
+    void *h_in = nullptr, *h_out = nullptr, *dh_in = nullptr, *d_a = nullptr, *d_b = nullptr;
+    CK(cudaHostAlloc(&h_in, lb, cudaHostAllocMapped));
+    CK(cudaHostAlloc(&h_out, lb, cudaHostAllocMapped));
+    CK(cudaHostGetDevicePointer(&dh_in, h_in, 0));
+    CK(cudaMalloc(&d_a, lb));
+    CK(cudaMalloc(&d_b, lb));
+    CK(cudaMemset(d_b, 2, lb));
+    for (size_t i = 0; i < lb; ++i) ((unsigned char *)h_in)[i] = (unsigned char)i;
+    cudaStream_t s0, s1;
+    CK(cudaStreamCreateWithFlags(&s0, cudaStreamNonBlocking));
+    CK(cudaStreamCreateWithFlags(&s1, cudaStreamNonBlocking));
+    cudaEvent_t join;
+    CK(cudaEventCreateWithFlags(&join, cudaEventDisableTiming));
+    // kind 0: DMA in, 1: DMA out, 2: both (two streams), 3: copy kernel reading host memory
+    double link_gbs[4];
+    for (int kind = 0; kind < 4; ++kind) {
+        float best = 1e30f;
+        for (int r = 0; r < 8; ++r) {   // the first three runs are warm-up
+            CK(cudaEventRecord(a, s0));
+            if (kind == 0 || kind == 2) CK(cudaMemcpyAsync(d_a, h_in, lb, cudaMemcpyHostToDevice, s0));
+            if (kind == 1) CK(cudaMemcpyAsync(h_out, d_b, lb, cudaMemcpyDeviceToHost, s0));
+            if (kind == 2) {
+                CK(cudaStreamWaitEvent(s1, a, 0));   // starts with the copy in: both run together
+                CK(cudaMemcpyAsync(h_out, d_b, lb, cudaMemcpyDeviceToHost, s1));
+                CK(cudaEventRecord(join, s1));
+                CK(cudaStreamWaitEvent(s0, join, 0));
+            }
+            if (kind == 3) k_copy<<<sms * 2, 512, 0, s0>>>((const uint4 *)dh_in, (uint4 *)d_a, lb / 16);
+            CK(cudaEventRecord(b, s0));
+            CK(cudaEventSynchronize(b));
+            CK(cudaGetLastError());
+            float ms = 0;
+            CK(cudaEventElapsedTime(&ms, a, b));
+            if (r >= 3 && ms < best) best = ms;
+        }
+        link_gbs[kind] = (kind == 2 ? 2.0 : 1.0) * lb / (best * 1e-3) / 1e9;
+    }
+    CK(cudaMemcpy(h_out, d_a, lb, cudaMemcpyDeviceToHost));   // the direct read delivered the host bytes
+    for (size_t i = 0; i < lb; i += 4093)
+        if (((unsigned char *)h_out)[i] != (unsigned char)i) {
+            fprintf(stderr, "host-read copy mismatch at %zu\n", i);
+            return 1;
+        }
+
+    printf("{\"sms\": %d, \"mma_sync_s8_tops\": %.1f, \"mma_sync_s8_ms\": %.3f, "
+           "\"copy_gbs\": %.1f, \"copy_ms\": %.3f, \"link_h2d_dma_gbs\": %.1f, "
+           "\"link_d2h_dma_gbs\": %.1f, \"link_bidir_dma_gbs\": %.1f, "
+           "\"link_h2d_sm_gbs\": %.1f, \"link_bytes\": %zu}\n",
+           sms, mma_tops, best_ms, copy_gbs, copy_ms, link_gbs[0], link_gbs[1], link_gbs[2],
+           link_gbs[3], lb);
+    CK(cudaFree(out));
+    CK(cudaFree(d_a));
+    CK(cudaFree(d_b));
+    CK(cudaFreeHost(h_in));
+    CK(cudaFreeHost(h_out));
     return 0;
 }
