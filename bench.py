@@ -216,6 +216,32 @@ def identity_bytes(w, inp, R):
                 total=dispatch_rows + routing + combine)
 
 
+def layer_row_bytes(w, inp, R):
+    """HBM bytes of the layer's row kernels per launch, two ways: with each
+    quantisation code counted as the int8 byte the method defines, and as the
+    bytes the kernels move (codes stored as fp16 images, the GEMMs' operand
+    format).  quant_scatter: x once per active token, the codes and per-row
+    scales of R rows, route_row; quant2: g (fp32) read, codes and scales
+    written; combine: y rows (bf16), the shared term, the output, route_row
+    and probabilities."""
+    T, K, H, Nh = w.num_tokens, w.topk, w.hidden, w.ffn // 2
+    mask = inp["mask"]
+    act = np.ones((T, K), bool)
+    if mask is not None:
+        act &= (mask[:, None] if mask.ndim == 1 else mask).astype(bool)
+    tok_active = int(act.any(axis=1).sum())
+    mask_bytes = 0 if mask is None else mask.size
+    idx = T * K * 4 + mask_bytes
+    comb = R * H * 2 + T * H * 2 * (2 if inp["shared"] is not None else 1) + T * K * 8 + mask_bytes
+    return {
+        "quant_scatter": {"int8_codes": tok_active * H * 2 + R * H + R * 4 + idx,
+                          "as_moved": tok_active * H * 2 + R * H * 2 + R * 4 + idx},
+        "quant2": {"int8_codes": R * Nh * 4 + R * Nh + R * 4,
+                   "as_moved": R * Nh * 4 + R * Nh * 2 + R * 4},
+        "combine": {"int8_codes": comb, "as_moved": comb},
+    }
+
+
 def max_over_ranks(v, dist, device=None):
     """Largest value of v over all ranks (v itself without a process group)."""
     if dist is None:
@@ -535,6 +561,16 @@ class LayerPath:
         extra = {"ffn_path": "small" if small else ("large_pair" if sfx else "large"),
                  "gemm_tflops": {k: fl[k] / (prof[k][1] / prof[k][0] * 1e-3) / 1e12 for k in fl},
                  "status": self.B.read_device_status(self.ws)}
+        rows = {}
+        for k, by in layer_row_bytes(w, self.inp, R).items():
+            if k not in prof:
+                continue
+            us = prof[k][1] / prof[k][0] * 1e3
+            rows[k] = {"us": round(us, 3), "bytes_int8_codes": by["int8_codes"],
+                       "bytes_as_moved": by["as_moved"],
+                       "frac_int8_codes": by["int8_codes"] / (us * 1e-6) / 1e9 / pk["hbm_gbs"],
+                       "frac_as_moved": by["as_moved"] / (us * 1e-6) / 1e9 / pk["hbm_gbs"]}
+        extra["row_kernels"] = rows
         step_bytes = None
         if small:
             # few rows per expert: reading the int8 weights of every expert that

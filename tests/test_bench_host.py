@@ -35,6 +35,23 @@ def test_identity_bytes_route_mask_counts_tokens_with_any_active_route():
     assert b["dispatch_rows"] == 2 * 16 + 2 * 16 + 3 * 2 * 4
 
 
+def test_layer_row_bytes_by_hand():
+    # 4 tokens, K = 2, H = 8, N = 16 (8 g columns), route mask with token 2
+    # fully masked; no shared term
+    w = wl.custom(P=2, M=2, H=8, E=3, K=2, N=16, mask_kind=2, mask_p=0.5)
+    inp = {"mask": np.array([[1, 0], [1, 1], [0, 0], [0, 1]], np.uint8), "shared": None}
+    R = 4
+    b = bench.layer_row_bytes(w, inp, R)
+    idx = 4 * 2 * 4 + 8                                   # route_row + the route mask
+    x = 3 * 8 * 2                                         # three tokens with an active route
+    assert b["quant_scatter"] == {"int8_codes": x + R * 8 + R * 4 + idx,
+                                  "as_moved": x + R * 8 * 2 + R * 4 + idx}
+    assert b["quant2"] == {"int8_codes": R * 8 * 4 + R * 8 + R * 4,
+                           "as_moved": R * 8 * 4 + R * 8 * 2 + R * 4}
+    comb = R * 16 + 4 * 16 + 4 * 2 * 8 + 8                # y rows, out, route_row + probs, mask
+    assert b["combine"] == {"int8_codes": comb, "as_moved": comb}
+
+
 def test_whole_job_rate_is_weak_scaling():
     assert bench.whole_job_tokens_per_s(2048, 1, 0.1) == pytest.approx(2048 / 1e-4)
     assert bench.whole_job_tokens_per_s(2048, 4, 0.1) == pytest.approx(4 * 2048 / 1e-4)
