@@ -90,7 +90,7 @@ def parse():
                          "core (timed) and every output token compared with it; one JSON line")
     ap.add_argument("--ffn-path", default="auto", choices=["auto", "large", "small", "large_pair"],
                     help="grouped-GEMM kernels of the layer workloads (auto: small-batch "
-                         "kernels when T*K <= 32*E)")
+                         "kernels when T*K <= 64*E)")
     args = ap.parse_args()
     if args.config is not None:
         args.workload = wl.CONFIGS[args.config]

@@ -21,10 +21,11 @@
 //   warps 1, 3   MMA issuers: one thread spends ~130 cycles issuing each
 //                tcgen05.mma whatever its N, and two threads issue at twice
 //                the rate, so the 8 MMAs (K = 16) of a 128-deep k-block are
-//                split: issuer i takes K [64 i, 64 i + 64) into its own pair of
-//                64-column accumulators (the sums are exact integers, so how
-//                they are split and added does not matter); warp 1 also owns
-//                TMEM (512 columns: 4 accumulators and four 64-column A stages)
+//                split: issuer i takes K [64 i, 64 i + 64) into its own 128
+//                accumulator columns (the sums are exact integers, so how they
+//                are split and added does not matter); warp 1 also owns TMEM
+//                (512 columns: the issuers' 256 accumulator columns and four
+//                64-column A stages)
 //   warp 2       row producer: the tile's rows (fp16 images, 128-byte swizzle)
 //                as 16-row TMA boxes, two 64-wide halves per k-block, into a
 //                4-stage ring
@@ -34,9 +35,17 @@
 //   warps 8..15  epilogue: warp % 4 selects the TMEM lane quadrant (32 output
 //                channels), (warp - 8) / 4 the half of the tile's rows; adds
 //                the two issuers' accumulators
-// Tiles are (expert, 64-row block of its rows, 128-channel block), channel
-// block fastest; the 64-row block schedule is computed here from the offsets.  Every wait is bounded (about two seconds) and sets
-// MOE_DEV_TIMEOUT.
+// Tiles are (expert, TB-row block of its rows, 128-channel block), channel
+// block fastest; the row block schedule is computed here from the offsets.
+// Two tile heights:
+//   TB = 64   each issuer's 128 columns hold two 64-column accumulators, so
+//             the MMAs of one 1024-deep chunk run while the epilogue drains
+//             the previous one (rows average at most 32 per expert);
+//   TB = 128  one 128-column accumulator per issuer: an expert of up to 128
+//             rows reads its weights once, at the cost of the MMAs waiting
+//             for each drain; chunks are 16 k-blocks (each issuer sums 1024
+//             products per row, still exact) to halve the drains.
+// Every wait is bounded (about two seconds) and sets MOE_DEV_TIMEOUT.
 #include "common.cuh"
 #include "tcgen05.cuh"
 
@@ -48,35 +57,48 @@ namespace {
 using namespace tc;
 
 constexpr int BW = 128;                  // weight rows (output channels) per tile = MMA M
-constexpr int TB = 64;                   // token rows per tile
 constexpr int BK = 128;                  // k-block
 constexpr int BKH = 64;                  // one 128-byte swizzle atom of fp16 rows
 constexpr int S8 = 4;                    // int8 weight ring stages
 constexpr int SA = 4;                    // operand stages: TMEM A + shared-memory rows
 constexpr int W8_BYTES = BW * BK;        // 16 KB
-constexpr int B_HALF_BYTES = TB * BKH * 2;   // 8 KB: one 64-wide half of the rows
-constexpr int B_BYTES = 2 * B_HALF_BYTES;
 constexpr int BOX_ROWS = 16;
 constexpr int BOX_BYTES = BOX_ROWS * BKH * 2;
-constexpr int CHUNK_KB = 8;              // 1024-deep exact chunk
 constexpr int CONV_WARP0 = 4;            // warps 4..7: TMEM lane quadrants 0..3
 constexpr int EPI_WARP0 = 8;
 constexpr int EPI_WARPS = 8;
-constexpr int EPI_COLS = TB / 2;         // tile rows per epilogue warp
 constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int ISSUERS = 2;
-constexpr uint32_t ACC_COLS = 128;         // per issuer: two accumulators of TB columns
+constexpr uint32_t ACC_COLS = 128;       // per issuer
 constexpr uint32_t A_COL0 = ISSUERS * ACC_COLS;
 constexpr uint32_t A_STAGE_COLS = BK / 2;
 constexpr size_t kBarrierBytes = 512;
-constexpr size_t RING_BYTES = (size_t)SA * B_BYTES + (size_t)S8 * W8_BYTES;
-constexpr size_t SMEM_BYTES = RING_BYTES + 1024 + kBarrierBytes + 2 * (kMaxExperts + 1) * sizeof(int32_t);
+// rows averaging at most this many per expert take the 64-row tiles
+constexpr int64_t kNarrowTileMaxRowsPerExpert = 32;
 static_assert(A_COL0 + SA * A_STAGE_COLS <= TMEM_COLS, "TMEM budget");
-static_assert(2 * TB <= (int)ACC_COLS, "accumulators");
 static_assert(BK / 16 == 4 * ISSUERS, "k-steps split between the issuers");
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert((2 * S8 + 2 * SA + 5) * 8 + 16 <= (int)kBarrierBytes, "barrier area");
+
+// Sizes that follow from the tile height TB (64 or 128 rows).
+template <int TB_>
+struct SmallCfg {
+    static constexpr int TB = TB_;
+    static constexpr int NBUF = (int)ACC_COLS / TB;    // accumulators per issuer
+    static constexpr int CHUNK_KB = TB == 64 ? 8 : 16;  // k-blocks per exact chunk
+    static constexpr int B_HALF_BYTES = TB * BKH * 2;   // one 64-wide half of the rows
+    static constexpr int B_BYTES = 2 * B_HALF_BYTES;
+    static constexpr int EPI_COLS = TB / 2;             // tile rows per epilogue warp
+    static constexpr size_t RING_BYTES = (size_t)SA * B_BYTES + (size_t)S8 * W8_BYTES;
+    static constexpr size_t SMEM_BYTES =
+        RING_BYTES + 1024 + kBarrierBytes + 2 * (kMaxExperts + 1) * sizeof(int32_t);
+    static_assert(TB == 64 || TB == 128, "tile heights");
+    static_assert(NBUF * TB == (int)ACC_COLS && NBUF <= 2, "accumulators");
+    // each issuer adds BK / ISSUERS products per k-block into its accumulator;
+    // fp32 holds every integer sum of at most 1024 int8 products exactly
+    static_assert(CHUNK_KB * (BK / ISSUERS) <= 1024, "exact chunk");
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
 
 struct SmallDev {
     const int32_t *offsets;
@@ -100,6 +122,7 @@ struct Tile {
     int e, row0, rows, wb;
 };
 
+template <int TB>
 __device__ __forceinline__ Tile decode_tile(int64_t tile, int n_wblocks, int E,
                                             const int32_t *s_sched, const int32_t *s_off) {
     Tile t;
@@ -129,7 +152,7 @@ __device__ __forceinline__ uint32_t widen_pair(uint32_t word, uint32_t sel) {
 // ---------------------------------------------------------------- epilogues
 // acc[i] is the exact int32 sum of output channel `ch` (a row of the weight
 // tile, lane quadrant q) for row t.row0 + c0 + i of the tile.
-template <int EPI>
+template <int EPI, int EPI_COLS>
 __device__ __forceinline__ void epilogue_small(const SmallDev &p, const Tile &t, int q, int lane,
                                                int c0, const int32_t (&acc)[EPI_COLS]) {
     const int ch = t.wb * BW + q * 32 + lane;
@@ -171,14 +194,19 @@ __device__ __forceinline__ void epilogue_small(const SmallDev &p, const Tile &t,
 }
 
 // ---------------------------------------------------------------- the kernel
-template <int EPI>
+template <int EPI, int TB_>
 __global__ void __launch_bounds__(THREADS, 1)
 k_gemm_small(const __grid_constant__ CUtensorMap tmRows, const __grid_constant__ CUtensorMap tmW,
              SmallDev p) {
+    using Cfg = SmallCfg<TB_>;
+    constexpr int TB = Cfg::TB, NBUF = Cfg::NBUF, CHUNK_KB = Cfg::CHUNK_KB;
+    constexpr int B_HALF_BYTES = Cfg::B_HALF_BYTES, B_BYTES = Cfg::B_BYTES;
+    constexpr int EPI_COLS = Cfg::EPI_COLS;
+    constexpr size_t RING_BYTES = Cfg::RING_BYTES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint8_t *ringB = smem;                                   // SA x 16 KB fp16 rows
+    uint8_t *ringB = smem;                                   // SA x B_BYTES fp16 rows
     uint8_t *ring8 = ringB + (size_t)SA * B_BYTES;           // S8 x 16 KB biased int8 weights
     uint64_t *w8_full = reinterpret_cast<uint64_t *>(smem + RING_BYTES);
     uint64_t *w8_empty = w8_full + S8;
@@ -259,7 +287,7 @@ k_gemm_small(const __grid_constant__ CUtensorMap tmRows, const __grid_constant__
             for (int s = 0; s < S8; ++s) issued_phase[s] = -1;
             bool ok = true;
             for (int64_t tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-                const Tile t = decode_tile(tile, p.n_wblocks, p.E, s_sched, s_off);
+                const Tile t = decode_tile<TB>(tile, p.n_wblocks, p.E, s_sched, s_off);
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!wait_bounded(&w8_empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
                     mbar_arrive_expect_tx(&w8_full[stage], W8_BYTES);
@@ -283,7 +311,7 @@ k_gemm_small(const __grid_constant__ CUtensorMap tmRows, const __grid_constant__
             for (int s = 0; s < SA; ++s) issued_phase[s] = -1;
             bool ok = true;
             for (int64_t tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-                const Tile t = decode_tile(tile, p.n_wblocks, p.E, s_sched, s_off);
+                const Tile t = decode_tile<TB>(tile, p.n_wblocks, p.E, s_sched, s_off);
                 const int nbox = (t.rows + BOX_ROWS - 1) / BOX_ROWS;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!wait_bounded(&ab_empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
@@ -357,7 +385,7 @@ k_gemm_small(const __grid_constant__ CUtensorMap tmRows, const __grid_constant__
             uint32_t acc_phase = 0;
             bool ok = true;
             for (int64_t tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-                const Tile t = decode_tile(tile, p.n_wblocks, p.E, s_sched, s_off);
+                const Tile t = decode_tile<TB>(tile, p.n_wblocks, p.E, s_sched, s_off);
                 const int n16 = ((t.rows + 15) / 16) * 16;
                 const uint32_t idesc = idesc_f16(BW, n16);
                 for (int kb0 = 0; ok && kb0 < p.num_kb; kb0 += CHUNK_KB) {
@@ -383,7 +411,7 @@ k_gemm_small(const __grid_constant__ CUtensorMap tmRows, const __grid_constant__
                     }
                     if (!ok) break;
                     mma_commit(&acc_full[accb]);
-                    if (++accb == 2) { accb = 0; acc_phase ^= 1u; }
+                    if (++accb == NBUF) { accb = 0; acc_phase ^= 1u; }
                 }
             }
             mma_commit(drain);
@@ -395,9 +423,12 @@ k_gemm_small(const __grid_constant__ CUtensorMap tmRows, const __grid_constant__
         const int c0 = ((warp - EPI_WARP0) >> 2) * EPI_COLS;   // first tile row of this warp
         int accb = 0;
         uint32_t acc_phase = 0;
+        // columns per TMEM load: 16 when a warp holds 64 rows' sums, so the load
+        // buffer and the sums fit the registers together
+        constexpr int LDW = EPI_COLS > 32 ? 16 : 32;
         for (int64_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-            const Tile t = decode_tile(tile, p.n_wblocks, p.E, s_sched, s_off);
-            const int nj = (t.rows - c0 + 31) / 32;   // 32-column groups holding rows (may be <= 0)
+            const Tile t = decode_tile<TB>(tile, p.n_wblocks, p.E, s_sched, s_off);
+            const int nj = (t.rows - c0 + LDW - 1) / LDW;   // column groups holding rows (may be <= 0)
             int32_t acc[EPI_COLS];
 #pragma unroll
             for (int i = 0; i < EPI_COLS; ++i) acc[i] = 0;
@@ -409,26 +440,29 @@ k_gemm_small(const __grid_constant__ CUtensorMap tmRows, const __grid_constant__
                 const uint32_t taddr =
                     tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(accb * TB + c0);
 #pragma unroll
-                for (int j = 0; j < EPI_COLS / 32; ++j) {
+                for (int j = 0; j < EPI_COLS / LDW; ++j) {
                     if (j < nj) {
 #pragma unroll
                         for (int is = 0; is < ISSUERS; ++is) {
-                            uint32_t r[32];
-                            tmem_ld32(taddr + is * ACC_COLS + 32 * j, r);
+                            uint32_t r[LDW];
+                            if constexpr (LDW == 32)
+                                tmem_ld32(taddr + is * ACC_COLS + LDW * j, r);
+                            else
+                                tmem_ld16(taddr + is * ACC_COLS + LDW * j, r);
                             tmem_ld_wait();
 #pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                acc[32 * j + i] += __float2int_rn(__uint_as_float(r[i]));
+                            for (int i = 0; i < LDW; ++i)
+                                acc[LDW * j + i] += __float2int_rn(__uint_as_float(r[i]));
                         }
                     }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&acc_empty[accb]);
-                if (++accb == 2) { accb = 0; acc_phase ^= 1u; }
+                if (++accb == NBUF) { accb = 0; acc_phase ^= 1u; }
             }
             if (!ok) break;
-            if (nj > 0) epilogue_small<EPI>(p, t, q, lane, c0, acc);
+            if (nj > 0) epilogue_small<EPI, EPI_COLS>(p, t, q, lane, c0, acc);
         }
     }
 
@@ -438,13 +472,21 @@ k_gemm_small(const __grid_constant__ CUtensorMap tmRows, const __grid_constant__
     if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
 }
 
+template <int EPI, int TB>
+moe_status launch_small_tb(const CUtensorMap &mr, const CUtensorMap &mw, const SmallDev &d,
+                           cudaStream_t stream) {
+    constexpr size_t smem = SmallCfg<TB>::SMEM_BYTES;
+    if (!set_smem_limit((const void *)k_gemm_small<EPI, TB>, smem)) return MOE_ERR_CUDA;
+    const char *names[3] = {"gemm_s32_small", "gemm1_swiglu_small", "gemm2_dequant_small"};
+    MOE_LAUNCH(names[EPI], (k_gemm_small<EPI, TB>), num_sms(), THREADS, smem, stream, mr, mw, d);
+    return MOE_OK;
+}
+
 template <int EPI>
 moe_status launch_small_epi(const CUtensorMap &mr, const CUtensorMap &mw, const SmallDev &d,
-                            cudaStream_t stream) {
-    if (!set_smem_limit((const void *)k_gemm_small<EPI>, SMEM_BYTES)) return MOE_ERR_CUDA;
-    const char *names[3] = {"gemm_s32_small", "gemm1_swiglu_small", "gemm2_dequant_small"};
-    MOE_LAUNCH(names[EPI], k_gemm_small<EPI>, num_sms(), THREADS, SMEM_BYTES, stream, mr, mw, d);
-    return MOE_OK;
+                            bool wide, cudaStream_t stream) {
+    return wide ? launch_small_tb<EPI, 128>(mr, mw, d, stream)
+                : launch_small_tb<EPI, 64>(mr, mw, d, stream);
 }
 
 }  // namespace
@@ -482,10 +524,14 @@ moe_status launch_grouped_gemm_small(Epi epi, const GemmArgs &a, cudaStream_t st
     d.scale2 = a.scale2;
     d.s2 = a.s2;
     d.status = a.status;
+    // the row capacity bounds the rows present: 64-row tiles while it averages
+    // at most 32 rows per expert, else 128-row tiles
+    const bool wide = a.cap_rows > kNarrowTileMaxRowsPerExpert * a.E;
     switch (epi) {
-        case Epi::S32: return launch_small_epi<(int)Epi::S32>(mr, mw, d, stream);
-        case Epi::SwiGLU: return launch_small_epi<(int)Epi::SwiGLU>(mr, mw, d, stream);
-        case Epi::DequantBF16: return launch_small_epi<(int)Epi::DequantBF16>(mr, mw, d, stream);
+        case Epi::S32: return launch_small_epi<(int)Epi::S32>(mr, mw, d, wide, stream);
+        case Epi::SwiGLU: return launch_small_epi<(int)Epi::SwiGLU>(mr, mw, d, wide, stream);
+        case Epi::DequantBF16:
+            return launch_small_epi<(int)Epi::DequantBF16>(mr, mw, d, wide, stream);
     }
     return MOE_ERR_PARAM_INVALID;
 }

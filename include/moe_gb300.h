@@ -115,7 +115,10 @@ typedef struct moe_shape {
  *          tensor memory as the MMA's 128-row side, against the expert's rows
  *          (only those present); for few rows per expert, where reading the
  *          weights bounds the time ("PTO MegaMoE ...", Supported Cases: the M
- *          sweep from 16 tokens per rank).
+ *          sweep from 16 tokens per rank).  Row tiles of 64 while the row
+ *          capacity (T*K, or the rows of moe_grouped_gemm_s32's A) is at most
+ *          32 per expert, else of 128, so that an expert of up to 128 rows
+ *          reads its weights once.
  *   AUTO:  SMALL when T*K <= MOE_FFN_SMALL_ROWS_PER_EXPERT * E, else LARGE_PAIR.
  * moe_pack_weights writes the weight format(s) of the path in the shape it is
  * given, and the FFN calls read the format of theirs: pack with the same
@@ -125,7 +128,7 @@ typedef struct moe_shape {
 #define MOE_FFN_PATH_SMALL 2
 #define MOE_FFN_PATH_LARGE_PAIR 3
 /* Any other ffn_path value returns MOE_ERR_PARAM_INVALID. */
-#define MOE_FFN_SMALL_ROWS_PER_EXPERT 32
+#define MOE_FFN_SMALL_ROWS_PER_EXPERT 64
 
 /* ------------------------------------------------------------------------
  * Dispatch.
@@ -304,9 +307,10 @@ moe_status moe_stage_views_get(const moe_shape *shape, int for_layer, void *work
  * rows r in [offsets[e], offsets[e+1]).
  *   A int8 [rows, Kd]; W int8 [E, N, Kd]; C int32 [rows, N]; rows >= offsets[E].
  *   N % 8 == 0, Kd % 8 == 0 (Kd % 16 == 0 for the SMALL kernel).
- * path: MOE_FFN_PATH_* (AUTO: SMALL when rows <= 32 * E and Kd % 16 == 0, else
- * LARGE_PAIR).  A is first converted into fp16 images in the workspace, and W
- * into fp16 images (LARGE, LARGE_PAIR) or biased bytes (SMALL).
+ * path: MOE_FFN_PATH_* (AUTO: SMALL when rows <= MOE_FFN_SMALL_ROWS_PER_EXPERT * E
+ * and Kd % 16 == 0, else LARGE_PAIR).  A is first converted into fp16 images in
+ * the workspace, and W into fp16 images (LARGE, LARGE_PAIR) or biased bytes
+ * (SMALL).
  * ------------------------------------------------------------------------ */
 moe_status moe_grouped_gemm_s32_workspace_size(int64_t rows, int64_t E, int64_t N, int64_t Kd,
                                                size_t *bytes);

@@ -41,6 +41,10 @@ PATHS = ["large", "large_pair", "small"]
     # N not a multiple of the 128-channel weight tile
     ([1, 15, 16, 17, 31, 33, 63, 64, 65, 127, 128, 129, 255, 256, 257, 0], 136, 80, 4),
     ([8] * 40 + [0] * 8 + [3] * 16, 384, 7168, 5),
+    # the same ragged counts spread over 48 experts: the small kernel's 64-row
+    # tiles (rows averaging at most 32 per expert), experts of 65-129 rows
+    # taking two or three of them; the cases above take its 128-row tiles
+    ([1, 15, 16, 17, 31, 33, 63, 64, 65, 127, 128, 129] + [0] * 36, 256, 2048, 6),
 ])
 def test_grouped_gemm_random(B, counts, N, Kd, seed, path):
     if path == "small" and Kd % 16:
