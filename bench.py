@@ -90,7 +90,7 @@ def parse():
                          "core (timed) and every output token compared with it; one JSON line")
     ap.add_argument("--ffn-path", default="auto", choices=["auto", "large", "small", "large_pair"],
                     help="grouped-GEMM kernels of the layer workloads (auto: small-batch "
-                         "kernels when T*K <= 64*E)")
+                         "kernels when T*K <= 128*E)")
     args = ap.parse_args()
     if args.config is not None:
         args.workload = wl.CONFIGS[args.config]
@@ -240,6 +240,21 @@ def layer_row_bytes(w, inp, R):
                    "as_moved": R * Nh * 4 + R * Nh * 2 + R * 4},
         "combine": {"int8_codes": comb, "as_moved": comb},
     }
+
+
+def row_kernel_fracs(row_bytes, prof, hbm_gbs):
+    """Each profiled row kernel's mean launch time and its two byte counts
+    (layer_row_bytes) against the HBM peak."""
+    out = {}
+    for name, nbytes in row_bytes.items():
+        if name not in prof:
+            continue
+        k_us = prof[name][1] / prof[name][0] * 1e3
+        out[name] = {"us": round(k_us, 3), "bytes_int8_codes": nbytes["int8_codes"],
+                     "bytes_as_moved": nbytes["as_moved"],
+                     "frac_int8_codes": nbytes["int8_codes"] / (k_us * 1e-6) / 1e9 / hbm_gbs,
+                     "frac_as_moved": nbytes["as_moved"] / (k_us * 1e-6) / 1e9 / hbm_gbs}
+    return out
 
 
 def max_over_ranks(v, dist, device=None):
@@ -561,16 +576,7 @@ class LayerPath:
         extra = {"ffn_path": "small" if small else ("large_pair" if sfx else "large"),
                  "gemm_tflops": {k: fl[k] / (prof[k][1] / prof[k][0] * 1e-3) / 1e12 for k in fl},
                  "status": self.B.read_device_status(self.ws)}
-        rows = {}
-        for k, by in layer_row_bytes(w, self.inp, R).items():
-            if k not in prof:
-                continue
-            us = prof[k][1] / prof[k][0] * 1e3
-            rows[k] = {"us": round(us, 3), "bytes_int8_codes": by["int8_codes"],
-                       "bytes_as_moved": by["as_moved"],
-                       "frac_int8_codes": by["int8_codes"] / (us * 1e-6) / 1e9 / pk["hbm_gbs"],
-                       "frac_as_moved": by["as_moved"] / (us * 1e-6) / 1e9 / pk["hbm_gbs"]}
-        extra["row_kernels"] = rows
+        extra["row_kernels"] = row_kernel_fracs(layer_row_bytes(w, self.inp, R), prof, pk["hbm_gbs"])
         step_bytes = None
         if small:
             # few rows per expert: reading the int8 weights of every expert that

@@ -52,6 +52,57 @@ def test_layer_row_bytes_by_hand():
     assert b["combine"] == {"int8_codes": comb, "as_moved": comb}
 
 
+class _FakeViews:
+    """Stands in for the binding in LayerPath.roofline: stage views held as
+    numpy arrays, a device status of 0."""
+
+    def __init__(self, offsets, counts):
+        import torch
+        self.v = {"expert_offsets": torch.tensor(offsets), "expert_token_nums": torch.tensor(counts)}
+
+    def stage_views(self, shape, ws):
+        return self.v
+
+    def read_device_status(self, ws):
+        return 0
+
+
+def _layer_path(w, counts):
+    p = bench.LayerPath.__new__(bench.LayerPath)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    p.B, p.w, p.shape, p.ws = _FakeViews(offsets, np.asarray(counts, np.int64)), w, None, None
+    p.inp = {"mask": None, "shared": None}
+    return p
+
+
+PK = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1700.0,
+      "source": "measured"}
+
+
+def test_layer_roofline_uses_the_dominant_kernels_own_time():
+    # large-tile path: GEMM1 dominates; the row kernels' times must not leak
+    # into its achieved rate
+    w = wl.custom(P=2, M=64, H=256, E=4, K=2, N=512)
+    p = _layer_path(w, [64, 64, 0, 128])
+    R = 256
+    prof = {"gemm1_swiglu_pair": (2, 2.0), "gemm2_dequant_pair": (2, 1.0),
+            "quant_scatter": (2, 0.02), "quant2": (2, 0.01), "combine": (2, 0.004)}
+    roof, _, extra = p.roofline(prof, PK)
+    assert roof["kernel"] == "gemm1_swiglu_pair"
+    flops = 2.0 * R * 256 * 512
+    assert roof["achieved"] == pytest.approx(flops / 1e-3 / 1e12)          # 1 ms per launch
+    assert roof["frac"] == pytest.approx(roof["achieved"] / 1700.0)
+    assert extra["row_kernels"]["combine"]["us"] == pytest.approx(2.0)
+    # small path: HBM-bound on the weights of the experts with rows
+    prof = {"gemm1_swiglu_small": (1, 0.5), "gemm2_dequant_small": (1, 0.25),
+            "quant_scatter": (1, 0.01), "combine": (1, 0.002)}
+    roof, _, extra = p.roofline(prof, PK)
+    by = 3 * 512 * 256 + R * 256 + R * 256 * 4
+    assert roof["kernel"] == "gemm1_swiglu_small"
+    assert roof["achieved"] == pytest.approx(by / 0.5e-3 / 1e9)
+    assert roof["frac"] < 1.0
+
+
 def test_whole_job_rate_is_weak_scaling():
     assert bench.whole_job_tokens_per_s(2048, 1, 0.1) == pytest.approx(2048 / 1e-4)
     assert bench.whole_job_tokens_per_s(2048, 4, 0.1) == pytest.approx(4 * 2048 / 1e-4)
