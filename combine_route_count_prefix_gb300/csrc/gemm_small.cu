@@ -26,9 +26,12 @@
 //                are split and added does not matter); warp 1 also owns TMEM
 //                (512 columns: the issuers' 256 accumulator columns and four
 //                64-column A stages)
-//   warp 2       row producer: the tile's rows (fp16 images, 128-byte swizzle)
-//                as 16-row TMA boxes, two 64-wide halves per k-block, into a
-//                4-stage ring
+//   warp 2       row producer: the tile's rows (fp16 images, 128-byte swizzle),
+//                one TB-row TMA box per 64-wide half of a k-block, into a
+//                4-stage ring; rows past the tile's (the next expert's, or zero
+//                fill past the row capacity) come along and are never read
+//                out: two large copies per k-block cost far less than one per
+//                16 rows present, whose count bounded the kernel
 //   warps 4..7   converters: thread (q, l) widens weight row 32 q + l of the
 //                tile (128 values) and writes it to its own TMEM lane (64
 //                columns, two fp16 values each)
@@ -62,8 +65,6 @@ constexpr int BKH = 64;                  // one 128-byte swizzle atom of fp16 ro
 constexpr int S8 = 4;                    // int8 weight ring stages
 constexpr int SA = 4;                    // operand stages: TMEM A + shared-memory rows
 constexpr int W8_BYTES = BW * BK;        // 16 KB
-constexpr int BOX_ROWS = 16;
-constexpr int BOX_BYTES = BOX_ROWS * BKH * 2;
 constexpr int CONV_WARP0 = 4;            // warps 4..7: TMEM lane quadrants 0..3
 constexpr int EPI_WARP0 = 8;
 constexpr int EPI_WARPS = 8;
@@ -86,7 +87,7 @@ struct SmallCfg {
     static constexpr int TB = TB_;
     static constexpr int NBUF = (int)ACC_COLS / TB;    // accumulators per issuer
     static constexpr int CHUNK_KB = TB == 64 ? 8 : 16;  // k-blocks per exact chunk
-    static constexpr int B_HALF_BYTES = TB * BKH * 2;   // one 64-wide half of the rows
+    static constexpr int B_HALF_BYTES = TB * BKH * 2;   // one 64-wide half of the rows: one TMA box
     static constexpr int B_BYTES = 2 * B_HALF_BYTES;
     static constexpr int EPI_COLS = TB / 2;             // tile rows per epilogue warp
     static constexpr size_t RING_BYTES = (size_t)SA * B_BYTES + (size_t)S8 * W8_BYTES;
@@ -312,15 +313,13 @@ k_gemm_small(const __grid_constant__ CUtensorMap tmRows, const __grid_constant__
             bool ok = true;
             for (int64_t tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
                 const Tile t = decode_tile<TB>(tile, p.n_wblocks, p.E, s_sched, s_off);
-                const int nbox = (t.rows + BOX_ROWS - 1) / BOX_ROWS;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!wait_bounded(&ab_empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&ab_full[stage], (uint32_t)(2 * nbox * BOX_BYTES));
+                    mbar_arrive_expect_tx(&ab_full[stage], (uint32_t)B_BYTES);
                     uint8_t *dst = ringB + (size_t)stage * B_BYTES;
                     for (int h = 0; h < 2; ++h)
-                        for (int i = 0; i < nbox; ++i)
-                            tma_load_2d(dst + h * B_HALF_BYTES + i * BOX_BYTES, &tmRows, &ab_full[stage],
-                                        kb * BK + h * BKH, t.row0 + i * BOX_ROWS);
+                        tma_load_2d(dst + h * B_HALF_BYTES, &tmRows, &ab_full[stage], kb * BK + h * BKH,
+                                    t.row0);
                     issued_phase[stage] = (int)phase;
                     if (++stage == SA) { stage = 0; phase ^= 1u; }
                 }
@@ -474,7 +473,7 @@ k_gemm_small(const __grid_constant__ CUtensorMap tmRows, const __grid_constant__
 
 template <int EPI, int TB>
 moe_status launch_small_tb(const CUtensorMap &mr, const CUtensorMap &mw, const SmallDev &d,
-                           cudaStream_t stream) {
+                           cudaStream_t stream) {   // mr: boxes of TB rows
     constexpr size_t smem = SmallCfg<TB>::SMEM_BYTES;
     if (!set_smem_limit((const void *)k_gemm_small<EPI, TB>, smem)) return MOE_ERR_CUDA;
     const char *names[3] = {"gemm_s32_small", "gemm1_swiglu_small", "gemm2_dequant_small"};
@@ -495,10 +494,13 @@ moe_status launch_grouped_gemm_small(Epi epi, const GemmArgs &a, cudaStream_t st
     if (a.cap_rows <= 0 || a.E <= 0) return MOE_OK;
     if (a.Kd % 16 != 0) return MOE_ERR_SHAPE;   // byte rows must be 16-byte strided for TMA
     if (epi == Epi::SwiGLU && a.Nout % 128 != 0) return MOE_ERR_SHAPE;
+    // the row capacity bounds the rows present: 64-row tiles while it averages
+    // at most 32 rows per expert, else 128-row tiles
+    const bool wide = a.cap_rows > kNarrowTileMaxRowsPerExpert * a.E;
     CUtensorMap mr, mw;
     const uint64_t rdims[2] = {(uint64_t)a.Kd, (uint64_t)a.cap_rows};
     const uint64_t rstr[1] = {(uint64_t)a.Kd * 2};
-    const uint32_t rbox[2] = {BKH, BOX_ROWS};
+    const uint32_t rbox[2] = {BKH, wide ? 128u : 64u};
     const uint64_t wdims[3] = {(uint64_t)a.Kd, (uint64_t)a.Nout, (uint64_t)a.E};
     const uint64_t wstr[2] = {(uint64_t)a.Kd, (uint64_t)a.Kd * a.Nout};
     const uint32_t wbox[3] = {BK, BW, 1};
@@ -524,9 +526,6 @@ moe_status launch_grouped_gemm_small(Epi epi, const GemmArgs &a, cudaStream_t st
     d.scale2 = a.scale2;
     d.s2 = a.s2;
     d.status = a.status;
-    // the row capacity bounds the rows present: 64-row tiles while it averages
-    // at most 32 rows per expert, else 128-row tiles
-    const bool wide = a.cap_rows > kNarrowTileMaxRowsPerExpert * a.E;
     switch (epi) {
         case Epi::S32: return launch_small_epi<(int)Epi::S32>(mr, mw, d, wide, stream);
         case Epi::SwiGLU: return launch_small_epi<(int)Epi::SwiGLU>(mr, mw, d, wide, stream);

@@ -113,7 +113,7 @@ typedef struct moe_shape {
  *          where no pair cluster fits.
  *   SMALL: the weights read as int8 (half the bytes), widened on chip into
  *          tensor memory as the MMA's 128-row side, against the expert's rows
- *          (only those present); for few rows per expert, where reading the
+ *          (the MMA's N); for few rows per expert, where reading the
  *          weights bounds the time ("PTO MegaMoE ...", Supported Cases: the M
  *          sweep from 16 tokens per rank).  Row tiles of 64 while the row
  *          capacity (T*K, or the rows of moe_grouped_gemm_s32's A) is at most
@@ -128,7 +128,7 @@ typedef struct moe_shape {
 #define MOE_FFN_PATH_SMALL 2
 #define MOE_FFN_PATH_LARGE_PAIR 3
 /* Any other ffn_path value returns MOE_ERR_PARAM_INVALID. */
-#define MOE_FFN_SMALL_ROWS_PER_EXPERT 64
+#define MOE_FFN_SMALL_ROWS_PER_EXPERT 128
 
 /* ------------------------------------------------------------------------
  * Dispatch.

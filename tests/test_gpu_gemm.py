@@ -5,8 +5,8 @@ images of the int8 values with fp32 accumulation and drains every 1024-deep K
 chunk to int32; the adversarial cases below reach the largest sums that
 chunking must keep exact.  All kernels are checked: "large" (128-row x
 256-channel tiles on fp16 weight images, one SM each), "large_pair" (256-row
-tiles on pairs of SMs) and "small" (int8 weights widened on chip, only the
-rows present loaded)."""
+tiles on pairs of SMs) and "small" (int8 weights widened on chip against
+64- or 128-row tiles of the expert's rows)."""
 import numpy as np
 import pytest
 import torch
