@@ -266,6 +266,34 @@ def test_large_prefill_full_size(B):
     assert ntok == 256 and nrows > 256 * 8
 
 
+@pytest.mark.parametrize("M,small", [(256, True), (260, False)])
+def test_auto_switches_at_the_rows_per_expert_limit(B, M, small):
+    """AUTO runs the small-batch kernels while T*K <= MOE_FFN_SMALL_ROWS_PER_EXPERT * E
+    (128 rows per expert) and the SM-pair kernels above; read from the
+    library's per-kernel profile."""
+    w = wl.custom(P=2, M=M, H=128, E=8, K=2, N=256)
+    T, P, H, E, K, N = (w.num_tokens, w.num_partitions, w.hidden, w.num_experts, w.topk, w.ffn)
+    assert (T * K <= 128 * E) == small
+    inp = wl.make_inputs(w, seed=13)
+    W1, S1, W2, S2 = wl.all_expert_weights(w, seed=13)
+    shape = B.make_shape(T, P, H, E, K, N)
+    (o1, w1p), (o2, w2p) = _device_weights(B, shape, W1, W2)
+    torch.cuda.synchronize()
+    B.profile_report()
+    B.profile_enable(True)
+    out, ws = B.layer(shape, dev_bf16(inp["x"]), dev(inp["ids"]), dev(inp["probs"]), w1p,
+                      dev(S1), w2p, dev(S2))
+    torch.cuda.synchronize()
+    B.profile_enable(False)
+    names = set(B.profile_report())
+    assert B.read_device_status(ws) == 0
+    if small:
+        assert {"gemm1_swiglu_small", "gemm2_dequant_small"} <= names, names
+    else:
+        assert {"gemm1_swiglu_pair", "gemm2_dequant_pair"} <= names, names
+    assert any(n.endswith("_small") for n in names) == small
+
+
 @pytest.mark.parametrize("path", ["auto", "large"])
 def test_small_batch_layer_every_token(B, path):
     """The smallest point of the tokens-per-rank sweep (8 x 16 tokens, 128
