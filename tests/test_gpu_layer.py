@@ -207,8 +207,9 @@ def _full_size_check(B, name, tokens_per_partition_out, seed=0, path="auto"):
     stages (q1, s1, g, q2, s2, y): sampled rows of every expert (first, last,
     one per 128-row block), computed by the oracle from the same inputs.
     Output: tokens spread over every partition, computed by the oracle token
-    by token through the whole layer."""
-    w = wl.WORKLOADS[name]
+    by token through the whole layer.  `name` is a workload's name or the
+    workload itself."""
+    w = wl.WORKLOADS[name] if isinstance(name, str) else name
     T, P, H, E, K, N = (w.num_tokens, w.num_partitions, w.hidden, w.num_experts, w.topk, w.ffn)
     M = w.tokens_per_partition
     inp = wl.make_inputs(w, seed=seed)
@@ -257,6 +258,21 @@ def test_full_layer_full_size(B):
     expert's 128-row blocks, and 512 output tokens (64 per partition)."""
     nrows, ntok = _full_size_check(B, "full_layer", tokens_per_partition_out=64)
     assert ntok == 512 and nrows > 128 * 8
+
+
+@pytest.mark.parametrize("M", [128, 256])
+def test_sweep_point_full_size(B, M):
+    """Points of the tokens-per-rank sweep that AUTO runs on the small-batch
+    kernels' 128-row tiles, at full H, E and N: 8 x 128 tokens (64 rows per
+    expert, one tile each) and 8 x 256 (128 per expert: about half the
+    experts span two tiles).  Sampled rows of every expert and 8 output
+    tokens per partition against the oracle."""
+    import dataclasses
+    w = dataclasses.replace(wl.WORKLOADS["full_layer"], name=f"full_layer_t{M}",
+                            tokens_per_partition=M)
+    assert w.num_tokens * w.topk <= 128 * w.num_experts      # AUTO: small-batch kernels
+    nrows, ntok = _full_size_check(B, w, tokens_per_partition_out=8)
+    assert ntok == 64 and nrows >= 2 * w.num_experts
 
 
 def test_large_prefill_full_size(B):
