@@ -118,6 +118,16 @@ def test_layer_many_partitions_unfused_routing(B, path):
     _stage_check(B, w, seed=3, path=path)
 
 
+@pytest.mark.parametrize("P,M", [(4, 64), (5, 512)])
+def test_layer_max_experts_small_batch_kernels(B, P, M):
+    """1024 experts, top-16 (the limits) on the small-batch kernels: 4 rows
+    per expert on average (64-row tiles) and 40 (128-row tiles), every stage
+    of every row against the oracle."""
+    w = wl.custom(P=P, M=M, H=64, E=1024, K=16, N=256, mask_kind=2, mask_p=0.9)
+    assert w.num_tokens * w.topk <= 128 * w.num_experts       # AUTO: small-batch kernels
+    _stage_check(B, w, seed=14, path="small")
+
+
 def test_layer_paths_agree_bit_for_bit(B):
     """Both GEMM kernels give the same g, q2, s2, y and output, bit for bit,
     with experts holding 0, a few, and more than 128 rows (two row blocks)."""
